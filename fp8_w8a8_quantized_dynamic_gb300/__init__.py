@@ -1,9 +1,213 @@
 """FP8 (e4m3fn) W8A8 linear with dynamic per-tensor activation quantization, for sm_103a.
 
-Placeholder binding; the C-ABI library and its loader follow.
+Thin ctypes binding over the C-ABI library libfp8w8a8.so (declared in include/fp8w8a8.h).
+The functions carry the C names. PyTorch supplies device memory and the current CUDA
+stream only; every step of the layer runs in the library's CUDA kernels. There is no CPU
+fallback: a missing library raises.
+
+Typical use::
+
+    qw, s_w = fp8_quantize_weight(w)                 # once, at load (per-tensor)
+    qw, s_w = fp8_quantize_weight(w, per_channel=True)
+    y = fp8_linear(a, qw, s_w, bias)                 # every forward; dynamic s_a
+    y = fp8_linear_channelwise(a, qw, s_w, bias)
 """
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+from ._build import LIB_PATH
+
+FP8_OK = 0
+FP8_ERR_INVALID_ARG = 1
+FP8_ERR_MISALIGNED = 2
+FP8_ERR_WORKSPACE = 3
+FP8_ERR_CUDA = 4
+FP8_ERR_TIMEOUT = 5
+FP8_ERR_UNSUPPORTED_DEVICE = 6
+FP8_QUANT_WORKSPACE_BYTES = 4352
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+_i64, _sz, _vp, _int = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int
+
+_SIGNATURES = {
+    "fp8_min_ld": (_i64, [_i64]),
+    "fp8_workspace_bytes": (_sz, [_i64, _i64, _i64]),
+    "fp8_uses_gemv": (_int, [_i64, _i64, _i64]),
+    "fp8_quantize_weight": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _i64, _vp, _vp, _sz, _vp]),
+    "fp8_quantize_act": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _sz, _vp]),
+    "fp8_scaled_mm": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _i64, _vp, _int, _vp, _vp, _i64, _vp]),
+    "fp8_linear": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _sz, _vp]),
+    "fp8_linear_channelwise": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _sz, _vp]),
+    "fp8_last_device_status": (_int, [_vp]),
+    "fp8_status_string": (ctypes.c_char_p, [_int]),
+}
+
+
+class FP8Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library; raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(f"FP8 CUDA library missing ({LIB_PATH}); build it with "
+                                       "fp8_w8a8_quantized_dynamic_gb300._build.build()")
+                L = ctypes.CDLL(LIB_PATH)
+                for name, (res, args) in _SIGNATURES.items():
+                    fn = getattr(L, name)
+                    fn.restype = res
+                    fn.argtypes = args
+                _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().fp8_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != FP8_OK:
+        raise FP8Error(status, where)
 
 
 def min_ld(K: int) -> int:
-    """Leading dimension (bytes) of the library's FP8 matrices: K rounded up to 16."""
-    return (int(K) + 15) // 16 * 16
+    """Leading dimension (bytes) of the library's FP8 matrices: K rounded up to 16 (16 for K == 0)."""
+    return (int(K) + 15) // 16 * 16 if K > 0 else 16
+
+
+# ---------------------------------------------------------------------------
+# torch-facing wrappers (torch is imported lazily: host-only users need none of it)
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(t) -> int:
+    return _torch().cuda.current_stream(t.device).cuda_stream
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _check_bf16_2d(t, name: str):
+    torch = _torch()
+    if t.dtype != torch.bfloat16 or t.dim() != 2 or t.stride(1) != 1 or not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA bf16 matrix with unit column stride")
+
+
+def _check_fp8_2d(t, K: int, name: str):
+    torch = _torch()
+    if t.dtype != torch.uint8 or t.dim() != 2 or t.stride(1) != 1 or not t.is_cuda or t.shape[1] < K:
+        raise ValueError(f"{name}: expected a CUDA uint8 [rows, ld >= K] matrix")
+
+
+def fp8_workspace_bytes(M: int, K: int, N: int) -> int:
+    return int(lib().fp8_workspace_bytes(M, K, N))
+
+
+def fp8_uses_gemv(M: int, K: int, N: int) -> bool:
+    return bool(lib().fp8_uses_gemv(M, K, N))
+
+
+def fp8_min_ld(K: int) -> int:
+    return int(lib().fp8_min_ld(K))
+
+
+def fp8_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def workspace(M: int, K: int, N: int, device):
+    """Allocate a workspace big enough for fp8_linear on [M, K] x [N, K] (and any quantize call)."""
+    torch = _torch()
+    return torch.empty(fp8_workspace_bytes(M, K, N), dtype=torch.uint8, device=device)
+
+
+def fp8_quantize_weight(w, per_channel: bool = False, ws=None) -> Tuple["torch.Tensor", "torch.Tensor"]:
+    """W bf16 [N, K] -> (qW uint8 [N, min_ld(K)], s_w fp32 [1] or [N])."""
+    torch = _torch()
+    _check_bf16_2d(w, "w")
+    N, K = w.shape
+    qw = torch.empty((N, min_ld(K)), dtype=torch.uint8, device=w.device)
+    s_w = torch.empty((N if per_channel else 1,), dtype=torch.float32, device=w.device)
+    if ws is None and not per_channel:
+        ws = torch.empty(FP8_QUANT_WORKSPACE_BYTES, dtype=torch.uint8, device=w.device)
+    _check(lib().fp8_quantize_weight(w.data_ptr(), N, K, w.stride(0), int(per_channel), qw.data_ptr(),
+                                     qw.stride(0), s_w.data_ptr(), _ptr(ws), 0 if ws is None else ws.numel(),
+                                     _stream_ptr(w)), "fp8_quantize_weight")
+    return qw, s_w
+
+
+def fp8_quantize_act(a, ws=None):
+    """A bf16 [M, K] -> (qA uint8 [M, min_ld(K)], s_a fp32 [1]) with s_a = amax(A)/448."""
+    torch = _torch()
+    _check_bf16_2d(a, "a")
+    M, K = a.shape
+    qa = torch.empty((M, min_ld(K)), dtype=torch.uint8, device=a.device)
+    s_a = torch.empty((1,), dtype=torch.float32, device=a.device)
+    if ws is None:
+        ws = torch.empty(FP8_QUANT_WORKSPACE_BYTES, dtype=torch.uint8, device=a.device)
+    _check(lib().fp8_quantize_act(a.data_ptr(), M, K, a.stride(0), qa.data_ptr(), qa.stride(0), s_a.data_ptr(),
+                                  ws.data_ptr(), ws.numel(), _stream_ptr(a)), "fp8_quantize_act")
+    return qa, s_a
+
+
+def fp8_scaled_mm(qa, K: int, s_a, qw, s_w, per_channel: bool = False, bias=None, out=None):
+    """Y = bf16(s_a * s_w * (qA @ qW^T) (+ bias)) on already-quantized operands."""
+    torch = _torch()
+    _check_fp8_2d(qa, K, "qa")
+    _check_fp8_2d(qw, K, "qw")
+    M, N = qa.shape[0], qw.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
+    _check(lib().fp8_scaled_mm(qa.data_ptr(), M, K, qa.stride(0), s_a.data_ptr(), qw.data_ptr(), N, qw.stride(0),
+                               s_w.data_ptr(), int(per_channel), _ptr(bias), y.data_ptr(), y.stride(0),
+                               _stream_ptr(qa)), "fp8_scaled_mm")
+    return y
+
+
+def _linear(fn_name: str, a, qw, s_w, bias, out, ws):
+    torch = _torch()
+    _check_bf16_2d(a, "a")
+    M, K = a.shape
+    _check_fp8_2d(qw, K, "qw")
+    N = qw.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    if ws is None:
+        ws = workspace(M, K, N, a.device)
+    fn = getattr(lib(), fn_name)
+    _check(fn(a.data_ptr(), M, K, a.stride(0), qw.data_ptr(), N, qw.stride(0), s_w.data_ptr(), _ptr(bias),
+              y.data_ptr(), y.stride(0), ws.data_ptr(), ws.numel(), _stream_ptr(a)), fn_name)
+    return y
+
+
+def fp8_linear(a, qw, s_w, bias=None, out=None, ws=None):
+    """Dynamic W8A8 linear, per-tensor weight scale s_w [1]: Y = A W^T (+ bias), bf16 out."""
+    return _linear("fp8_linear", a, qw, s_w, bias, out, ws)
+
+
+def fp8_linear_channelwise(a, qw, s_w, bias=None, out=None, ws=None):
+    """Dynamic W8A8 linear, per-output-channel weight scales s_w [N]."""
+    return _linear("fp8_linear_channelwise", a, qw, s_w, bias, out, ws)
+
+
+def fp8_last_device_status(stream=None) -> int:
+    """Synchronizes the stream; returns FP8_OK or the device-side error the kernels recorded."""
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    return int(lib().fp8_last_device_status(s))

@@ -1,0 +1,397 @@
+// C ABI of the FP8 W8A8 linear (declared in include/fp8w8a8.h): argument validation,
+// M-based dispatch between the decode GEMV and the tcgen05 GEMM, launch configuration.
+// Every step of the layer runs in this library's kernels; nothing falls back to the CPU.
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "fp8w8a8.h"
+#include "device_common.cuh"
+#include "gemm_tcgen05.h"
+#include "gemv.cuh"
+#include "quantize.cuh"
+
+#define FP8_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+using namespace fp8k;
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+constexpr int kGemvMaxK = gemv::kMaxCluster * gemv::kMaxSlice;  // 32768
+
+// ---------------------------------------------------------------------------
+// device properties (cached per device)
+// ---------------------------------------------------------------------------
+
+struct DevInfo {
+  int checked = 0;
+  int supported = 0;
+  int sms = 0;
+};
+
+std::mutex g_dev_mu;
+DevInfo g_dev[64];
+
+fp8_status current_device(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.checked) {
+    int major = 0, minor = 0, n = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FP8_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3);
+    d.sms = n;
+    d.checked = 1;
+  }
+  if (!d.supported) return FP8_ERR_UNSUPPORTED_DEVICE;
+  *sms = d.sms;
+  return FP8_OK;
+}
+
+int gemv_max_m() {
+  static const int v = [] {
+    const char* e = std::getenv("FP8W8A8_GEMV_MAX_M");
+    int x = e ? std::atoi(e) : gemv::kMaxTokens;
+    return std::max(0, std::min(x, gemv::kMaxTokens));
+  }();
+  return v;
+}
+
+bool use_gemv(int64_t M, int64_t K) { return M <= gemv_max_m() && K <= kGemvMaxK; }
+
+int64_t round_up16(int64_t k) { return (k + 15) / 16 * 16; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---------------------------------------------------------------------------
+// launch helpers
+// ---------------------------------------------------------------------------
+
+template <typename... KArgs, typename... Args>
+fp8_status launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                  dim3 cluster, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster.x * cluster.y * cluster.z > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster.x;
+    attr[n].val.clusterDim.y = cluster.y;
+    attr[n].val.clusterDim.z = cluster.z;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+struct BF16Mat {
+  const uint16_t* p;
+  int64_t rows, cols, ld;
+  int contiguous() const { return ld == cols && aligned(p, 16); }
+  int vec() const { return aligned(p, 16) && ld % 8 == 0; }
+};
+
+int amax_grid(const BF16Mat& a, int sms) {
+  const int64_t units = (a.rows * a.cols + 7) / 8;
+  const int64_t per_block = int64_t(kQuantThreads) * 4;
+  int64_t g = (units + per_block - 1) / per_block;
+  g = std::min<int64_t>(g, std::min<int64_t>(kAmaxMaxBlocks, int64_t(sms) * 8));
+  return int(std::max<int64_t>(g, 1));
+}
+
+fp8_status launch_amax(const BF16Mat& a, float* partials, int grid, cudaStream_t st, bool pdl) {
+  return launch(amax_partials_kernel, dim3(grid), dim3(kQuantThreads), 0, st, pdl, dim3(1, 1, 1), a.p, a.rows,
+                a.cols, a.ld, a.contiguous(), a.vec(), partials, int(pdl));
+}
+
+fp8_status launch_cast(const BF16Mat& a, const float* partials, int n_partials, float* s_out, uint8_t* q,
+                       int64_t ldq, int sms, cudaStream_t st, bool pdl) {
+  const int64_t units = a.rows * (ldq / 16);
+  const int64_t g = std::max<int64_t>(1, std::min<int64_t>((units + kQuantThreads - 1) / kQuantThreads,
+                                                           int64_t(sms) * 8));
+  if (units < (int64_t(1) << 31))
+    return launch(cast_kernel<uint32_t>, dim3(unsigned(g)), dim3(kQuantThreads), 0, st, pdl, dim3(1, 1, 1), a.p,
+                  a.rows, a.cols, a.ld, a.vec(), partials, n_partials, s_out, q, ldq, int(pdl));
+  return launch(cast_kernel<uint64_t>, dim3(unsigned(g)), dim3(kQuantThreads), 0, st, pdl, dim3(1, 1, 1), a.p,
+                a.rows, a.cols, a.ld, a.vec(), partials, n_partials, s_out, q, ldq, int(pdl));
+}
+
+fp8_status launch_fill_bias(const void* bias, void* y, int64_t M, int64_t N, int64_t ldy, int sms, cudaStream_t st) {
+  const int64_t total = M * N;
+  const int64_t g = std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, int64_t(sms) * 8));
+  return launch(fill_bias_kernel, dim3(unsigned(g)), dim3(256), 0, st, true, dim3(1, 1, 1),
+                static_cast<const uint16_t*>(bias), static_cast<uint16_t*>(y), M, N, ldy, 1);
+}
+
+template <int NT, bool kDyn>
+fp8_status launch_gemv_t(const gemv::Params& p, dim3 grid, int cluster_y, size_t smem, cudaStream_t st) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    const size_t max_smem = size_t(NT) * 8 * (gemv::kMaxSlice + 64) + gemv::kRowsPerCta * gemv::kMaxTokens * 4;
+    if (cudaFuncSetAttribute(gemv::gemv_kernel<NT, kDyn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(max_smem)) != cudaSuccess)
+      return FP8_ERR_CUDA;
+    attr_done = true;
+  }
+  return launch(gemv::gemv_kernel<NT, kDyn>, grid, dim3(gemv::kThreads), smem, st, true, dim3(1, cluster_y, 1), p);
+}
+
+// Split-K GEMV: a 128-row block per cluster, its K split over up to 8 CTAs so that the grid
+// is about two CTAs deep per SM, each CTA keeping >= 4 chunks (256 bytes) of K.
+fp8_status launch_gemv(gemv::Params p, bool dynamic, int sms, cudaStream_t st) {
+  const int row_blocks = (p.N + gemv::kRowsPerCta - 1) / gemv::kRowsPerCta;
+  const int kchunks = int((round_up16(p.K) + gemv::kChunk - 1) / gemv::kChunk);
+  const int max_slice_chunks = gemv::kMaxSlice / gemv::kChunk;
+  int S = std::max(1, std::min(gemv::kMaxCluster, (2 * sms + row_blocks - 1) / row_blocks));
+  S = std::min(S, std::max(1, kchunks / 4));
+  S = std::max(S, (kchunks + max_slice_chunks - 1) / max_slice_chunks);
+  const int slice_chunks = std::max(1, (kchunks + S - 1) / S);
+  S = std::max(1, (kchunks + slice_chunks - 1) / slice_chunks);  // no CTA without work
+  p.kslice = slice_chunks * gemv::kChunk;
+  p.act_stride = (p.kslice % 128 == 0) ? p.kslice + 64 : p.kslice;
+  const int NT = p.M <= 8 ? 1 : 2;
+  const size_t smem = size_t(NT) * 8 * p.act_stride + gemv::kRowsPerCta * gemv::kMaxTokens * 4;
+  const dim3 grid(row_blocks, S);
+  if (NT == 1)
+    return dynamic ? launch_gemv_t<1, true>(p, grid, S, smem, st) : launch_gemv_t<1, false>(p, grid, S, smem, st);
+  return dynamic ? launch_gemv_t<2, true>(p, grid, S, smem, st) : launch_gemv_t<2, false>(p, grid, S, smem, st);
+}
+
+// ---------------------------------------------------------------------------
+// validation
+// ---------------------------------------------------------------------------
+
+fp8_status check_bf16_mat(const void* p, int64_t rows, int64_t cols, int64_t ld) {
+  if (rows < 0 || cols < 0 || rows > kMaxDim || cols > kMaxDim) return FP8_ERR_INVALID_ARG;
+  if (ld < std::max<int64_t>(cols, 1)) return FP8_ERR_INVALID_ARG;
+  if (rows > 0 && cols > 0 && p == nullptr) return FP8_ERR_INVALID_ARG;
+  if (!aligned(p, 2)) return FP8_ERR_MISALIGNED;
+  return FP8_OK;
+}
+
+fp8_status check_fp8_mat(const void* p, int64_t rows, int64_t cols, int64_t ld) {
+  if (rows < 0 || cols < 0 || rows > kMaxDim || cols > kMaxDim) return FP8_ERR_INVALID_ARG;
+  if (ld < std::max<int64_t>(round_up16(cols), 16)) return FP8_ERR_INVALID_ARG;
+  if (ld % FP8_LD_ALIGN != 0) return FP8_ERR_MISALIGNED;
+  if (rows > 0 && p == nullptr) return FP8_ERR_INVALID_ARG;
+  if (!aligned(p, 16)) return FP8_ERR_MISALIGNED;
+  return FP8_OK;
+}
+
+fp8_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
+  if (need == 0) return FP8_OK;
+  if (ws == nullptr || ws_bytes < need) return FP8_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return FP8_ERR_WORKSPACE;
+  return FP8_OK;
+}
+
+#define FP8_TRY(expr)                  \
+  do {                                 \
+    const fp8_status _s = (expr);      \
+    if (_s != FP8_OK) return _s;       \
+  } while (0)
+
+size_t linear_ws_bytes(int64_t M, int64_t K) {
+  size_t b = FP8_QUANT_WORKSPACE_BYTES;
+  if (M > 0 && K > 0 && !use_gemv(M, K)) b += size_t(M) * size_t(round_up16(K));
+  return b;
+}
+
+fp8_status linear_impl(const void* a, int64_t M, int64_t K, int64_t lda, const uint8_t* qw, int64_t N,
+                       int64_t ldqw, const float* s_w, int per_channel, const void* bias, void* y, int64_t ldy,
+                       void* ws, size_t ws_bytes, fp8_stream_t stream) {
+  FP8_TRY(check_bf16_mat(a, M, K, lda));
+  FP8_TRY(check_fp8_mat(qw, N, K, ldqw));
+  FP8_TRY(check_bf16_mat(y, M, N, ldy));
+  if (N > 0 && s_w == nullptr) return FP8_ERR_INVALID_ARG;
+  if (!aligned(bias, 2)) return FP8_ERR_MISALIGNED;
+  if (M == 0 || N == 0) return FP8_OK;
+  FP8_TRY(check_ws(ws, ws_bytes, linear_ws_bytes(M, K)));
+  int sms = 0;
+  FP8_TRY(current_device(&sms));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return launch_fill_bias(bias, y, M, N, ldy, sms, st);
+
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* partials = reinterpret_cast<float*>(wsb);
+  float* s_a = reinterpret_cast<float*>(wsb + kWsScaleOffset);
+  const BF16Mat A{static_cast<const uint16_t*>(a), M, K, lda};
+  const int g = amax_grid(A, sms);
+  FP8_TRY(launch_amax(A, partials, g, st, true));
+
+  if (use_gemv(M, K)) {
+    gemv::Params p = {};
+    p.a = a;
+    p.lda = lda;
+    p.partials = partials;
+    p.n_partials = g;
+    p.qw = qw;
+    p.ldqw = ldqw;
+    p.s_w = s_w;
+    p.per_channel = per_channel;
+    p.bias = static_cast<const uint16_t*>(bias);
+    p.y = static_cast<uint16_t*>(y);
+    p.ldy = ldy;
+    p.M = int(M);
+    p.N = int(N);
+    p.K = int(K);
+    p.vec_a = A.vec();
+    return launch_gemv(p, true, sms, st);
+  }
+  uint8_t* qa = wsb + kWsQaOffset;
+  const int64_t ldqa = round_up16(K);
+  FP8_TRY(launch_cast(A, partials, g, s_a, qa, ldqa, sms, st, true));
+  if (gemm_launch(qa, ldqa, s_a, qw, ldqw, s_w, per_channel, static_cast<const uint16_t*>(bias),
+                  static_cast<uint16_t*>(y), ldy, int(M), int(N), int(K), sms, st) != 0)
+    return FP8_ERR_CUDA;
+  return FP8_OK;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// exported C ABI
+// ---------------------------------------------------------------------------
+
+FP8_API int64_t fp8_min_ld(int64_t K) { return K <= 0 ? 16 : round_up16(K); }
+
+FP8_API size_t fp8_workspace_bytes(int64_t M, int64_t K, int64_t N) {
+  (void)N;
+  return linear_ws_bytes(std::max<int64_t>(M, 0), std::max<int64_t>(K, 0));
+}
+
+FP8_API int fp8_uses_gemv(int64_t M, int64_t K, int64_t N) {
+  (void)N;
+  return use_gemv(M, K) ? 1 : 0;
+}
+
+FP8_API fp8_status fp8_quantize_weight(const void* w_bf16, int64_t N, int64_t K, int64_t ldw, int per_channel,
+                                       uint8_t* qw, int64_t ldq, float* s_w, void* ws, size_t ws_bytes,
+                                       fp8_stream_t stream) {
+  FP8_TRY(check_bf16_mat(w_bf16, N, K, ldw));
+  FP8_TRY(check_fp8_mat(qw, N, K, ldq));
+  if (per_channel != 0 && per_channel != 1) return FP8_ERR_INVALID_ARG;
+  if (s_w == nullptr) return FP8_ERR_INVALID_ARG;
+  if (!per_channel) FP8_TRY(check_ws(ws, ws_bytes, FP8_QUANT_WORKSPACE_BYTES));
+  if (per_channel && N == 0) return FP8_OK;
+  int sms = 0;
+  FP8_TRY(current_device(&sms));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const BF16Mat W{static_cast<const uint16_t*>(w_bf16), N, K, ldw};
+  // Weight kernels never trigger programmatic launch early: a following linear call may
+  // read qW before its own wait (see the header's launch-ordering note).
+  if (per_channel) {
+    const int g = int(std::min<int64_t>(N, int64_t(sms) * 8));
+    return launch(quantize_rows_kernel, dim3(g), dim3(kQuantThreads), 0, st, false, dim3(1, 1, 1), W.p, N, K, ldw,
+                  W.vec(), qw, ldq, s_w);
+  }
+  float* partials = static_cast<float*>(ws);
+  const int g = amax_grid(W, sms);
+  FP8_TRY(launch_amax(W, partials, g, st, false));
+  return launch_cast(W, partials, g, s_w, qw, ldq, sms, st, false);
+}
+
+FP8_API fp8_status fp8_quantize_act(const void* a_bf16, int64_t M, int64_t K, int64_t lda, uint8_t* qa, int64_t ldq,
+                                    float* s_a, void* ws, size_t ws_bytes, fp8_stream_t stream) {
+  FP8_TRY(check_bf16_mat(a_bf16, M, K, lda));
+  FP8_TRY(check_fp8_mat(qa, M, K, ldq));
+  if (s_a == nullptr) return FP8_ERR_INVALID_ARG;
+  FP8_TRY(check_ws(ws, ws_bytes, FP8_QUANT_WORKSPACE_BYTES));
+  int sms = 0;
+  FP8_TRY(current_device(&sms));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const BF16Mat A{static_cast<const uint16_t*>(a_bf16), M, K, lda};
+  float* partials = static_cast<float*>(ws);
+  const int g = amax_grid(A, sms);
+  FP8_TRY(launch_amax(A, partials, g, st, true));
+  return launch_cast(A, partials, g, s_a, qa, ldq, sms, st, true);
+}
+
+FP8_API fp8_status fp8_scaled_mm(const uint8_t* qa, int64_t M, int64_t K, int64_t ldqa, const float* s_a,
+                                 const uint8_t* qw, int64_t N, int64_t ldqw, const float* s_w, int per_channel,
+                                 const void* bias_bf16, void* y_bf16, int64_t ldy, fp8_stream_t stream) {
+  FP8_TRY(check_fp8_mat(qa, M, K, ldqa));
+  FP8_TRY(check_fp8_mat(qw, N, K, ldqw));
+  FP8_TRY(check_bf16_mat(y_bf16, M, N, ldy));
+  if (per_channel != 0 && per_channel != 1) return FP8_ERR_INVALID_ARG;
+  if (M > 0 && N > 0 && (s_a == nullptr || s_w == nullptr)) return FP8_ERR_INVALID_ARG;
+  if (!aligned(bias_bf16, 2)) return FP8_ERR_MISALIGNED;
+  if (M == 0 || N == 0) return FP8_OK;
+  int sms = 0;
+  FP8_TRY(current_device(&sms));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return launch_fill_bias(bias_bf16, y_bf16, M, N, ldy, sms, st);
+  if (use_gemv(M, K)) {
+    gemv::Params p = {};
+    p.a = qa;
+    p.lda = ldqa;
+    p.s_a = s_a;
+    p.qw = qw;
+    p.ldqw = ldqw;
+    p.s_w = s_w;
+    p.per_channel = per_channel;
+    p.bias = static_cast<const uint16_t*>(bias_bf16);
+    p.y = static_cast<uint16_t*>(y_bf16);
+    p.ldy = ldy;
+    p.M = int(M);
+    p.N = int(N);
+    p.K = int(K);
+    return launch_gemv(p, false, sms, st);
+  }
+  if (fp8k::gemm_launch(qa, ldqa, s_a, qw, ldqw, s_w, per_channel, static_cast<const uint16_t*>(bias_bf16),
+                        static_cast<uint16_t*>(y_bf16), ldy, int(M), int(N), int(K), sms, st) != 0)
+    return FP8_ERR_CUDA;
+  return FP8_OK;
+}
+
+FP8_API fp8_status fp8_linear(const void* a_bf16, int64_t M, int64_t K, int64_t lda, const uint8_t* qw, int64_t N,
+                              int64_t ldqw, const float* s_w, const void* bias_bf16, void* y_bf16, int64_t ldy,
+                              void* ws, size_t ws_bytes, fp8_stream_t stream) {
+  return linear_impl(a_bf16, M, K, lda, qw, N, ldqw, s_w, 0, bias_bf16, y_bf16, ldy, ws, ws_bytes, stream);
+}
+
+FP8_API fp8_status fp8_linear_channelwise(const void* a_bf16, int64_t M, int64_t K, int64_t lda, const uint8_t* qw,
+                                          int64_t N, int64_t ldqw, const float* s_w, const void* bias_bf16,
+                                          void* y_bf16, int64_t ldy, void* ws, size_t ws_bytes,
+                                          fp8_stream_t stream) {
+  return linear_impl(a_bf16, M, K, lda, qw, N, ldqw, s_w, 1, bias_bf16, y_bf16, ldy, ws, ws_bytes, stream);
+}
+
+FP8_API fp8_status fp8_last_device_status(fp8_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8_ERR_CUDA;
+  const unsigned int e = fp8k::gemm_read_and_clear_error();
+  if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
+  return (e & kErrTimeout) ? FP8_ERR_TIMEOUT : FP8_OK;
+}
+
+FP8_API const char* fp8_status_string(fp8_status s) {
+  switch (s) {
+    case FP8_OK: return "FP8_OK";
+    case FP8_ERR_INVALID_ARG: return "FP8_ERR_INVALID_ARG";
+    case FP8_ERR_MISALIGNED: return "FP8_ERR_MISALIGNED";
+    case FP8_ERR_WORKSPACE: return "FP8_ERR_WORKSPACE";
+    case FP8_ERR_CUDA: return "FP8_ERR_CUDA";
+    case FP8_ERR_TIMEOUT: return "FP8_ERR_TIMEOUT";
+    case FP8_ERR_UNSUPPORTED_DEVICE: return "FP8_ERR_UNSUPPORTED_DEVICE";
+  }
+  return "FP8_ERR_UNKNOWN";
+}

@@ -1,0 +1,163 @@
+// Device helpers shared by the library's kernels (sm_103a).
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+
+namespace fp8k {
+
+constexpr float kE4M3Max = 448.0f;      // largest finite float8_e4m3fn value
+constexpr int kAmaxMaxBlocks = 1024;    // partial-amax slots in a workspace
+constexpr size_t kWsScaleOffset = 4096; // workspace: fp32 activation scale after the partials
+constexpr size_t kWsQaOffset = 4352;    // workspace: quantized activations (256-byte aligned)
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded device waits: 2 s
+
+// Device error bits (ORed into a per-module word, read by fp8_last_device_status).
+constexpr unsigned int kErrTimeout = 1u;
+
+// ---------------------------------------------------------------------------
+// Quantization arithmetic: q = e4m3(fp32(x / s)), saturating RNE.
+// ---------------------------------------------------------------------------
+
+// Two fp32 -> packed e4m3fn pair (round to nearest even, saturate to +-448; NaN stays NaN).
+// `lo` lands in bits 0..7, `hi` in bits 8..15.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Four values -> four e4m3fn bytes (x0 in the lowest byte). The quotient is the IEEE
+// round-to-nearest fp32 division, independent of compiler flags.
+__device__ __forceinline__ uint32_t quant4(float x0, float x1, float x2, float x3, float s) {
+  const uint32_t lo = cvt_e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+  const uint32_t hi = cvt_e4m3x2(__fdiv_rn(x2, s), __fdiv_rn(x3, s));
+  return lo | (hi << 16);
+}
+
+// Eight bf16 (packed in a uint4) -> eight e4m3fn bytes (uint2).
+__device__ __forceinline__ uint2 quant8_bf16(uint4 v, float s) {
+  auto f = [](uint32_t w, int hi) { return __uint_as_float(hi ? (w & 0xFFFF0000u) : (w << 16)); };
+  uint2 r;
+  r.x = quant4(f(v.x, 0), f(v.x, 1), f(v.y, 0), f(v.y, 1), s);
+  r.y = quant4(f(v.z, 0), f(v.z, 1), f(v.w, 0), f(v.w, 1), s);
+  return r;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+
+// scale = amax / 448 (IEEE fp32 division); 1 when amax is 0 (or the quotient underflows).
+__device__ __forceinline__ float scale_from_amax(float amax) {
+  const float s = __fdiv_rn(amax, kE4M3Max);
+  return s == 0.0f ? 1.0f : s;
+}
+
+// max |x| of the bf16 pairs in a 32-bit word, as two 16-bit magnitudes (sign bits cleared).
+__device__ __forceinline__ uint32_t abs_max_u16x2(uint32_t acc, uint32_t w) {
+  return __vmaxu2(acc, w & 0x7FFF7FFFu);
+}
+
+__device__ __forceinline__ float u16x2_max_to_float(uint32_t m2) {
+  const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+  return __uint_as_float(m << 16);
+}
+
+// ---------------------------------------------------------------------------
+// Loads / reductions
+// ---------------------------------------------------------------------------
+
+// Streaming 16-byte load (read-only path, no L1 allocation).
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Max over n non-negative partial amax values, by the whole block; result broadcast to all
+// threads. `red` must hold blockDim.x/32 floats.
+__device__ __forceinline__ float block_max_partials(const float* __restrict__ partials, int n, float* red) {
+  float m = 0.0f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, partials[i]);
+  m = warp_max(m);
+  const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  __syncthreads();  // `red` may still be in use by a previous reduction
+  if ((threadIdx.x & 31) == 0) red[w] = m;
+  __syncthreads();
+  m = 0.0f;
+  for (int i = 0; i < nw; ++i) m = fmaxf(m, red[i]);
+  return m;
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch
+// ---------------------------------------------------------------------------
+
+// Let the next kernel in the stream start launching; it still waits (pdl_wait) for our completion.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Wait until the preceding kernel in the stream has completed and its writes are visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete. Gives up (returns false) when
+// *abort_flag becomes non-zero or after kWaitLimitNs; on a timeout it raises the abort
+// flag and ORs kErrTimeout into *err so the host can report it. Never spins unbounded.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag, unsigned int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15u) == 0) {
+      if (abort_flag != nullptr && *abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (abort_flag != nullptr) *abort_flag = 1;
+        atomicOr(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+
+}  // namespace fp8k

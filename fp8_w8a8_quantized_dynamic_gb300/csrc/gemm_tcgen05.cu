@@ -1,0 +1,414 @@
+// Prefill FP8 GEMM for sm_103a on the 5th-generation tensor cores.
+//
+//   Y[m, n] = bf16( s_a * s_w[n] * sum_k qA[m, k] qW[n, k]  (+ bias[n]) )
+//
+// The W8A8 product the pages run through torch._scaled_mm / CUTLASS ("Prototype FP8Linear
+// W8A8 runtime quantization"; "[Kernel] Implement fallback for FP8 channelwise using
+// torch._scaled_mm"), with the channelwise rescale s_a*s_w[n] applied to the fp32
+// accumulator in the epilogue: (s_a A)(s_w,n W_n)^T = s_a s_w,n (A W_n^T).
+//
+// Structure (one CTA per SM, persistent over output tiles of 128 x 256):
+//   warp 0      TMA producer: qA tile [128 x 128B] and qW tile [256 x 128B] per stage into a
+//               4-stage ring of 128B-swizzled shared memory, completion on an mbarrier.
+//   warp 1      TMEM allocator + MMA issuer: tcgen05.mma.cta_group::1.kind::f8f6f4,
+//               M=128 N=256 K=32, fp32 accumulators in TMEM, two accumulator buffers of 256
+//               columns so the epilogue of tile i overlaps the main loop of tile i+1.
+//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, scale (+bias), bf16, store.
+// Ragged M, N and K need no padding: TMA fills out-of-range rows/columns with zeros and
+// the epilogue predicates its stores.
+//
+// Every wait is bounded (2 s); on expiry the kernel records an error for the host, drains
+// its own outstanding copies and MMAs (again bounded), frees its TMEM and returns.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "device_common.cuh"
+#include "gemm_tcgen05.h"
+
+namespace fp8k {
+namespace gemm {
+
+__device__ unsigned int g_gemm_error;
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;  // bytes (= e4m3 elements) of K per stage: one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kAccBufs = 2;
+constexpr int kTmemCols = kAccBufs * BN;  // 512: the whole tensor memory of the SM
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr uint32_t kABytes = BM * BK;
+constexpr uint32_t kBBytes = BN * BK;
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr int kMmaK = 32;  // K of one kind::f8f6f4 MMA
+
+struct SharedCtl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[kAccBufs];
+  uint64_t tempty[kAccBufs];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  float colscale[kAccBufs][BN];
+  float colbias[kAccBufs][BN];
+};
+
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + sizeof(SharedCtl);
+
+// Instruction descriptor, kind::f8f6f4: D fp32 (bits 4-5 = 1), A and B e4m3 (bits 7-9, 10-12 = 0),
+// both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+
+// Shared-memory matrix descriptor for a K-major operand tile written by TMA with 128-byte
+// swizzle: rows of 128 bytes, 8-row swizzle atoms of 1024 bytes (stride byte offset), start
+// address >> 4 in bits 0-13, descriptor version 1 at bit 46, swizzle mode 2 (128B) at bits 61-63.
+// The leading byte offset is unused for swizzled K-major layouts (set to 1).
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr & 0x3FFFFu) >> 4);
+  d |= uint64_t(1) << 16;
+  d |= uint64_t(1024 >> 4) << 32;
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(2) << 61;
+  return d;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y) : "memory");
+}
+
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Named barrier over the 128 epilogue threads that also ORs a flag across them, so every
+// epilogue warp takes the same exit decision.
+__device__ __forceinline__ bool epi_bar_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r) : "r"(uint32_t(v)), "n"(kEpiThreads) : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+         (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+
+// Tile order: groups of `group_n` column tiles; inside a group the column index runs
+// fastest, so the CTAs resident at one time share a few A row blocks and a W slice that
+// stays in L2 while the group sweeps all rows.
+__device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& m_idx, int& n_idx) {
+  const int per_group = p.group_n * p.m_tiles;
+  const int gidx = tile / per_group;
+  const int r = tile - gidx * per_group;
+  const int n_first = gidx * p.group_n;
+  const int gn = min(p.group_n, p.n_tiles - n_first);
+  m_idx = r / gn;
+  n_idx = n_first + (r - m_idx * gn);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+            const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-aligned for the 128B swizzle
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + kStages * kStageBytes);
+  const uint32_t smem_base = smem_u32(smem);
+  auto a_stage = [&](int s) { return smem_base + s * kStageBytes; };
+  auto b_stage = [&](int s) { return smem_base + s * kStageBytes + kABytes; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_tiles = p.m_tiles * p.n_tiles;
+  const int num_kb = (p.K + BK - 1) / BK;
+  volatile int* abort_flag = &ctl->abort_flag;
+
+  if (threadIdx.x == 0) {
+    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    for (int b = 0; b < kAccBufs; ++b) {
+      mbar_init(smem_u32(&ctl->tfull[b]), 1);
+      mbar_init(smem_u32(&ctl->tempty[b]), kEpiThreads);
+    }
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_u32(&ctl->tmem_base)), "n"(kTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tmem_fence_before();
+  __syncthreads();
+  tmem_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  pdl_trigger();
+  pdl_wait();  // qA / s_a come from the preceding kernel; Y may still be read by it
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        int m_idx, n_idx;
+        tile_coords(tile, p, m_idx, n_idx);
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1u;
+          if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, &g_gemm_error)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&ctl->full[s]);
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          tma_load_2d(a_stage(s), &tmap_a, fb, kb * BK, m_idx * BM);
+          tma_load_2d(b_stage(s), &tmap_b, fb, kb * BK, n_idx * BN);
+        }
+      }
+      if (!ok) {
+        // drain: the last fill of every stage must land before the CTA's memory is released
+        const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0u;
+        for (uint32_t j = first; j < it; ++j)
+          mbar_wait_bounded(smem_u32(&ctl->full[j % kStages]), (j / kStages) & 1u, nullptr, &g_gemm_error);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      uint32_t it = 0, acc_it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++acc_it) {
+        const int ab = acc_it % kAccBufs;
+        const uint32_t aph = (acc_it / kAccBufs) & 1u;
+        if (!mbar_wait_bounded(smem_u32(&ctl->tempty[ab]), aph ^ 1u, abort_flag, &g_gemm_error)) { ok = false; break; }
+        tmem_fence_after();
+        const uint32_t d_tmem = tmem_base + ab * BN;
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1u;
+          if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, &g_gemm_error)) { ok = false; break; }
+          tmem_fence_after();
+          const uint64_t adesc = make_sdesc(a_stage(s));
+          const uint64_t bdesc = make_sdesc(b_stage(s));
+#pragma unroll
+          for (int kk = 0; kk < BK / kMmaK; ++kk) {
+            // advance the start address by 32 bytes of K inside the swizzled 128-byte row
+            mma_f8(d_tmem, adesc + uint64_t(kk * kMmaK >> 4), bdesc + uint64_t(kk * kMmaK >> 4),
+                   (kb | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&ctl->empty[s]));  // frees the stage once these MMAs have read it
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&ctl->tfull[ab]));   // accumulator ready for the epilogue
+      }
+      // all MMAs issued by this thread must finish before TMEM is released
+      mma_commit(smem_u32(&ctl->drain));
+      mbar_wait_bounded(smem_u32(&ctl->drain), 0, nullptr, &g_gemm_error);
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5 ----------------
+    const int q = warp & 3;                    // TMEM lane quarter this warp may access
+    const int row_in_tile = q * 32 + lane;
+    const int et = threadIdx.x - 64;           // 0..127
+    const float s_a = *p.s_a;
+    uint32_t acc_it = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++acc_it) {
+      int m_idx, n_idx;
+      tile_coords(tile, p, m_idx, n_idx);
+      const int ab = acc_it % kAccBufs;
+      const uint32_t aph = (acc_it / kAccBufs) & 1u;
+      // column scales/bias of this tile, double-buffered by accumulator: a warp can only
+      // rewrite buffer ab after every epilogue warp passed the barrier of the tile between.
+      for (int j = et; j < BN; j += kEpiThreads) {
+        const int n = n_idx * BN + j;
+        float sc = 0.0f, bb = 0.0f;
+        if (n < p.N) {
+          sc = s_a * p.s_w[p.per_channel ? n : 0];
+          bb = p.bias ? bf16_bits_to_float(p.bias[n]) : 0.0f;
+        }
+        ctl->colscale[ab][j] = sc;
+        ctl->colbias[ab][j] = bb;
+      }
+      // publishes the column tables; a set abort flag makes all epilogue warps leave together
+      if (epi_bar_any(*abort_flag != 0)) break;
+      // after a timeout, skip to the next barrier above, which ends the loop uniformly
+      if (!mbar_wait_bounded(smem_u32(&ctl->tfull[ab]), aph, abort_flag, &g_gemm_error)) continue;
+      tmem_fence_after();
+      const int m = m_idx * BM + row_in_tile;
+      uint16_t* yrow = p.y + (int64_t)m * p.ldy;
+      const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + ab * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int n0 = n_idx * BN + c * 32;
+        if (n0 >= p.N) break;  // warp-uniform
+        uint32_t r[32];
+        tmem_ld32(tbase + c * 32, r);
+        if (m < p.M) {
+          const float* cs = &ctl->colscale[ab][c * 32];
+          const float* cb = &ctl->colbias[ab][c * 32];
+          if (p.y_vec && n0 + 32 <= p.N) {
+            uint4* dst = reinterpret_cast<uint4*>(yrow + n0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t w[4];
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                const int j = v * 8 + h * 2;
+                w[h] = pack_bf16x2(fmaf(__uint_as_float(r[j]), cs[j], cb[j]),
+                                   fmaf(__uint_as_float(r[j + 1]), cs[j + 1], cb[j + 1]));
+              }
+              dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (n0 + j < p.N)
+                yrow[n0 + j] = __bfloat16_as_ushort(
+                    __float2bfloat16_rn(fmaf(__uint_as_float(r[j]), cs[j], cb[j])));
+            }
+          }
+        }
+      }
+      tmem_fence_before();
+      mbar_arrive(smem_u32(&ctl->tempty[ab]));
+    }
+  }
+
+  tmem_fence_before();
+  __syncthreads();
+  tmem_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem_base), "n"(kTmemCols) : "memory");
+  }
+}
+
+}  // namespace gemm
+}  // namespace fp8k
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
+  return fn;
+}
+
+// 2-D e4m3 tensor map: [rows, K] with row stride ld bytes, box [box_rows, 128 bytes], 128B swizzle.
+bool make_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t K, int64_t ld, uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(ld)};
+  const cuuint32_t box[2] = {uint32_t(fp8k::gemm::BK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+namespace fp8k {
+
+int gemm_launch(const uint8_t* qa, int64_t ldqa, const float* s_a, const uint8_t* qw, int64_t ldqw,
+                const float* s_w, int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy,
+                int M, int N, int K, int num_sms, cudaStream_t stream) {
+  using namespace gemm;
+  static bool attr_done = false;  // the attribute is per function, set once per process
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes)) != cudaSuccess)
+      return 1;
+    attr_done = true;
+  }
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, qa, M, K, ldqa, BM) || !make_map(&mb, qw, N, K, ldqw, BN)) return 2;
+
+  GemmParams p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.s_a = s_a;
+  p.s_w = s_w;
+  p.per_channel = per_channel;
+  p.bias = bias;
+  p.y = y;
+  p.ldy = ldy;
+  p.m_tiles = (M + BM - 1) / BM;
+  p.n_tiles = (N + BN - 1) / BN;
+  p.group_n = p.n_tiles < 16 ? p.n_tiles : 16;
+  p.y_vec = (ldy % 8 == 0) && (reinterpret_cast<uintptr_t>(y) % 16 == 0);
+
+  const int tiles = p.m_tiles * p.n_tiles;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles < num_sms ? tiles : num_sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_kernel, ma, mb, p) == cudaSuccess ? 0 : 3;
+}
+
+unsigned int gemm_read_and_clear_error() {
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, gemm::g_gemm_error, sizeof(v)) != cudaSuccess) return 0;
+  cudaMemcpyToSymbol(gemm::g_gemm_error, &zero, sizeof(zero));
+  return v;
+}
+
+}  // namespace fp8k

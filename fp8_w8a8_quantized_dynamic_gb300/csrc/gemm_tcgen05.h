@@ -1,0 +1,31 @@
+// Internal interface between the C-ABI layer and the tcgen05 GEMM translation unit.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace fp8k {
+
+struct GemmParams {
+  int M, N, K;
+  const float* s_a;
+  const float* s_w;
+  int per_channel;
+  const uint16_t* bias;
+  uint16_t* y;
+  int64_t ldy;
+  int m_tiles, n_tiles, group_n;
+  int y_vec;
+};
+
+// Enqueues the persistent GEMM. Returns 0 on success, non-zero when the tensor maps could
+// not be encoded or the launch failed. qa/qw: 16-byte aligned, ld multiples of 16.
+int gemm_launch(const uint8_t* qa, int64_t ldqa, const float* s_a, const uint8_t* qw, int64_t ldqw,
+                const float* s_w, int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy,
+                int M, int N, int K, int num_sms, cudaStream_t stream);
+
+// Device-side error bits recorded by the GEMM kernel on the current device (read, then cleared).
+unsigned int gemm_read_and_clear_error();
+
+}  // namespace fp8k

@@ -1,0 +1,180 @@
+// Dynamic FP8 quantization kernels: amax reduction and the saturating RNE cast.
+//
+// Per-tensor scale ("Prototype FP8Linear W8A8 runtime quantization": weights and
+// activations are quantized at run time; "Fp8 Quantization Support": symmetric,
+// strategy "tensor"): s = amax / 448, q = e4m3(x / s).
+// Per-output-channel scale ("[Kernel] Implement fallback for FP8 channelwise using
+// torch._scaled_mm"): one s per row of W.
+//
+// The per-tensor amax is a two-step reduction with no atomics and no state that must
+// start at zero: amax_partials_kernel writes one partial maximum per CTA into the
+// workspace; every consumer CTA (the cast kernel, the GEMV) reduces those partials
+// itself. Max is exact and order-free, so every CTA derives the identical scale.
+#pragma once
+
+#include "device_common.cuh"
+
+namespace fp8k {
+
+constexpr int kQuantThreads = 256;
+
+// Cached 16-byte load (the row is read again shortly after).
+__device__ __forceinline__ uint4 ld_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t abs_max_v4(uint32_t m2, uint4 v) {
+  m2 = abs_max_u16x2(m2, v.x);
+  m2 = abs_max_u16x2(m2, v.y);
+  m2 = abs_max_u16x2(m2, v.z);
+  return abs_max_u16x2(m2, v.w);
+}
+
+// Block-wide max of a non-negative float; the result is valid in thread 0.
+__device__ __forceinline__ float block_max_to_thread0(float v, float* red) {
+  v = warp_max(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) v = fmaxf(v, red[i]);
+  }
+  return v;
+}
+
+// Partial max |x| over a bf16 matrix [rows, cols] with row stride ld (elements).
+// contiguous != 0: ld == cols and the base is 16-byte aligned (flat 16-byte loads).
+// vec != 0: base 16-byte aligned and ld % 8 == 0 (16-byte loads per row).
+// Writes partials[blockIdx.x]. `pdl` lets the next kernel launch early (activations only).
+__global__ void __launch_bounds__(kQuantThreads)
+amax_partials_kernel(const uint16_t* __restrict__ a, int64_t rows, int64_t cols, int64_t ld,
+                     int contiguous, int vec, float* __restrict__ partials, int pdl) {
+  __shared__ float red[kQuantThreads / 32];
+  if (pdl) pdl_trigger();
+  pdl_wait();
+  uint32_t m2 = 0;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (contiguous) {
+    const int64_t n = rows * cols;
+    const int64_t n8 = n >> 3;
+    const uint4* v = reinterpret_cast<const uint4*>(a);
+    int64_t i = tid;
+    for (; i + 3 * stride < n8; i += 4 * stride) {
+      const uint4 v0 = ld_nc_v4(v + i), v1 = ld_nc_v4(v + i + stride);
+      const uint4 v2 = ld_nc_v4(v + i + 2 * stride), v3 = ld_nc_v4(v + i + 3 * stride);
+      m2 = abs_max_v4(abs_max_v4(m2, v0), v1);
+      m2 = abs_max_v4(abs_max_v4(m2, v2), v3);
+    }
+    for (; i < n8; i += stride) m2 = abs_max_v4(m2, ld_nc_v4(v + i));
+    if (blockIdx.x == 0)
+      for (int64_t j = (n8 << 3) + threadIdx.x; j < n; j += blockDim.x) m2 = abs_max_u16x2(m2, a[j]);
+  } else {
+    const int64_t upr = (cols + 7) >> 3;  // 8-element units per row
+    const int64_t units = rows * upr;
+    for (int64_t u = tid; u < units; u += stride) {
+      const int64_t r = u / upr;
+      const int64_t c = (u - r * upr) << 3;
+      const uint16_t* src = a + r * ld + c;
+      if (vec && c + 8 <= cols) {
+        m2 = abs_max_v4(m2, ld_nc_v4(src));
+      } else {
+        for (int j = 0; j < 8 && c + j < cols; ++j) m2 = abs_max_u16x2(m2, src[j]);
+      }
+    }
+  }
+  const float m = block_max_to_thread0(u16x2_max_to_float(m2), red);
+  if (threadIdx.x == 0) partials[blockIdx.x] = m;
+}
+
+// Quantize 16 consecutive elements of one row (columns c .. c+15) into 16 e4m3 bytes;
+// columns >= cols give 0x00.
+__device__ __forceinline__ uint4 quant16_row(const uint16_t* __restrict__ src, int64_t c, int64_t cols,
+                                             bool vec, float s) {
+  uint4 out;
+  if (vec && c + 16 <= cols) {
+    const uint2 q0 = quant8_bf16(ld_v4(src), s);
+    const uint2 q1 = quant8_bf16(ld_v4(src + 8), s);
+    out = make_uint4(q0.x, q0.y, q1.x, q1.y);
+  } else {
+    float x[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) x[j] = (c + j < cols) ? bf16_bits_to_float(src[j]) : 0.0f;
+    out.x = quant4(x[0], x[1], x[2], x[3], s);
+    out.y = quant4(x[4], x[5], x[6], x[7], s);
+    out.z = quant4(x[8], x[9], x[10], x[11], s);
+    out.w = quant4(x[12], x[13], x[14], x[15], s);
+  }
+  return out;
+}
+
+// q[r, 0:ldq) = e4m3(A[r, 0:cols) / s) with zero bytes for columns >= cols, where
+// s = scale_from_amax(max of the n_partials partials). CTA 0 stores s to *s_out.
+template <typename Idx>
+__global__ void __launch_bounds__(kQuantThreads)
+cast_kernel(const uint16_t* __restrict__ a, int64_t rows, int64_t cols, int64_t ld, int vec,
+            const float* __restrict__ partials, int n_partials, float* __restrict__ s_out,
+            uint8_t* __restrict__ q, int64_t ldq, int pdl) {
+  __shared__ float red[kQuantThreads / 32];
+  if (pdl) pdl_trigger();
+  pdl_wait();
+  const float s = scale_from_amax(block_max_partials(partials, n_partials, red));
+  if (blockIdx.x == 0 && threadIdx.x == 0) *s_out = s;
+  const Idx upr = static_cast<Idx>(ldq >> 4);  // 16-byte output units per row
+  const Idx units = static_cast<Idx>(rows) * upr;
+  const Idx stride = static_cast<Idx>(gridDim.x) * blockDim.x;
+  for (Idx u = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x; u < units; u += stride) {
+    const Idx r = u / upr;
+    const int64_t c = static_cast<int64_t>(u - r * upr) << 4;
+    const uint4 out = quant16_row(a + (int64_t)r * ld + c, c, cols, vec != 0, s);
+    *reinterpret_cast<uint4*>(q + (int64_t)r * ldq + c) = out;
+  }
+}
+
+// Per-row (output channel) weight quantization: CTA per row, s_w[r] = amax(W[r,:]) / 448.
+// The row is read twice; the second read hits L1/L2.
+__global__ void __launch_bounds__(kQuantThreads)
+quantize_rows_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t K, int64_t ld, int vec,
+                     uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s_w) {
+  __shared__ float red[kQuantThreads / 32];
+  __shared__ float s_sh;
+  pdl_wait();
+  for (int64_t r = blockIdx.x; r < N; r += gridDim.x) {
+    const uint16_t* row = w + r * ld;
+    uint32_t m2 = 0;
+    if (vec) {
+      const int64_t k8 = K >> 3;
+      for (int64_t i = threadIdx.x; i < k8; i += blockDim.x) m2 = abs_max_v4(m2, ld_v4(row + (i << 3)));
+      for (int64_t j = (k8 << 3) + threadIdx.x; j < K; j += blockDim.x) m2 = abs_max_u16x2(m2, row[j]);
+    } else {
+      for (int64_t j = threadIdx.x; j < K; j += blockDim.x) m2 = abs_max_u16x2(m2, row[j]);
+    }
+    const float m = block_max_to_thread0(u16x2_max_to_float(m2), red);
+    if (threadIdx.x == 0) {
+      s_sh = scale_from_amax(m);
+      s_w[r] = s_sh;
+    }
+    __syncthreads();
+    const float s = s_sh;
+    for (int64_t c = (int64_t)threadIdx.x << 4; c < ldq; c += (int64_t)blockDim.x << 4)
+      *reinterpret_cast<uint4*>(q + r * ldq + c) = quant16_row(row + c, c, K, vec != 0, s);
+    __syncthreads();  // s_sh and red are reused by the next row
+  }
+}
+
+// Y[m, :] = bias (or 0) for all m: the K == 0 product.
+__global__ void fill_bias_kernel(const uint16_t* __restrict__ bias, uint16_t* __restrict__ y,
+                                 int64_t M, int64_t N, int64_t ldy, int pdl) {
+  if (pdl) pdl_trigger();
+  pdl_wait();
+  const int64_t total = M * N;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = i / N, n = i - m * N;
+    y[m * ldy + n] = bias ? bias[n] : uint16_t(0);
+  }
+}
+
+}  // namespace fp8k

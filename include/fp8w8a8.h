@@ -1,0 +1,166 @@
+/*
+ * fp8w8a8.h — C ABI of the FP8 (e4m3fn) W8A8 linear layer with dynamic
+ * per-tensor activation quantization, for NVIDIA sm_103a (GB300).
+ *
+ * The layer (source pages: "Prototype FP8Linear W8A8 runtime quantization",
+ * "[WIP] FP8 support", "[Kernel] Implement fallback for FP8 channelwise using
+ * torch._scaled_mm", "Fp8 Quantization Support"):
+ *
+ *   s_w      = amax(W) / 448              (per tensor, or per output row n)
+ *   qW       = e4m3(W / s_w)              once, when weights are loaded
+ *   s_a      = amax(A) / 448              every call, on the device
+ *   qA       = e4m3(A / s_a)
+ *   Y[m, n]  = bf16( s_a * s_w[n] * sum_k qA[m, k] qW[n, k]  (+ bias[n]) )
+ *
+ * e4m3(x): IEEE fp32 quotient, then round-to-nearest-even to float8_e4m3fn,
+ * saturating to +-448; the sign of zero is kept. A zero amax gives scale 1.
+ * The product accumulates in fp32 on tensor cores.
+ *
+ * Conventions for every call:
+ *  - Matrices are row-major. A bf16 [M, K] with row stride lda >= K elements;
+ *    W bf16 [N, K] (out_features x in_features, as in nn.Linear) with stride
+ *    ldw >= K; Y bf16 [M, N] with stride ldy >= N. bf16 strides may be any
+ *    value: no padding of the logical dimensions is required ("[WIP] FP8
+ *    support": dimensions that are not multiples of 16 must work).
+ *  - The library's own FP8 matrices (qA, qW) are u8 [rows, ld] with ld a
+ *    multiple of 16 and ld >= K (fp8_min_ld(K) is the smallest). The
+ *    quantizers write bytes [K, ld) of every row as zero; consumers rely on
+ *    that. The base address of an FP8 matrix must be 16-byte aligned.
+ *  - Scales (s_a, s_w) are fp32 in DEVICE memory, so dynamic quantization
+ *    never needs a host round trip.
+ *  - Every pointer is a device pointer owned by the caller. The library
+ *    allocates nothing, never synchronizes (except fp8_last_device_status),
+ *    and enqueues all work on `stream` (NULL = the legacy default stream).
+ *  - Argument errors are returned synchronously before anything is enqueued.
+ *    FP8_ERR_CUDA reports a failed launch. Kernel-side errors (a bounded wait
+ *    that expired) are reported later by fp8_last_device_status().
+ *  - M == 0 or N == 0 is a no-op returning FP8_OK. K == 0 gives Y = bias (or 0).
+ *  - A workspace may be used by one call at a time; calls are otherwise
+ *    reentrant and thread-safe.
+ *  - Launch ordering: kernels use programmatic dependent launch. The weight
+ *    operands (qW, s_w, bias) of a linear call may be read before the kernel
+ *    enqueued just before it has finished, so they must not be written by the
+ *    immediately preceding kernel unless that kernel is fp8_quantize_weight or
+ *    a kernel that does not trigger programmatic launch early (any ordinary
+ *    CUDA or PyTorch kernel). Activations, workspace and Y are always ordered.
+ */
+#ifndef FP8W8A8_H
+#define FP8W8A8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* fp8_stream_t;
+
+typedef enum fp8_status {
+  FP8_OK = 0,
+  FP8_ERR_INVALID_ARG = 1,        /* null pointer, negative size, ld too small, bad flag */
+  FP8_ERR_MISALIGNED = 2,         /* FP8 ld not a multiple of 16, or a base address not aligned */
+  FP8_ERR_WORKSPACE = 3,          /* workspace too small or not 256-byte aligned */
+  FP8_ERR_CUDA = 4,               /* a CUDA runtime/driver call or kernel launch failed */
+  FP8_ERR_TIMEOUT = 5,            /* a device-side bounded wait expired (see fp8_last_device_status) */
+  FP8_ERR_UNSUPPORTED_DEVICE = 6  /* current device is not sm_103 */
+} fp8_status;
+
+#define FP8_E4M3_MAX 448.0f
+#define FP8_LD_ALIGN 16
+/* Workspace needed by fp8_quantize_weight / fp8_quantize_act (partial amax values). */
+#define FP8_QUANT_WORKSPACE_BYTES 4352
+
+/* Smallest valid leading dimension (bytes) of an FP8 matrix with K columns: K rounded up to 16 (16 for K == 0). */
+int64_t fp8_min_ld(int64_t K);
+
+/* Bytes of workspace fp8_linear / fp8_linear_channelwise need for this shape
+ * (partial amax values, the activation scale and, when the shape runs on the
+ * GEMM path, the quantized activations qA [M, fp8_min_ld(K)]). Always >=
+ * FP8_QUANT_WORKSPACE_BYTES. Host-only, never touches the device. */
+size_t fp8_workspace_bytes(int64_t M, int64_t K, int64_t N);
+
+/* 1 when fp8_linear takes the decode GEMV path for this shape, 0 for the GEMM path. Host-only. */
+int fp8_uses_gemv(int64_t M, int64_t K, int64_t N);
+
+/*
+ * Quantize bf16 weights W [N, K] (stride ldw) to qW u8 [N, ldq] and scales s_w.
+ * per_channel == 0: one scale, s_w[0] = amax(W)/448 ("Fp8 Quantization
+ * Support", recipe strategy "tensor"). per_channel == 1: s_w[n] = amax(W[n,:])/448
+ * for each output channel ("[Kernel] Implement fallback for FP8 channelwise
+ * using torch._scaled_mm"). Bytes [K, ldq) of each row are written as zero.
+ * ws: device workspace of >= FP8_QUANT_WORKSPACE_BYTES bytes, 256-byte aligned
+ * (unused when per_channel == 1; may then be NULL).
+ */
+fp8_status fp8_quantize_weight(const void* w_bf16, int64_t N, int64_t K, int64_t ldw,
+                               int per_channel, uint8_t* qw, int64_t ldq, float* s_w,
+                               void* ws, size_t ws_bytes, fp8_stream_t stream);
+
+/*
+ * Dynamic per-tensor activation quantization ("Prototype FP8Linear W8A8
+ * runtime quantization": activations are quantized at run time):
+ * s_a[0] = amax(A)/448, qA = e4m3(A / s_a) as u8 [M, ldq], tail bytes zero.
+ * ws: >= FP8_QUANT_WORKSPACE_BYTES bytes, 256-byte aligned.
+ */
+fp8_status fp8_quantize_act(const void* a_bf16, int64_t M, int64_t K, int64_t lda,
+                            uint8_t* qa, int64_t ldq, float* s_a,
+                            void* ws, size_t ws_bytes, fp8_stream_t stream);
+
+/*
+ * Scaled FP8 GEMM on already-quantized operands — the step the pages run with
+ * torch._scaled_mm ("Prototype FP8Linear W8A8 runtime quantization";
+ * "[Kernel] Implement fallback for FP8 channelwise using torch._scaled_mm"):
+ *   Y[m, n] = bf16( s_a[0] * s_w[n or 0] * sum_k qA[m,k] qW[n,k] (+ bias[n]) ).
+ * qa u8 [M, ldqa], qw u8 [N, ldqw] (both ld multiples of 16, tails zero);
+ * s_a device fp32 [1]; s_w device fp32 [1] (per_channel == 0) or [N]
+ * (per_channel == 1); bias bf16 [N] or NULL; y bf16 [M, ldy].
+ * Uses no workspace.
+ */
+fp8_status fp8_scaled_mm(const uint8_t* qa, int64_t M, int64_t K, int64_t ldqa, const float* s_a,
+                         const uint8_t* qw, int64_t N, int64_t ldqw, const float* s_w,
+                         int per_channel, const void* bias_bf16, void* y_bf16, int64_t ldy,
+                         fp8_stream_t stream);
+
+/*
+ * The W8A8 linear with dynamic per-tensor activation quantization and a
+ * per-tensor weight scale s_w[0]: amax(A) -> s_a -> e4m3(A/s_a) -> FP8 GEMM
+ * (fp32 accumulate) -> s_a*s_w (+bias) epilogue -> bf16 Y.
+ * Decode shapes (fp8_uses_gemv) run a split-K GEMV that quantizes A on the fly
+ * ("[WIP] FP8 support": LLM decode runs at sequence length < 16 and wants a
+ * custom gemv); larger M runs the tcgen05 GEMM. No padding or repacking of A,
+ * W or Y happens on any path.
+ * ws: >= fp8_workspace_bytes(M, K, N) bytes, 256-byte aligned.
+ */
+fp8_status fp8_linear(const void* a_bf16, int64_t M, int64_t K, int64_t lda,
+                      const uint8_t* qw, int64_t N, int64_t ldqw, const float* s_w,
+                      const void* bias_bf16, void* y_bf16, int64_t ldy,
+                      void* ws, size_t ws_bytes, fp8_stream_t stream);
+
+/*
+ * Same as fp8_linear with one weight scale per output channel, s_w[N]; the
+ * channel scale is applied to column n after the product, using
+ * (s_a A)(s_w,n W_n)^T = s_a s_w,n (A W_n^T) ("[Kernel] Implement fallback for
+ * FP8 channelwise using torch._scaled_mm"), fused into the epilogue.
+ */
+fp8_status fp8_linear_channelwise(const void* a_bf16, int64_t M, int64_t K, int64_t lda,
+                                  const uint8_t* qw, int64_t N, int64_t ldqw, const float* s_w,
+                                  const void* bias_bf16, void* y_bf16, int64_t ldy,
+                                  void* ws, size_t ws_bytes, fp8_stream_t stream);
+
+/*
+ * Synchronizes `stream`, then reports and clears device-side errors recorded
+ * by the library's kernels on the current device since the last query
+ * (FP8_ERR_TIMEOUT when a bounded wait expired), or FP8_ERR_CUDA when the
+ * stream itself reports an error. FP8_OK otherwise.
+ */
+fp8_status fp8_last_device_status(fp8_stream_t stream);
+
+/* Static, human-readable name of a status code. Never NULL. */
+const char* fp8_status_string(fp8_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8W8A8_H */

@@ -1,0 +1,149 @@
+"""C-ABI boundary tests that need no GPU.
+
+The library is built here (nvcc cross-compiles for sm_103a) and loaded with ctypes.
+Only host logic runs: symbol exports, size/layout helpers, status strings, and argument
+validation, which must reject bad input synchronously before any CUDA call.
+"""
+
+import os
+import re
+
+import pytest
+
+import fp8_w8a8_quantized_dynamic_gb300 as F
+from fp8_w8a8_quantized_dynamic_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+INCLUDE = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return F.lib()
+
+
+def declared_functions():
+    names = set()
+    for h in os.listdir(INCLUDE):
+        if not h.endswith(".h"):
+            continue
+        src = re.sub(r"/\*.*?\*/", "", open(os.path.join(INCLUDE, h)).read(), flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(fp8_\w+)\s*\(", src, flags=re.M))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary_calls():
+    names = declared_functions()
+    for required in ("fp8_quantize_weight", "fp8_quantize_act", "fp8_linear", "fp8_linear_channelwise",
+                     "fp8_scaled_mm", "fp8_workspace_bytes", "fp8_last_device_status", "fp8_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_binding_names_match_c_abi():
+    for name in declared_functions():
+        assert callable(getattr(F, name)), name
+
+
+def test_status_strings(L):
+    for code, name in [(0, "FP8_OK"), (1, "FP8_ERR_INVALID_ARG"), (2, "FP8_ERR_MISALIGNED"),
+                       (3, "FP8_ERR_WORKSPACE"), (4, "FP8_ERR_CUDA"), (5, "FP8_ERR_TIMEOUT"),
+                       (6, "FP8_ERR_UNSUPPORTED_DEVICE")]:
+        assert F.status_string(code) == name
+    assert F.status_string(99) == "FP8_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("K", [0, 1, 15, 16, 17, 1000, 4095, 4096, 4100, 14336])
+def test_min_ld(L, K):
+    assert F.fp8_min_ld(K) == F.min_ld(K)
+    assert F.fp8_min_ld(K) % 16 == 0 and F.fp8_min_ld(K) >= max(K, 16)
+
+
+def test_workspace_and_dispatch(L):
+    base = F.FP8_QUANT_WORKSPACE_BYTES
+    # decode shapes run the GEMV: no activation buffer in the workspace
+    for M in (1, 2, 8, 15, 16):
+        assert F.fp8_uses_gemv(M, 4096, 4096)
+        assert F.fp8_workspace_bytes(M, 4096, 4096) == base
+    # GEMM shapes hold qA [M, min_ld(K)]
+    for M, K in ((17, 4096), (16384, 14336), (100, 4100)):
+        assert not F.fp8_uses_gemv(M, K, 4096)
+        assert F.fp8_workspace_bytes(M, K, 4096) == base + M * F.min_ld(K)
+    assert F.fp8_workspace_bytes(0, 4096, 4096) == base
+    assert not F.fp8_uses_gemv(4, 40000, 4096)  # K beyond the GEMV's slice budget -> GEMM
+
+
+# ---------------------------------------------------------------------------
+# argument validation (fake, never dereferenced device addresses)
+# ---------------------------------------------------------------------------
+
+P = 0x7F0000000000  # 256-byte aligned fake address
+WS = 0x7F0000100000
+
+
+def lin(L, a=P, M=4, K=64, lda=64, qw=P, N=32, ldqw=64, s_w=P, bias=None, y=P, ldy=32, ws=WS,
+        ws_bytes=1 << 20, channelwise=False):
+    fn = L.fp8_linear_channelwise if channelwise else L.fp8_linear
+    return fn(a, M, K, lda, qw, N, ldqw, s_w, bias, y, ldy, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("channelwise", [False, True])
+def test_linear_rejects_bad_arguments(L, channelwise):
+    c = dict(channelwise=channelwise)
+    assert lin(L, a=None, **c) == F.FP8_ERR_INVALID_ARG
+    assert lin(L, qw=None, **c) == F.FP8_ERR_INVALID_ARG
+    assert lin(L, y=None, **c) == F.FP8_ERR_INVALID_ARG
+    assert lin(L, s_w=None, **c) == F.FP8_ERR_INVALID_ARG
+    assert lin(L, M=-1, **c) == F.FP8_ERR_INVALID_ARG
+    assert lin(L, K=-1, **c) == F.FP8_ERR_INVALID_ARG
+    assert lin(L, N=-5, **c) == F.FP8_ERR_INVALID_ARG
+    assert lin(L, lda=63, **c) == F.FP8_ERR_INVALID_ARG           # lda < K
+    assert lin(L, ldy=31, **c) == F.FP8_ERR_INVALID_ARG           # ldy < N
+    assert lin(L, ldqw=48, **c) == F.FP8_ERR_INVALID_ARG          # ldqw < K
+    assert lin(L, K=60, lda=60, ldqw=72, **c) == F.FP8_ERR_MISALIGNED  # FP8 ld not a multiple of 16
+    assert lin(L, qw=P + 8, **c) == F.FP8_ERR_MISALIGNED          # FP8 base not 16-byte aligned
+    assert lin(L, a=P + 1, **c) == F.FP8_ERR_MISALIGNED           # bf16 base odd
+    assert lin(L, bias=P + 1, **c) == F.FP8_ERR_MISALIGNED
+    assert lin(L, ws=None, **c) == F.FP8_ERR_WORKSPACE
+    assert lin(L, ws_bytes=100, **c) == F.FP8_ERR_WORKSPACE
+    assert lin(L, ws=WS + 16, **c) == F.FP8_ERR_WORKSPACE         # not 256-byte aligned
+    # GEMM-path shapes need room for qA
+    need = F.fp8_workspace_bytes(64, 64, 32)
+    assert lin(L, M=64, ws_bytes=need - 1, **c) == F.FP8_ERR_WORKSPACE
+
+
+def test_linear_empty_is_noop_without_device(L):
+    # M == 0 or N == 0 returns before any CUDA call (no GPU in this container)
+    assert lin(L, M=0, a=None, y=None) == F.FP8_OK
+    assert lin(L, N=0, qw=None, ldy=1, s_w=None) == F.FP8_OK
+
+
+def test_quantize_calls_reject_bad_arguments(L):
+    q = L.fp8_quantize_weight
+    assert q(None, 8, 64, 64, 0, P, 64, P, WS, 1 << 16, None) == F.FP8_ERR_INVALID_ARG
+    assert q(P, 8, 64, 64, 2, P, 64, P, WS, 1 << 16, None) == F.FP8_ERR_INVALID_ARG   # bad flag
+    assert q(P, 8, 64, 64, 0, P, 64, None, WS, 1 << 16, None) == F.FP8_ERR_INVALID_ARG
+    assert q(P, 8, 64, 64, 0, P, 64, P, WS, 16, None) == F.FP8_ERR_WORKSPACE
+    assert q(P, 8, 64, 64, 0, P, 40, P, WS, 1 << 16, None) == F.FP8_ERR_INVALID_ARG   # ldq < K
+    assert q(P, 8, 64, 64, 1, P, 64, P, None, 0, None) != F.FP8_ERR_WORKSPACE       # per-channel: no ws
+    a = L.fp8_quantize_act
+    assert a(P, 8, 64, 32, P, 64, P, WS, 1 << 16, None) == F.FP8_ERR_INVALID_ARG      # lda < K
+    assert a(P, 8, 64, 64, P + 4, 64, P, WS, 1 << 16, None) == F.FP8_ERR_MISALIGNED
+    assert a(P, 8, 64, 64, P, 64, None, WS, 1 << 16, None) == F.FP8_ERR_INVALID_ARG
+    s = L.fp8_scaled_mm
+    assert s(P, 4, 64, 64, None, P, 8, 64, P, 0, None, P, 8, None) == F.FP8_ERR_INVALID_ARG
+    assert s(P, 4, 64, 64, P, P, 8, 64, P, 3, None, P, 8, None) == F.FP8_ERR_INVALID_ARG
+    assert s(P, 4, 64, 24, P, P, 8, 64, P, 0, None, P, 8, None) == F.FP8_ERR_INVALID_ARG
+
+
+def test_valid_call_without_gpu_reports_cuda_error(L):
+    # validation passes, then the device query fails: no crash, an error code
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lin(L) in (F.FP8_ERR_CUDA, F.FP8_ERR_UNSUPPORTED_DEVICE)

@@ -1,0 +1,222 @@
+"""GPU parity of the W8A8 linear (decode GEMV and tcgen05 GEMM paths) against the oracle.
+
+Y must lie within one bf16 ulp of the exact value plus K * 2^-23 * sum_k |a_k w_k|
+(oracle.tolerance); the GPU's qW / s_w are checked bit-exact where the test quantizes
+them. Output buffers carry canary guard bands to catch stray writes.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import fp8_w8a8_quantized_dynamic_gb300 as F
+from fp8_w8a8_quantized_dynamic_gb300 import _build
+from fp8_w8a8_quantized_dynamic_gb300 import inputs as I
+from parity import (assert_codes_equal, assert_guards_intact, assert_scale_equal, guarded, linear_parity,
+                    oracle_weight)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    _build.build()
+    F.lib()
+
+
+def run_linear(a_cpu, w_cpu, per_channel, bias_cpu=None, guard=True, lda_pad=0):
+    """Quantize W on the GPU, run the linear (into a guarded Y buffer), return (y, qw, s_w)."""
+    M, K = a_cpu.shape
+    N = w_cpu.shape[0]
+    qw, s_w = F.fp8_quantize_weight(w_cpu.to(DEV), per_channel=per_channel)
+    if lda_pad:
+        big = torch.zeros((M, K + lda_pad), dtype=torch.bfloat16)
+        big[:, :K] = a_cpu
+        a = big.to(DEV)[:, :K]
+    else:
+        a = a_cpu.to(DEV)
+    bias = None if bias_cpu is None else bias_cpu.to(DEV)
+    fn = F.fp8_linear_channelwise if per_channel else F.fp8_linear
+    if guard:
+        buf, y, base, row_bytes, used = guarded((M, N), torch.bfloat16, DEV)
+        fn(a, qw, s_w, bias, out=y)
+        torch.cuda.synchronize()
+        assert_guards_intact(buf, base, row_bytes, used, M)
+    else:
+        y = fn(a, qw, s_w, bias)
+        torch.cuda.synchronize()
+    assert F.fp8_last_device_status() == F.FP8_OK
+    return y, qw, s_w
+
+
+def check(a, w, per_channel, bias=None, what="", rows=None, cols=None, lda_pad=0, check_w=True):
+    y, qw, s_w = run_linear(a, w, per_channel, bias, lda_pad=lda_pad)
+    if check_w:
+        q_ref, s_ref = oracle_weight(w, per_channel, None if cols is None else np.asarray(cols))
+        sel = slice(None) if cols is None else torch.as_tensor(np.asarray(cols), device=DEV)
+        assert_scale_equal(s_w if not per_channel else s_w[sel], s_ref, what + " s_w")
+        assert_codes_equal(qw[sel], q_ref, w.shape[1], what + " qW")
+    return linear_parity(y, a, w, per_channel, bias, rows, cols, what)
+
+
+# --------------------------------------------------------------------------- decode GEMV
+
+@pytest.mark.parametrize("M", list(range(1, 17)))
+def test_gemv_every_m(M):
+    K, N = 1000, 1027
+    assert F.fp8_uses_gemv(M, K, N)
+    a = I.activations_normal(M, K, (901, M), outlier_cols=4)
+    w = I.weights_row_std(N, K, (902,))
+    b = I.bias_normal(N, (903,))
+    check(a, w, False, b, f"gemv M={M} per-tensor")
+    check(a, w, True, None, f"gemv M={M} channelwise", check_w=False)
+
+
+def test_tiny_config():
+    c = I.tiny_case()
+    check(c.a, c.w, c.per_channel, None, c.name)
+
+
+@pytest.mark.parametrize("idx", range(4))
+def test_unaligned_config(idx):
+    c = I.unaligned_cases()[idx]
+    check(c.a, c.w, c.per_channel, None, c.name)
+    check(c.a, c.w, True, I.bias_normal(c.N, (904,)), c.name + " channelwise+bias", lda_pad=5, check_w=False)
+
+
+@pytest.mark.parametrize("layer", range(4))
+@pytest.mark.parametrize("M", [1, 15])
+def test_decode_config_layers(layer, M):
+    """Mistral-7B decode layers at full size; Y checked on all rows and 1536 sampled columns."""
+    L = I.LLAMA8B_LAYERS[layer]
+    w = I.decode_weight(layer)
+    a = I.decode_activations(M, layer)
+    cols = np.unique(np.concatenate([np.random.default_rng(layer).choice(L.N, 1536, replace=False),
+                                     [0, L.N - 1]]))
+    check(a, w, False, None, f"decode {L.name} M={M}", cols=cols)
+
+
+# --------------------------------------------------------------------------- prefill GEMM
+
+@pytest.mark.parametrize("M,K,N", [(17, 256, 256), (128, 128, 256), (130, 1000, 1027), (300, 4100, 257),
+                                   (257, 2050, 3001), (512, 4096, 512), (1000, 96, 520)])
+@pytest.mark.parametrize("per_channel", [False, True])
+def test_gemm_ragged(M, K, N, per_channel):
+    assert not F.fp8_uses_gemv(M, K, N)
+    a = I.activations_heavy_tail(M, K, (905, M, K))
+    w = I.weights_row_std(N, K, (906, N, K))
+    b = I.bias_normal(N, (907, N))
+    check(a, w, per_channel, b, f"gemm {M}x{K}x{N} pc={per_channel}")
+
+
+def test_gemm_strided_activations_and_output():
+    M, K, N = 200, 1000, 300
+    a = I.activations_normal(M, K, (908,))
+    w = I.weights_normal(N, K, (909,))
+    check(a, w, True, None, "gemm strided A", lda_pad=24, check_w=False)
+    # odd ldy: scalar epilogue stores
+    qw, s_w = F.fp8_quantize_weight(w.to(DEV), per_channel=True)
+    ybig = torch.full((M, N + 3), 7.0, dtype=torch.bfloat16, device=DEV)
+    F.fp8_linear_channelwise(a.to(DEV), qw, s_w, out=ybig[:, :N])
+    torch.cuda.synchronize()
+    assert torch.all(ybig[:, N:] == 7.0)
+    linear_parity(ybig[:, :N], a, w, True, what="gemm odd ldy")
+
+
+@pytest.mark.parametrize("layer", [0, 3])
+def test_prefill_config_full_size_sampled(layer):
+    """Llama-3-8B prefill layer at M = 16384, channelwise, as the benchmark runs it.
+    qW/s_w bit-exact on sampled rows; Y on 40 sampled rows x 768 sampled columns."""
+    L = I.LLAMA8B_LAYERS[layer]
+    w = I.prefill_weight(layer)
+    a = I.prefill_activations(layer)
+    g = np.random.default_rng(100 + layer)
+    rows = np.unique(np.concatenate([g.choice(a.shape[0], 38, replace=False), [0, a.shape[0] - 1]]))
+    cols = np.unique(np.concatenate([g.choice(L.N, 766, replace=False), [0, L.N - 1]]))
+    y, qw, s_w = run_linear(a, w, True, guard=False)
+    q_ref, s_ref = oracle_weight(w, True, cols)
+    sel = torch.as_tensor(cols, device=DEV)
+    assert_scale_equal(s_w[sel], s_ref, "prefill s_w")
+    assert_codes_equal(qw[sel], q_ref, L.K, "prefill qW")
+    linear_parity(y, a, w, True, None, rows, cols, f"prefill {L.name}")
+
+
+@pytest.mark.parametrize("M", [1, 16, 64, 512, 4096])
+def test_tinyllama_sweep_sampled(M):
+    for li, L in enumerate(I.TINYLLAMA_LAYERS):
+        w = I.tinyllama_weight(0, li)
+        a = I.tinyllama_activations(M, 0, li)
+        rows = np.arange(M) if M <= 64 else np.unique(np.r_[np.random.default_rng(M).choice(M, 30), M - 1])
+        for pc in (False, True):
+            y, _, _ = run_linear(a, w, pc, guard=False)
+            linear_parity(y, a, w, pc, None, rows, None, f"tinyllama {L.name} M={M} pc={pc}")
+
+
+# --------------------------------------------------------------------------- API behaviour
+
+@pytest.mark.parametrize("M", [4, 300])
+def test_scaled_mm_equals_linear(M):
+    K, N = 2050, 777
+    a = I.activations_normal(M, K, (910, M)).to(DEV)
+    w = I.weights_row_std(N, K, (911,)).to(DEV)
+    qw, s_w = F.fp8_quantize_weight(w, per_channel=True)
+    y1 = F.fp8_linear_channelwise(a, qw, s_w)
+    qa, s_a = F.fp8_quantize_act(a)
+    y2 = F.fp8_scaled_mm(qa, K, s_a, qw, s_w, per_channel=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("M", [3, 200])
+def test_k_zero_gives_bias(M):
+    N = 300
+    a = torch.empty((M, 0), dtype=torch.bfloat16, device=DEV)
+    qw = torch.zeros((N, 16), dtype=torch.uint8, device=DEV)
+    s_w = torch.ones(1, device=DEV)
+    b = I.bias_normal(N, (912,)).to(DEV)
+    y = F.fp8_linear(a, qw, s_w, b)
+    torch.cuda.synchronize()
+    assert torch.equal(y, b.expand(M, N))
+
+
+def test_m_zero_is_noop():
+    y = torch.full((0, 8), 1.0, dtype=torch.bfloat16, device=DEV)
+    qw, s_w = F.fp8_quantize_weight(torch.ones((8, 32), dtype=torch.bfloat16, device=DEV))
+    F.fp8_linear(torch.empty((0, 32), dtype=torch.bfloat16, device=DEV), qw, s_w, out=y)
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("M", [8, 1000])
+def test_linear_is_deterministic(M):
+    K, N = 4096, 1024
+    a = I.activations_normal(M, K, (913, M)).to(DEV)
+    qw, s_w = F.fp8_quantize_weight(I.weights_normal(N, K, (914,)).to(DEV))
+    y1 = F.fp8_linear(a, qw, s_w)
+    y2 = F.fp8_linear(a, qw, s_w)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+def test_back_to_back_layers_on_one_stream():
+    """Each layer consumes the previous layer's output on one stream, so the programmatic
+    dependent launches must order correctly: the chained result must equal the same layers
+    run with a host synchronization between them. Layer 0 is also checked against the oracle."""
+    K = 1024
+    w = [I.weights_normal(K, K, (915, i)) for i in range(3)]
+    q = [F.fp8_quantize_weight(x.to(DEV)) for x in w]
+    torch.cuda.synchronize()
+    for M in (4, 256):
+        a0 = I.activations_normal(M, K, (916, M))
+        x = a0.to(DEV)
+        chained = []
+        for qw, s_w in q:
+            x = F.fp8_linear(x, qw, s_w)
+            chained.append(x)
+        torch.cuda.synchronize()
+        x = a0.to(DEV)
+        for i, (qw, s_w) in enumerate(q):
+            x = F.fp8_linear(x, qw, s_w)
+            torch.cuda.synchronize()
+            assert torch.equal(x, chained[i]), f"M={M} layer {i}"
+        linear_parity(chained[0], a0, w[0], False, what=f"chain M={M} layer 0")
