@@ -1,0 +1,407 @@
+"""Benchmark of the FP8 W8A8 linear on one GB300 (or N independent replicas).
+
+Headline workload (one "step"): the four Llama-3-8B decoder linears (qkv 4096->6144,
+o_proj 4096->4096, gate_up 4096->28672, down 14336->4096) at M = 16384 tokens with
+per-output-channel weight scales and a dynamic per-tensor activation scale, i.e. per
+layer: amax(A) -> e4m3 cast -> tcgen05 FP8 GEMM -> channelwise rescale epilogue -> bf16 Y.
+value = sum(2*M*N*K) / step time in TFLOP/s, inputs resident in HBM.
+
+Also reported on the same line:
+  decode    weight GB/s of the split-K GEMV on the Mistral-7B layers at M in {1,2,4,8,15}
+            (per-tensor scales), rotating through weight copies so L2 never holds them;
+  roofline  the GEMM kernel's achieved TFLOP/s (fp8_scaled_mm launches timed with CUDA
+            events) against the FP8 dense peak;
+  e2e       the same step through the C-ABI call with host buffers: pinned host->device
+            copy of A, fp8_linear_channelwise, device->host copy of Y, per layer;
+  cpu_baseline  the CPU oracle on a bounded sample of the workload.
+
+`--impl reference` times the CPU oracle alone on that bounded sample (rank 0 only).
+Multi-GPU (torchrun): every rank runs the same workload independently (replicas only;
+the layer does not shard across GPUs here) and value sums over ranks with the slowest
+rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP8 W8A8 linear TFLOP/s (prefill) and weight GB/s (decode M<16) vs roofline"
+NOMINAL_FP8_OVER_BF16 = 2.0  # 4.5 PF fp8 / 2.25 PF bf16 dense (nominal)
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks: nvidia-smi sampled during the timed regions
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                except ValueError:
+                    continue
+                for name, v in zip(names, p[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+def prefill_inputs(M: int):
+    from fp8_w8a8_quantized_dynamic_gb300 import inputs as I
+    return [(L, I.prefill_activations(i, M=M), I.prefill_weight(i)) for i, L in enumerate(I.LLAMA8B_LAYERS)]
+
+
+def flops(M, layers):
+    return sum(2.0 * M * L.N * L.K for L in layers)
+
+
+def time_loop(torch, fn, steps: int, warmup: int):
+    """Median-free timing: W warm-up calls, then K calls between two events (both synced)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / steps  # ms per call
+
+
+def run_ours(args, rank: int, world: int):
+    import torch
+    import fp8_w8a8_quantized_dynamic_gb300 as F
+    from fp8_w8a8_quantized_dynamic_gb300 import _build
+    from fp8_w8a8_quantized_dynamic_gb300 import inputs as I
+
+    if rank == 0 or not os.path.exists(_build.LIB_PATH):
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    F.lib()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    M = args.m
+    layers = I.LLAMA8B_LAYERS
+
+    # ---- inputs: bf16 A per layer, FP8 weights quantized once on the device (load time)
+    host = prefill_inputs(M)
+    A = [a.to(dev) for _, a, _ in host]
+    Wq = []
+    for _, _, w in host:
+        qw, s_w = F.fp8_quantize_weight(w.to(dev), per_channel=True)
+        Wq.append((qw, s_w))
+    Y = [torch.empty((M, L.N), dtype=torch.bfloat16, device=dev) for L in layers]
+    ws = torch.empty(max(F.fp8_workspace_bytes(M, L.K, L.N) for L in layers), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    def step():
+        for i in range(len(layers)):
+            F.fp8_linear_channelwise(A[i], Wq[i][0], Wq[i][1], out=Y[i], ws=ws)
+
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = t0.elapsed_time(t1) / args.steps
+    ms_max = ms
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(t.item())
+    total_flops = flops(M, layers)
+    value = world * total_flops / (ms_max * 1e-3) / 1e12
+    launches = args.steps * len(layers) * 3  # amax, cast, gemm per layer
+
+    # ---- GEMM kernel alone (fp8_scaled_mm on the quantized activations), per layer
+    Q = [F.fp8_quantize_act(a) for a in A]
+    torch.cuda.synchronize()
+    gemm_ms = []
+    for i, L in enumerate(layers):
+        qa, s_a = Q[i]
+        f = lambda i=i, qa=qa, s_a=s_a, L=L: F.fp8_scaled_mm(qa, L.K, s_a, Wq[i][0], Wq[i][1], True, out=Y[i])
+        gemm_ms.append(time_loop(torch, f, max(3, args.steps // 2), 2))
+    quant_ms = []
+    for i, L in enumerate(layers):
+        f = lambda i=i: F.fp8_quantize_act(A[i], ws=ws)
+        quant_ms.append(time_loop(torch, f, max(3, args.steps // 2), 2))
+    del Q
+    gemm_flops = [2.0 * M * L.N * L.K for L in layers]
+    gemm_tflops = sum(gemm_flops) / (sum(gemm_ms) * 1e-3) / 1e12
+    fp8_peak = peaks["bf16_tflops"] * NOMINAL_FP8_OVER_BF16
+    roofline = {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
+                "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4), "traffic": None,
+                "kernel": "gemm_kernel (tcgen05 kind::f8f6f4)",
+                "peak_source": f"{peak_src} bf16 burst x {NOMINAL_FP8_OVER_BF16} nominal fp8/bf16 ratio",
+                "per_layer_ms": {L.name: round(t, 4) for L, t in zip(layers, gemm_ms)}}
+
+    # ---- torch._scaled_mm (cuBLAS FP8) on the same quantized operands, for context only
+    cublas = None
+    if args.compare_cublas:
+        try:
+            tot = 0.0
+            for i, L in enumerate(layers):
+                if L.K % 16:
+                    raise ValueError("K not a multiple of 16")
+                qa, s_a = F.fp8_quantize_act(A[i])
+                a8 = qa[:, :L.K].view(torch.float8_e4m3fn)
+                b8 = Wq[i][0][:, :L.K].view(torch.float8_e4m3fn)
+                sa = s_a.expand(M).reshape(M, 1).contiguous()
+                sw = Wq[i][1].reshape(1, L.N).contiguous()
+                f = lambda a8=a8, b8=b8, sa=sa, sw=sw: torch._scaled_mm(a8, b8.t(), sa, sw,
+                                                                        out_dtype=torch.bfloat16)
+                tot += time_loop(torch, f, max(3, args.steps // 2), 2)
+            cublas = {"what": "torch._scaled_mm rowwise-scaled FP8 GEMM on the same operands (context)",
+                      "tflops": round(sum(gemm_flops) / (tot * 1e-3) / 1e12, 1), "ms_4_layers": round(tot, 4)}
+        except Exception as e:  # noqa: BLE001 - context only
+            cublas = {"unavailable": str(e)[:200]}
+
+    # ---- decode GEMV: Mistral-7B layers, per-tensor scales, weight copies rotated past L2
+    decode = None
+    if not args.no_decode:
+        copies = args.decode_copies
+        dq = [[F.fp8_quantize_weight(I.decode_weight(i, c).to(dev)) for i in range(len(layers))]
+              for c in range(copies)]
+        wbytes_step = copies * sum(L.N * L.K for L in layers)
+        yd = [torch.empty((16, L.N), dtype=torch.bfloat16, device=dev) for L in layers]
+        wsd = torch.empty(F.FP8_QUANT_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
+        per_m = {}
+        for Md in I.DECODE_MS:
+            ad = [I.decode_activations(Md, i).to(dev) for i in range(len(layers))]
+
+            def dstep(ad=ad, Md=Md):
+                for c in range(copies):
+                    for i in range(len(layers)):
+                        F.fp8_linear(ad[i], dq[c][i][0], dq[c][i][1], out=yd[i][:Md], ws=wsd)
+
+            t = time_loop(torch, dstep, max(5, args.steps), 3)
+            per_m[str(Md)] = {"weight_gbs": round(wbytes_step / (t * 1e-3) / 1e9, 1),
+                              "us_per_layer": round(t * 1e3 / (copies * len(layers)), 2)}
+        gbs = [v["weight_gbs"] for v in per_m.values()]
+        hbm = peaks["hbm_gbs"]
+        decode = {"metric": "decode weight GB/s (amax kernel + split-K GEMV per layer)", "unit": "GB/s",
+                  "value": round(statistics.median(gbs), 1), "per_M": per_m,
+                  "workload": "Mistral-7B linears qkv/o_proj/gate_up/down, M in 1,2,4,8,15, per-tensor scales",
+                  "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
+                               "frac_median": round(statistics.median(gbs) / hbm, 4),
+                               "peak_source": f"{peak_src} copy bandwidth"},
+                  "l2": f"{copies} weight copies of {sum(L.N * L.K for L in layers) / 1e6:.0f} MB rotated"}
+        del dq
+
+    clk = clocks.stop()
+
+    # ---- e2e: host buffers through the C-ABI call, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        A_h = [a.pin_memory() for _, a, _ in host]
+        Y_h = [torch.empty((M, L.N), dtype=torch.bfloat16).pin_memory() for L in layers]
+        A_d = A
+
+        def estep():
+            for i in range(len(layers)):
+                A_d[i].copy_(A_h[i], non_blocking=True)
+                F.fp8_linear_channelwise(A_d[i], Wq[i][0], Wq[i][1], out=Y[i], ws=ws)
+                Y_h[i].copy_(Y[i], non_blocking=True)
+
+        te = time_loop(torch, estep, max(3, args.steps // 4), 2)
+        e2e = {"value": round(world * total_flops / (te * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(sum(a.numel() * 2 for a in A_h)),
+               "d2h_bytes_per_step": int(sum(y.numel() * 2 for y in Y_h)), "ms_per_step": round(te, 3)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = oracle_sample(host, M, args.cpu_rows, args.cpu_cols)
+
+    if rank != 0:
+        return None
+    return {
+        "metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 x e4m3 -> fp32 accumulate, bf16 out", "data": "synthetic",
+        "config": {"workload": "prefill: Llama-3-8B linears qkv/o_proj/gate_up/down at M=16384, channelwise "
+                               "weight scales, dynamic per-tensor activation scale",
+                   "M": M, "layers": [[L.name, L.K, L.N] for L in layers], "global_batch": M,
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: each step streams 0.87 GB of bf16 activations and writes "
+                         "1.4 GB of outputs across four layers"},
+        "roofline": roofline, "kernels_ms": {"quantize_act(amax+cast)": [round(t, 4) for t in quant_ms],
+                                             "gemm": [round(t, 4) for t in gemm_ms]},
+        "cublas_context": cublas, "decode": decode, "e2e": e2e, "gpu_launches": launches,
+        "clocks": clk, "cpu_baseline": cpu,
+    }
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(host, M: int, rows: int, cols: int, repeats: int = 1):
+    """Oracle on `rows` activation rows x `cols` output channels of every layer; the amax
+    runs over the full A as the method defines. Returns TFLOP/s of the sampled product."""
+    from oracle import fp8_oracle as O
+    g = np.random.default_rng(0)
+    work = []
+    for L, a, w in host:
+        r = np.sort(g.choice(a.shape[0], rows, replace=False))
+        c = np.sort(g.choice(w.shape[0], cols, replace=False))
+        work.append((L, a.float().numpy(), w[c].float().numpy(), r))
+    t0 = time.perf_counter()
+    fl = 0.0
+    for _ in range(repeats):
+        for L, a32, w32, r in work:
+            s_a = np.float32(O.scale_from_amax(O.amax(a32)))
+            qa = O.quantize_with_scale(a32[r], s_a)
+            qw, s_w = O.quantize_per_row(w32)
+            O.scaled_mm(qa, s_a, qw, s_w)
+            fl += 2.0 * rows * cols * L.K
+    dt = time.perf_counter() - t0
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+            "seconds": round(dt, 2),
+            "sample": f"{rows} activation rows x {cols} output channels per layer of the M={M} prefill step "
+                      f"(full-tensor amax included), numpy float64"}
+
+
+def run_reference(args):
+    from fp8_w8a8_quantized_dynamic_gb300 import inputs as I
+    M = args.m
+    host = prefill_inputs(M)
+    layers = I.LLAMA8B_LAYERS
+    for _ in range(args.warmup):
+        oracle_sample(host, M, args.cpu_rows, args.cpu_cols)
+    res = oracle_sample(host, M, args.cpu_rows, args.cpu_cols, repeats=args.steps)
+    step_s = res["seconds"] / args.steps
+    value = res["value"]
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (exact product)",
+        "data": "synthetic",
+        "config": {"workload": "prefill: Llama-3-8B linears qkv/o_proj/gate_up/down at M=16384, channelwise "
+                               "weight scales, dynamic per-tensor activation scale (bounded CPU sample)",
+                   "M": M, "layers": [[L.name, L.K, L.N] for L in layers]},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": res["cores"], "kind": "oracle",
+                         "sample": res["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--m", type=int, default=16384, help="tokens per prefill layer")
+    ap.add_argument("--decode-copies", type=int, default=3)
+    ap.add_argument("--cpu-rows", type=int, default=16)
+    ap.add_argument("--cpu-cols", type=int, default=512)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--compare-cublas", type=int, default=1)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    out = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
