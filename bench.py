@@ -212,27 +212,6 @@ def run_ours(args, rank: int, world: int):
                 "peak_source": f"{peak_src} bf16 burst x {NOMINAL_FP8_OVER_BF16} nominal fp8/bf16 ratio",
                 "per_layer_ms": {L.name: round(t, 4) for L, t in zip(layers, gemm_ms)}}
 
-    # ---- torch._scaled_mm (cuBLAS FP8) on the same quantized operands, for context only
-    cublas = None
-    if args.compare_cublas:
-        try:
-            tot = 0.0
-            for i, L in enumerate(layers):
-                if L.K % 16:
-                    raise ValueError("K not a multiple of 16")
-                qa, s_a = F.fp8_quantize_act(A[i])
-                a8 = qa[:, :L.K].view(torch.float8_e4m3fn)
-                b8 = Wq[i][0][:, :L.K].view(torch.float8_e4m3fn)
-                sa = s_a.expand(M).reshape(M, 1).contiguous()
-                sw = Wq[i][1].reshape(1, L.N).contiguous()
-                f = lambda a8=a8, b8=b8, sa=sa, sw=sw: torch._scaled_mm(a8, b8.t(), sa, sw,
-                                                                        out_dtype=torch.bfloat16)
-                tot += time_loop(torch, f, max(3, args.steps // 2), 2)
-            cublas = {"what": "torch._scaled_mm rowwise-scaled FP8 GEMM on the same operands (context)",
-                      "tflops": round(sum(gemm_flops) / (tot * 1e-3) / 1e12, 1), "ms_4_layers": round(tot, 4)}
-        except Exception as e:  # noqa: BLE001 - context only
-            cublas = {"unavailable": str(e)[:200]}
-
     # ---- decode GEMV: Mistral-7B layers, per-tensor scales, weight copies rotated past L2
     decode = None
     if not args.no_decode:
@@ -303,7 +282,7 @@ def run_ours(args, rank: int, world: int):
                          "1.4 GB of outputs across four layers"},
         "roofline": roofline, "kernels_ms": {"quantize_act(amax+cast)": [round(t, 4) for t in quant_ms],
                                              "gemm": [round(t, 4) for t in gemm_ms]},
-        "cublas_context": cublas, "decode": decode, "e2e": e2e, "gpu_launches": launches,
+        "decode": decode, "e2e": e2e, "gpu_launches": launches,
         "clocks": clk, "cpu_baseline": cpu,
     }
 
@@ -382,7 +361,6 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--compare-cublas", type=int, default=1)
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
