@@ -30,6 +30,7 @@ FP8_ERR_CUDA = 4
 FP8_ERR_TIMEOUT = 5
 FP8_ERR_UNSUPPORTED_DEVICE = 6
 FP8_QUANT_WORKSPACE_BYTES = 4352
+FP8_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -45,6 +46,7 @@ _SIGNATURES = {
     "fp8_scaled_mm": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _i64, _vp, _int, _vp, _vp, _i64, _vp]),
     "fp8_linear": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _sz, _vp]),
     "fp8_linear_channelwise": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _sz, _vp]),
+    "fp8_linear_noalloc": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _int, _vp, _vp, _i64, _vp]),
     "fp8_last_device_status": (_int, [_vp]),
     "fp8_status_string": (ctypes.c_char_p, [_int]),
 }
@@ -204,6 +206,25 @@ def fp8_linear(a, qw, s_w, bias=None, out=None, ws=None):
 def fp8_linear_channelwise(a, qw, s_w, bias=None, out=None, ws=None):
     """Dynamic W8A8 linear, per-output-channel weight scales s_w [N]."""
     return _linear("fp8_linear_channelwise", a, qw, s_w, bias, out, ws)
+
+
+def fp8_linear_noalloc(a, qw, s_w, per_channel: bool = False, bias=None, out=None):
+    """The linear without a workspace, for callers that cannot allocate device memory.
+
+    Uses the library's fixed scratch array (FP8_NOALLOC_SCRATCH_BYTES per GPU) instead of
+    a caller workspace; calls that overlap on the GPU share it and race. Only `out` (when
+    omitted) is allocated here, by torch, for convenience; pass `out` to allocate nothing.
+    """
+    torch = _torch()
+    _check_bf16_2d(a, "a")
+    M, K = a.shape
+    _check_fp8_2d(qw, K, "qw")
+    N = qw.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    _check(lib().fp8_linear_noalloc(a.data_ptr(), M, K, a.stride(0), qw.data_ptr(), N, qw.stride(0),
+                                    s_w.data_ptr(), int(per_channel), _ptr(bias), y.data_ptr(), y.stride(0),
+                                    _stream_ptr(a)), "fp8_linear_noalloc")
+    return y
 
 
 def fp8_last_device_status(stream=None) -> int:

@@ -395,3 +395,52 @@ FP8_API const char* fp8_status_string(fp8_status s) {
   }
   return "FP8_ERR_UNKNOWN";
 }
+
+// ---------------------------------------------------------------------------
+// fp8_linear_noalloc: the linear for callers that cannot allocate device memory
+// ---------------------------------------------------------------------------
+//
+// The scratch the linear needs (partial amax values, the activation scale and, on the GEMM
+// path, the quantized activations) lives in this fixed array instead of a caller workspace.
+// Every GPU that loads the library holds it until the process exits. Host code must not pass
+// the array's name to a kernel: on the host that name is only a stand-in for the symbol, so
+// its device address is looked up once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FP8_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {};
+
+// Device address of g_noalloc_scratch on the current device (looked up on first use).
+fp8_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return FP8_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return FP8_OK;
+}
+
+}  // namespace
+
+FP8_API fp8_status fp8_linear_noalloc(const void* a_bf16, int64_t M, int64_t K, int64_t lda, const uint8_t* qw,
+                                      int64_t N, int64_t ldqw, const float* s_w, int per_channel,
+                                      const void* bias_bf16, void* y_bf16, int64_t ldy, fp8_stream_t stream) {
+  if (per_channel != 0 && per_channel != 1) return FP8_ERR_INVALID_ARG;
+  FP8_TRY(check_bf16_mat(a_bf16, M, K, lda));
+  FP8_TRY(check_fp8_mat(qw, N, K, ldqw));
+  FP8_TRY(check_bf16_mat(y_bf16, M, N, ldy));
+  if (M == 0 || N == 0)
+    return linear_impl(a_bf16, M, K, lda, qw, N, ldqw, s_w, per_channel, bias_bf16, y_bf16, ldy, nullptr, 0, stream);
+  // shapes whose scratch would not fit are refused before anything is enqueued
+  if (linear_ws_bytes(M, K) > size_t(FP8_NOALLOC_SCRATCH_BYTES)) return FP8_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  FP8_TRY(noalloc_scratch(&scratch));
+  return linear_impl(a_bf16, M, K, lda, qw, N, ldqw, s_w, per_channel, bias_bf16, y_bf16, ldy, scratch,
+                     size_t(FP8_NOALLOC_SCRATCH_BYTES), stream);
+}

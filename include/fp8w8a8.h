@@ -149,6 +149,37 @@ fp8_status fp8_linear_channelwise(const void* a_bf16, int64_t M, int64_t K, int6
                                   void* ws, size_t ws_bytes, fp8_stream_t stream);
 
 /*
+ * fp8_linear (per_channel == 0) or fp8_linear_channelwise (per_channel == 1)
+ * without a workspace argument, for callers that cannot allocate device memory:
+ * for example code that runs inside a host application which owns the whole
+ * device-memory budget and hands a kernel only its input and output buffers,
+ * or a latency-critical path that must not call cudaMalloc, which can block
+ * until other work on the device has finished. The source pages have no
+ * counterpart of this call; it exists only for such callers.
+ *
+ * The scratch lives in one fixed array inside the library of
+ * FP8_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads the library holds
+ * until the process exits. Decode shapes (fp8_uses_gemv) need 4352 bytes of
+ * it; GEMM shapes need fp8_workspace_bytes(M, K, N), so M * fp8_min_ld(K) may
+ * be at most FP8_NOALLOC_SCRATCH_BYTES - 4352. Larger shapes are refused with
+ * FP8_ERR_WORKSPACE before anything is enqueued. The call allocates nothing.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. All calls share the one array and it keeps the
+ * previous call's contents: nothing in it has to start at zero (each call
+ * writes every scratch byte it reads before reading it), but two calls whose
+ * kernels overlap on the GPU — on different streams or from different host
+ * threads — race on it and give wrong results. Order such calls on one stream.
+ * Arguments and every other rule are those of fp8_linear.
+ */
+#define FP8_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+fp8_status fp8_linear_noalloc(const void* a_bf16, int64_t M, int64_t K, int64_t lda,
+                              const uint8_t* qw, int64_t N, int64_t ldqw, const float* s_w,
+                              int per_channel, const void* bias_bf16, void* y_bf16, int64_t ldy,
+                              fp8_stream_t stream);
+
+/*
  * Synchronizes `stream`, then reports and clears device-side errors recorded
  * by the library's kernels on the current device since the last query
  * (FP8_ERR_TIMEOUT when a bounded wait expired), or FP8_ERR_CUDA when the
