@@ -190,11 +190,13 @@ def _linear(fn_name: str, a, qw, s_w, bias, out, ws):
     _check_fp8_2d(qw, K, "qw")
     N = qw.shape[0]
     y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    L = lib()
     if ws is None:
-        ws = workspace(M, K, N, a.device)
-    fn = getattr(lib(), fn_name)
+        need = L.fp8_workspace_bytes(M, K, N)
+        ws = workspace(M, K, N, a.device) if need else None
+    fn = getattr(L, fn_name)
     _check(fn(a.data_ptr(), M, K, a.stride(0), qw.data_ptr(), N, qw.stride(0), s_w.data_ptr(), _ptr(bias),
-              y.data_ptr(), y.stride(0), ws.data_ptr(), ws.numel(), _stream_ptr(a)), fn_name)
+              y.data_ptr(), y.stride(0), _ptr(ws), 0 if ws is None else ws.numel(), _stream_ptr(a)), fn_name)
     return y
 
 

@@ -6,8 +6,11 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "fp8w8a8.h"
 #include "device_common.cuh"
@@ -72,6 +75,13 @@ int64_t round_up16(int64_t k) { return (k + 15) / 16 * 16; }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Passes `e` through; with FP8W8A8_DEBUG set, a failure is also described on stderr.
+cudaError_t report_cuda(cudaError_t e, const char* where) {
+  static const bool debug = std::getenv("FP8W8A8_DEBUG") != nullptr;
+  if (e != cudaSuccess && debug) std::fprintf(stderr, "fp8w8a8: %s: %s\n", where, cudaGetErrorString(e));
+  return e;
+}
+
 // ---------------------------------------------------------------------------
 // launch helpers
 // ---------------------------------------------------------------------------
@@ -100,7 +110,8 @@ fp8_status launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, 
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+  return report_cuda(cudaLaunchKernelEx(&cfg, kernel, args...), "kernel launch") == cudaSuccess ? FP8_OK
+                                                                                       : FP8_ERR_CUDA;
 }
 
 struct BF16Mat {
@@ -142,38 +153,138 @@ fp8_status launch_fill_bias(const void* bias, void* y, int64_t M, int64_t N, int
                 static_cast<const uint16_t*>(bias), static_cast<uint16_t*>(y), M, N, ldy, 1);
 }
 
-template <int NT, bool kDyn>
-fp8_status launch_gemv_t(const gemv::Params& p, dim3 grid, int cluster_y, size_t smem, cudaStream_t st) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    const size_t max_smem = size_t(NT) * 8 * (gemv::kMaxSlice + 64) + gemv::kRowsPerCta * gemv::kMaxTokens * 4;
-    if (cudaFuncSetAttribute(gemv::gemv_kernel<NT, kDyn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(max_smem)) != cudaSuccess)
-      return FP8_ERR_CUDA;
-    attr_done = true;
-  }
-  return launch(gemv::gemv_kernel<NT, kDyn>, grid, dim3(gemv::kThreads), smem, st, true, dim3(1, cluster_y, 1), p);
+gemv::Params gemv_params(const uint8_t* qa, int64_t ldqa, const float* s_a, const float* s_w, int per_channel,
+                         const void* bias, void* y, int64_t ldy, int64_t M, int64_t N, int64_t K) {
+  gemv::Params p = {};
+  p.qa = qa;
+  p.ldqa = ldqa;
+  p.s_a = s_a;
+  p.s_w = s_w;
+  p.per_channel = per_channel;
+  p.bias = static_cast<const uint16_t*>(bias);
+  p.y = static_cast<uint16_t*>(y);
+  p.ldy = ldy;
+  p.M = int(M);
+  p.N = int(N);
+  p.K = int(K);
+  return p;
 }
 
-// Split-K GEMV: a 128-row block per cluster, its K split over up to 8 CTAs so that the grid
-// is about two CTAs deep per SM, each CTA keeping >= 4 chunks (256 bytes) of K.
-fp8_status launch_gemv(gemv::Params p, bool dynamic, int sms, cudaStream_t st) {
-  const int row_blocks = (p.N + gemv::kRowsPerCta - 1) / gemv::kRowsPerCta;
-  const int kchunks = int((round_up16(p.K) + gemv::kChunk - 1) / gemv::kChunk);
-  const int max_slice_chunks = gemv::kMaxSlice / gemv::kChunk;
-  int S = std::max(1, std::min(gemv::kMaxCluster, (2 * sms + row_blocks - 1) / row_blocks));
-  S = std::min(S, std::max(1, kchunks / 4));
-  S = std::max(S, (kchunks + max_slice_chunks - 1) / max_slice_chunks);
-  const int slice_chunks = std::max(1, (kchunks + S - 1) / S);
-  S = std::max(1, (kchunks + slice_chunks - 1) / slice_chunks);  // no CTA without work
-  p.kslice = slice_chunks * gemv::kChunk;
-  p.act_stride = (p.kslice % 128 == 0) ? p.kslice + 64 : p.kslice;
+// Dynamic shared memory the GEMV may use: the device's opt-in per-block limit minus the
+// kernel's static shared memory (set as the kernel attribute on first use; cached).
+const void* gemv_fn(int NT, bool dyn) {
+  if (NT == 1) return dyn ? reinterpret_cast<const void*>(gemv::gemv_kernel<1, true>)
+                          : reinterpret_cast<const void*>(gemv::gemv_kernel<1, false>);
+  return dyn ? reinterpret_cast<const void*>(gemv::gemv_kernel<2, true>)
+             : reinterpret_cast<const void*>(gemv::gemv_kernel<2, false>);
+}
+
+int gemv_smem_limit(int NT, bool dyn) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, bool>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(std::make_tuple(dev, NT, dyn));
+  if (it != cache.end()) return it->second;
+  const void* fn = gemv_fn(NT, dyn);
+  int optin = 0;
+  cudaFuncAttributes fa = {};
+  int limit = 0;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+      cudaFuncGetAttributes(&fa, fn) == cudaSuccess) {
+    limit = std::min(optin - int(fa.sharedSizeBytes), gemv::kSmemLimit);
+    if (report_cuda(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, limit),
+                    "gemv smem attribute") != cudaSuccess)
+      limit = 0;
+  }
+  cache[std::make_tuple(dev, NT, dyn)] = limit;
+  return limit;
+}
+
+// Largest number of co-resident clusters of `S` CTAs for the GEMV at `smem` bytes (cached).
+int gemv_max_clusters(int NT, bool dyn, int S, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, bool, int, size_t>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, NT, dyn, S, smem);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  const void* fn = gemv_fn(NT, dyn);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(S * 64);
+  cfg.blockDim = dim3(gemv::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (report_cuda(cudaOccupancyMaxActiveClusters(&n, fn, &cfg), "gemv cluster occupancy") != cudaSuccess) n = 0;
+  cache[key] = n;
+  return n;
+}
+
+// Persistent split-K GEMV on e4m3 activations. Picks the cluster size S (K split) and the
+// number of clusters C so that the CTA with the most work streams as few 16 KB weight tiles
+// as possible, every cluster holds at most kMaxRowBlocks row blocks, and the smem fits.
+fp8_status launch_gemv(gemv::Params p, bool dyn, const uint8_t* qw, int64_t ldqw, cudaStream_t st) {
+  using namespace gemv;
+  const int R = (p.N + kRows - 1) / kRows;
+  const int KT = (p.K + kTileK - 1) / kTileK;
+  int best_cost = -1, bS = 1, bC = 1, bstages = kMaxStages, bslice = kTileK;
+  size_t bsmem = 0;
   const int NT = p.M <= 8 ? 1 : 2;
-  const size_t smem = size_t(NT) * 8 * p.act_stride + gemv::kRowsPerCta * gemv::kMaxTokens * 4;
-  const dim3 grid(row_blocks, S);
+  const int smem_limit = gemv_smem_limit(NT, dyn);
+  for (int S : {1, 2, 4, 8}) {
+    if (S > KT) break;
+    const int slice_tiles = (KT + S - 1) / S;
+    if ((KT + slice_tiles - 1) / slice_tiles != S) continue;  // every rank must own tiles
+    const int kslice = slice_tiles * kTileK;
+    if (kslice > kMaxSlice) continue;
+    const int act_stride = kslice % 128 == 0 ? kslice + 64 : kslice;
+    int stages = kMaxStages;
+    auto smem_for = [&](int stg, int nrb) { return size_t(layout(stg, act_stride, nrb).total) + 1024; };
+    while (stages > kMinStages && smem_for(stages, kMaxRowBlocks) > size_t(smem_limit)) --stages;
+    if (smem_for(stages, kMaxRowBlocks) > size_t(smem_limit)) continue;
+    const int cmax = gemv_max_clusters(NT, dyn, S, smem_for(stages, kMaxRowBlocks));
+    if (cmax <= 0) continue;
+    int C = std::min(cmax, R);
+    const int nrb = (R + C - 1) / C;
+    if (nrb > kMaxRowBlocks) continue;
+    C = (R + nrb - 1) / nrb;
+    const int cost = nrb * slice_tiles;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      bS = S;
+      bC = C;
+      bstages = stages;
+      bslice = kslice;
+      bsmem = smem_for(stages, nrb);
+    }
+  }
+  if (best_cost < 0) {
+    report_cuda(cudaErrorInvalidConfiguration, "no GEMV configuration fits");
+    return FP8_ERR_CUDA;
+  }
+  p.kslice = bslice;
+  p.act_stride = bslice % 128 == 0 ? bslice + 64 : bslice;
+  p.stages = bstages;
+  p.row_blocks = R;
+  p.num_clusters = bC;
+  CUtensorMap map;
+  if (!make_fp8_tensor_map(&map, qw, p.N, p.K, ldqw, kRows)) return FP8_ERR_CUDA;
+  const dim3 grid(bC * bS), block(kThreads), cl(bS, 1, 1);
   if (NT == 1)
-    return dynamic ? launch_gemv_t<1, true>(p, grid, S, smem, st) : launch_gemv_t<1, false>(p, grid, S, smem, st);
-  return dynamic ? launch_gemv_t<2, true>(p, grid, S, smem, st) : launch_gemv_t<2, false>(p, grid, S, smem, st);
+    return dyn ? launch(gemv_kernel<1, true>, grid, block, bsmem, st, true, cl, map, p)
+               : launch(gemv_kernel<1, false>, grid, block, bsmem, st, true, cl, map, p);
+  return dyn ? launch(gemv_kernel<2, true>, grid, block, bsmem, st, true, cl, map, p)
+             : launch(gemv_kernel<2, false>, grid, block, bsmem, st, true, cl, map, p);
 }
 
 // ---------------------------------------------------------------------------
@@ -210,10 +321,11 @@ fp8_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
     if (_s != FP8_OK) return _s;       \
   } while (0)
 
+// Decode shapes need no workspace (the GEMV quantizes A itself); the GEMM path holds the
+// partial amax values, s_a and qA [M, round_up(K, 16)].
 size_t linear_ws_bytes(int64_t M, int64_t K) {
-  size_t b = FP8_QUANT_WORKSPACE_BYTES;
-  if (M > 0 && K > 0 && !use_gemv(M, K)) b += size_t(M) * size_t(round_up16(K));
-  return b;
+  if (M <= 0 || K <= 0 || use_gemv(M, K)) return 0;
+  return FP8_QUANT_WORKSPACE_BYTES + size_t(M) * size_t(round_up16(K));
 }
 
 fp8_status linear_impl(const void* a, int64_t M, int64_t K, int64_t lda, const uint8_t* qw, int64_t N,
@@ -235,30 +347,18 @@ fp8_status linear_impl(const void* a, int64_t M, int64_t K, int64_t lda, const u
   float* partials = reinterpret_cast<float*>(wsb);
   float* s_a = reinterpret_cast<float*>(wsb + kWsScaleOffset);
   const BF16Mat A{static_cast<const uint16_t*>(a), M, K, lda};
-  const int g = amax_grid(A, sms);
-  FP8_TRY(launch_amax(A, partials, g, st, true));
-
   if (use_gemv(M, K)) {
-    gemv::Params p = {};
-    p.a = a;
+    // decode: one persistent GEMV kernel quantizes A (cluster-wide amax) and streams qW
+    gemv::Params p = gemv_params(nullptr, 0, nullptr, s_w, per_channel, bias, y, ldy, M, N, K);
+    p.a = A.p;
     p.lda = lda;
-    p.partials = partials;
-    p.n_partials = g;
-    p.qw = qw;
-    p.ldqw = ldqw;
-    p.s_w = s_w;
-    p.per_channel = per_channel;
-    p.bias = static_cast<const uint16_t*>(bias);
-    p.y = static_cast<uint16_t*>(y);
-    p.ldy = ldy;
-    p.M = int(M);
-    p.N = int(N);
-    p.K = int(K);
     p.vec_a = A.vec();
-    return launch_gemv(p, true, sms, st);
+    return launch_gemv(p, true, qw, ldqw, st);
   }
   uint8_t* qa = wsb + kWsQaOffset;
   const int64_t ldqa = round_up16(K);
+  const int g = amax_grid(A, sms);
+  FP8_TRY(launch_amax(A, partials, g, st, true));
   FP8_TRY(launch_cast(A, partials, g, s_a, qa, ldqa, sms, st, true));
   if (gemm_launch(qa, ldqa, s_a, qw, ldqw, s_w, per_channel, static_cast<const uint16_t*>(bias),
                   static_cast<uint16_t*>(y), ldy, int(M), int(N), int(K), sms, st) != 0)
@@ -340,23 +440,9 @@ FP8_API fp8_status fp8_scaled_mm(const uint8_t* qa, int64_t M, int64_t K, int64_
   FP8_TRY(current_device(&sms));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (K == 0) return launch_fill_bias(bias_bf16, y_bf16, M, N, ldy, sms, st);
-  if (use_gemv(M, K)) {
-    gemv::Params p = {};
-    p.a = qa;
-    p.lda = ldqa;
-    p.s_a = s_a;
-    p.qw = qw;
-    p.ldqw = ldqw;
-    p.s_w = s_w;
-    p.per_channel = per_channel;
-    p.bias = static_cast<const uint16_t*>(bias_bf16);
-    p.y = static_cast<uint16_t*>(y_bf16);
-    p.ldy = ldy;
-    p.M = int(M);
-    p.N = int(N);
-    p.K = int(K);
-    return launch_gemv(p, false, sms, st);
-  }
+  if (use_gemv(M, K))
+    return launch_gemv(gemv_params(qa, ldqa, s_a, s_w, per_channel, bias_bf16, y_bf16, ldy, M, N, K), false, qw,
+                       ldqw, st);
   if (fp8k::gemm_launch(qa, ldqa, s_a, qw, ldqw, s_w, per_channel, static_cast<const uint16_t*>(bias_bf16),
                         static_cast<uint16_t*>(y_bf16), ldy, int(M), int(N), int(K), sms, st) != 0)
     return FP8_ERR_CUDA;
@@ -378,7 +464,11 @@ FP8_API fp8_status fp8_linear_channelwise(const void* a_bf16, int64_t M, int64_t
 
 FP8_API fp8_status fp8_last_device_status(fp8_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8_ERR_CUDA;
-  const unsigned int e = fp8k::gemm_read_and_clear_error();
+  unsigned int e = fp8k::gemm_read_and_clear_error();
+  unsigned int ge = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&ge, gemv::g_gemv_error, sizeof(ge)) == cudaSuccess)
+    cudaMemcpyToSymbol(gemv::g_gemv_error, &zero, sizeof(zero));
+  e |= ge;
   if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
   return (e & kErrTimeout) ? FP8_ERR_TIMEOUT : FP8_OK;
 }

@@ -95,6 +95,19 @@ __device__ __forceinline__ float block_max_partials(const float* __restrict__ pa
   return m;
 }
 
+// Eight bf16 of row `row` starting at column k (k a multiple of 8), zero beyond K.
+__device__ __forceinline__ uint4 load8_bf16(const uint16_t* row, int k, int K, int vec) {
+  if (vec && k + 8 <= K) return ld_nc_v4(row + k);
+  uint32_t w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t lo = (k + 2 * j < K) ? row[k + 2 * j] : 0u;
+    const uint32_t hi = (k + 2 * j + 1 < K) ? row[k + 2 * j + 1] : 0u;
+    w[j] = lo | (hi << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch
 // ---------------------------------------------------------------------------

@@ -312,10 +312,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     }
   }
 
+  __syncwarp();
   tmem_fence_before();
   __syncthreads();
   tmem_fence_after();
   if (warp == 1) {
+    __syncwarp();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem_base), "n"(kTmemCols) : "memory");
   }
 }
@@ -345,8 +347,12 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
+}  // namespace
+
+namespace fp8k {
+
 // 2-D e4m3 tensor map: [rows, K] with row stride ld bytes, box [box_rows, 128 bytes], 128B swizzle.
-bool make_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t K, int64_t ld, uint32_t box_rows) {
+bool make_fp8_tensor_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t K, int64_t ld, uint32_t box_rows) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
@@ -357,10 +363,6 @@ bool make_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t K, in
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-}  // namespace
-
-namespace fp8k {
 
 int gemm_launch(const uint8_t* qa, int64_t ldqa, const float* s_a, const uint8_t* qw, int64_t ldqw,
                 const float* s_w, int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy,
@@ -373,7 +375,7 @@ int gemm_launch(const uint8_t* qa, int64_t ldqa, const float* s_a, const uint8_t
     attr_done = true;
   }
   CUtensorMap ma, mb;
-  if (!make_map(&ma, qa, M, K, ldqa, BM) || !make_map(&mb, qw, N, K, ldqw, BN)) return 2;
+  if (!make_fp8_tensor_map(&ma, qa, M, K, ldqa, BM) || !make_fp8_tensor_map(&mb, qw, N, K, ldqw, BN)) return 2;
 
   GemmParams p;
   p.M = M;

@@ -1,6 +1,7 @@
 // Internal interface between the C-ABI layer and the tcgen05 GEMM translation unit.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -24,6 +25,11 @@ struct GemmParams {
 int gemm_launch(const uint8_t* qa, int64_t ldqa, const float* s_a, const uint8_t* qw, int64_t ldqw,
                 const float* s_w, int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy,
                 int M, int N, int K, int num_sms, cudaStream_t stream);
+
+// 2-D e4m3 tensor map over [rows, K] (row stride ld bytes), box [box_rows rows x 128 bytes],
+// 128-byte swizzle, zero fill outside the matrix. False when the encoder is unavailable or fails.
+bool make_fp8_tensor_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t K, int64_t ld,
+                         uint32_t box_rows);
 
 // Device-side error bits recorded by the GEMM kernel on the current device (read, then cleared).
 unsigned int gemm_read_and_clear_error();

@@ -2,24 +2,31 @@
 //
 // "[WIP] FP8 support": LLM decode runs at sequence length < 16 (the batch), which calls
 // for a custom gemv rather than a 16-padded GEMM. The weight matrix is streamed from HBM
-// exactly once; everything else is small.
+// exactly once.
 //
-// Decomposition. A CTA owns 128 weight rows (8 warps x 16 rows) and one K-slice. The
-// K-slices of one row block form a thread-block cluster (up to 8 CTAs); their fp32
-// partial sums are combined through distributed shared memory in a fixed order, so the
-// result is deterministic and no global scratch is needed.
+// Dynamic activation quantization happens inside this kernel: the ranks of a cluster
+// together cover all of K, so each rank's max |A| over its own K-slice, combined across the
+// cluster through distributed shared memory, is the global amax. Every CTA derives the same
+// s_a = amax / 448 and quantizes only its own slice, straight from the registers that
+// loaded it, while its TMA ring is already filling with weights. With pre-quantized
+// activations (fp8_scaled_mm) qA and s_a are read instead.
 //
-// Tensor-core mapping (mma.sync m16n8k32, e4m3 x e4m3 -> f32): W rows are the MMA's M
-// dimension, tokens its N dimension (one n8 tile for M <= 8, two for M <= 16). The sum over
-// k is order-free, so the k order inside each 64-byte chunk is permuted such that a lane
-// (group g, thread t) feeds both MMAs of the chunk from ONE 16-byte load of W row g
-// (bytes 16t..16t+15) and one of row g+8: weights are read with fully used 16-byte loads
-// straight into registers. The activation fragment uses the same permutation, which is
-// simply row-major [token][k] in shared memory.
+// Work split. Rows of W come in blocks of 128; K is split over the S CTAs of a
+// thread-block cluster (rank r owns K-range [r*kslice, (r+1)*kslice)). The grid is
+// persistent: cluster c processes row blocks c, c + C, c + 2C, ... with C chosen on the
+// host so every CTA streams the same number of tiles. Each CTA keeps the fp32 partial sums
+// of its row blocks in shared memory; at the end one cluster barrier publishes them and
+// rank r reduces its share of the rows over all ranks in a fixed order (deterministic,
+// no global scratch), applies the scale/bias epilogue and writes Y.
 //
-// Activations: with the dynamic path each CTA quantizes its own K-slice of A into shared
-// memory (scale from the partial amax values the amax kernel left in the workspace).
-// Weight loads for the first chunks are issued before waiting on the preceding kernel.
+// Streaming. Warp 8 is a TMA producer: 2-D tensor-map loads of [128 rows x 128 B] weight
+// tiles (128B-swizzled, 16 KB) into an mbarrier ring of up to 8 stages, issued from kernel
+// entry — before the wait on the preceding (quantize) kernel — so up to 128 KB per SM is in
+// flight at once. Warps 0..7 (16 rows each) read their rows from the tile and run
+// mma.sync m16n8k32 e4m3 x e4m3 -> f32 with W rows as the MMA's M dimension and tokens as
+// its N dimension. The k order inside each 64-byte half-row is permuted so that a lane
+// (group g, thread t) takes one 16-byte load of row g and one of row g+8 per half; the
+// activation fragment uses the same permutation, which is plain row-major [token][k].
 #pragma once
 
 #include "device_common.cuh"
@@ -27,33 +34,59 @@
 namespace fp8k {
 namespace gemv {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kRowsPerCta = kWarps * 16;
-constexpr int kChunk = 64;        // bytes of K consumed per lane-group step (two k32 MMAs)
-constexpr int kUnroll = 4;        // chunks per register group
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + one producer warp
+constexpr int kConsumerThreads = 32 * kConsumerWarps;
+constexpr int kRows = 16 * kConsumerWarps;            // 128 rows per row block
+constexpr int kTileK = 128;                           // bytes of K per tile (one swizzle row)
+constexpr int kTileBytes = kRows * kTileK;            // 16 KB
+constexpr int kMaxStages = 8;
+constexpr int kMinStages = 4;
 constexpr int kMaxTokens = 16;
 constexpr int kMaxCluster = 8;
-constexpr int kMaxSlice = 4096;   // bytes of K per CTA (shared-memory bound)
+constexpr int kMaxRowBlocks = 8;                      // per cluster (partials live in smem)
+constexpr int kPartBytes = kRows * kMaxTokens * 4;    // 8 KB per row block
+constexpr int kMaxSlice = 4096;                       // bytes of K per rank
+constexpr int kSmemLimit = 227 * 1024;
+constexpr int kRegUnits = 8;  // 8-element units of A a consumer thread keeps in registers
+
+// Device error bits of the GEMV (bounded waits that expired), read by fp8_last_device_status.
+__device__ unsigned int g_gemv_error;
 
 struct Params {
-  const void* a;            // bf16 [M, lda] (dynamic) or e4m3 [M, lda] (pre-quantized)
+  const uint8_t* qa;   // pre-quantized: e4m3 [M, ldqa], bytes [K, ldqa) zero
+  int64_t ldqa;
+  const float* s_a;    // pre-quantized: activation scale (device)
+  const uint16_t* a;   // dynamic: bf16 [M, lda]
   int64_t lda;
-  const float* partials;    // dynamic: partial amax values
-  int n_partials;
-  const float* s_a;         // pre-quantized: activation scale (device)
-  const uint8_t* qw;        // e4m3 [N, ldqw]
-  int64_t ldqw;
-  const float* s_w;         // [1] or [N]
+  int vec_a;           // dynamic: A rows allow 16-byte loads
+  const float* s_w;    // [1] or [N]
   int per_channel;
-  const uint16_t* bias;     // bf16 [N] or null
-  uint16_t* y;              // bf16 [M, ldy]
+  const uint16_t* bias;  // bf16 [N] or null
+  uint16_t* y;           // bf16 [M, ldy]
   int64_t ldy;
   int M, N, K;
-  int kslice;               // bytes of K per CTA, multiple of kChunk
-  int act_stride;           // shared-memory row stride of the activation tile (== 64 mod 128)
-  int vec_a;                // bf16 A rows allow 16-byte loads
+  int kslice;          // bytes of K per rank, multiple of kTileK
+  int act_stride;      // smem row stride of the activation slice (== 64 mod 128)
+  int stages;          // ring depth
+  int row_blocks;      // ceil(N / kRows)
+  int num_clusters;    // C
 };
+
+// Shared-memory layout (from a 1024-aligned base): ring | act | partials | barriers.
+struct Layout {
+  uint32_t ring, act, part, bars, total;
+};
+
+__host__ __device__ inline Layout layout(int stages, int act_stride, int rb_per_cluster) {
+  Layout L;
+  L.ring = 0;
+  L.act = stages * kTileBytes;
+  L.part = L.act + kMaxTokens * act_stride;
+  L.bars = L.part + rb_per_cluster * kPartBytes;
+  L.total = L.bars + 2 * kMaxStages * 8;
+  return L;
+}
 
 __device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -70,16 +103,19 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
   return v;
 }
 
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t local_addr, uint32_t rank) {
   uint32_t remote;
-  float v;
+  float4 v;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote) : "memory");
   return v;
 }
 
+// Cluster-wide barrier (release/acquire); the non-aligned form tolerates diverged warps.
 __device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  __syncwarp();
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -94,160 +130,256 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
   return r;
 }
 
-// One group of kUnroll chunks of W for rows g and g+8 of this warp's 16-row tile.
-struct WGroup {
-  uint4 lo[kUnroll];  // row g
-  uint4 hi[kUnroll];  // row g + 8
-};
-
-// Loads chunk u of the group at slice offset kbyte0 + u*kChunk when that offset is < lim.
-__device__ __forceinline__ void load_wgroup(WGroup& w, const uint8_t* row_lo, const uint8_t* row_hi,
-                                            bool ok_lo, bool ok_hi, int kbyte0, int lim) {
-#pragma unroll
-  for (int u = 0; u < kUnroll; ++u) {
-    const int k = kbyte0 + u * kChunk;
-    const bool in_k = k < lim;
-    w.lo[u] = (ok_lo && in_k) ? ld_nc_v4(row_lo + k) : make_uint4(0, 0, 0, 0);
-    w.hi[u] = (ok_hi && in_k) ? ld_nc_v4(row_hi + k) : make_uint4(0, 0, 0, 0);
-  }
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
 }
 
-template <int NT>
-__device__ __forceinline__ void mma_wgroup(float (&acc)[NT][4], const WGroup& w, uint32_t act_base,
-                                           int act_stride, int chunk0, int nchunks) {
-#pragma unroll
-  for (int u = 0; u < kUnroll; ++u) {
-    if (chunk0 + u < nchunks) {  // warp-uniform
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const uint4 b = lds_v4(act_base + nt * 8 * act_stride + (chunk0 + u) * kChunk);
-        mma_e4m3(acc[nt], w.lo[u].x, w.hi[u].x, w.lo[u].y, w.hi[u].y, b.x, b.y);
-        mma_e4m3(acc[nt], w.lo[u].z, w.hi[u].z, w.lo[u].w, w.hi[u].w, b.z, b.w);
-      }
-    }
-  }
+// Split-phase cluster barrier: every thread of every CTA arrives once per phase and waits
+// before arriving again.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+
+__device__ __forceinline__ void consumer_bar_sync() {
+  asm volatile("bar.sync 1, %0;" :: "n"(kConsumerThreads) : "memory");
 }
 
-// NT: number of n8 token tiles (1: M <= 8, 2: M <= 16). kDynamic: A is bf16 and is
-// quantized here with the scale derived from the partial amax values; otherwise A is
-// already e4m3 and s_a is read from memory.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y) : "memory");
+}
+
+// NT: n8 token tiles (1: M <= 8, 2: M <= 16). kDynamic: A is bf16 and quantized here.
 template <int NT, bool kDynamic>
-__global__ void __launch_bounds__(kThreads)
-gemv_kernel(const __grid_constant__ Params p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ float red[kWarps];
-  __shared__ float s_a_sh;
+__global__ void __launch_bounds__(kThreads, 1)
+gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ Params p) {
+  unsigned int* err = &g_gemv_error;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
 
-  uint8_t* act = smem;  // [NT*8][act_stride] e4m3
-  float* part = reinterpret_cast<float*>(smem + NT * 8 * p.act_stride);  // [128][16] fp32 partial sums
+  const uint32_t rank = cluster_ctarank(), nrank = cluster_nctarank();
+  const int cluster = blockIdx.x / nrank;
+  const int rb_count = (p.row_blocks - cluster + p.num_clusters - 1) / p.num_clusters;  // row blocks of this cluster
+  const Layout L = layout(p.stages, p.act_stride, rb_count);
+  const uint32_t ring = base + L.ring, act = base + L.act, part = base + L.part;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
 
+  const int k0 = int(rank) * p.kslice;
+  const int kspan = max(0, min(p.kslice, p.K - k0));
+  const int ntiles = (kspan + kTileK - 1) / kTileK;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int row_lo = blockIdx.x * kRowsPerCta + warp * 16 + g;
-  const int row_hi = row_lo + 8;
-  const int k0 = blockIdx.y * p.kslice;
-  const int kend16 = (p.K + 15) & ~15;                      // W bytes [K, kend16) are zero
-  const int klen = max(0, min(p.kslice, kend16 - k0));
-  const int nchunks = (klen + kChunk - 1) / kChunk;
 
-  pdl_trigger();
-
-  // --- weights do not depend on the preceding kernel: start streaming them now
-  const uint8_t* wlo = p.qw + (int64_t)row_lo * p.ldqw + k0 + 16 * t;
-  const uint8_t* whi = p.qw + (int64_t)row_hi * p.ldqw + k0 + 16 * t;
-  const bool ok_lo = row_lo < p.N, ok_hi = row_hi < p.N;
-  // a lane's 16-byte load at slice offset x is valid if x < lim: inside the row's K16
-  // bytes and inside this CTA's chunks (never prefetch the next slice's bytes)
-  const int lim = min(kend16 - k0, nchunks * kChunk) - 16 * t;
-  WGroup cur;
-  load_wgroup(cur, wlo, whi, ok_lo, ok_hi, 0, lim);
-
-  pdl_wait();
-
-  // --- activation scale
-  if constexpr (kDynamic) {
-    const float amax = block_max_partials(p.partials, p.n_partials, red);
-    if (threadIdx.x == 0) s_a_sh = scale_from_amax(amax);
-  } else {
-    if (threadIdx.x == 0) s_a_sh = *p.s_a;
+  __shared__ int abort_flag;
+  __shared__ float s_a_out;
+  __shared__ float slice_amax;
+  __shared__ float red[kConsumerWarps];
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kConsumerWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
-  const float s_a = s_a_sh;
+  pdl_trigger();
+  volatile int* ab = &abort_flag;
 
-  // --- stage this CTA's K-slice of the activations into shared memory as e4m3
-  {
-    const int span = nchunks * kChunk;
-    const int units_per_tok = span >> 3;  // 8 bytes per unit
-    const int units = NT * 8 * units_per_tok;
-    for (int i = threadIdx.x; i < units; i += kThreads) {
-      const int m = i / units_per_tok;
-      const int kk = (i - m * units_per_tok) << 3;
-      const int k = k0 + kk;
-      uint2 q = make_uint2(0, 0);
-      if (m < p.M && k < p.K) {
-        if constexpr (kDynamic) {
-          const uint16_t* src = static_cast<const uint16_t*>(p.a) + (int64_t)m * p.lda + k;
-          if (p.vec_a && k + 8 <= p.K) {
-            q = quant8_bf16(ld_nc_v4(src), s_a);
-          } else {
-            float x[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) x[j] = (k + j < p.K) ? bf16_bits_to_float(src[j]) : 0.0f;
-            q.x = quant4(x[0], x[1], x[2], x[3], s_a);
-            q.y = quant4(x[4], x[5], x[6], x[7], s_a);
-          }
-        } else {
-          // e4m3 rows: ld is a multiple of 16 and bytes [K, ld) are zero
-          q = *reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(p.a) + (int64_t)m * p.lda + k);
+  if (warp == kConsumerWarps) {
+    // ---------------- producer: weights never depend on the preceding kernel ----------------
+    cluster_arrive();  // phase 1 (the amax exchange) never waits for the weight stream
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
+      uint32_t it = 0;
+      bool ok = true;
+      for (int r = 0; r < rb_count && ok; ++r) {
+        const int rb = cluster + r * p.num_clusters;
+        for (int kt = 0; kt < ntiles; ++kt, ++it) {
+          const int s = it % p.stages;
+          const uint32_t ph = (it / p.stages) & 1u;
+          if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1u, ab, err)) { ok = false; break; }
+          mbar_arrive_expect_tx(full0 + 8 * s, kTileBytes);
+          tma_load_2d(ring + s * kTileBytes, &tmap_w, full0 + 8 * s, k0 + kt * kTileK, rb * kRows);
         }
       }
-      *reinterpret_cast<uint2*>(act + m * p.act_stride + kk) = q;
+      if (!ok) {  // let the copies already issued land before the CTA's memory is released
+        const uint32_t first = it > uint32_t(p.stages) ? it - p.stages : 0u;
+        for (uint32_t j = first; j < it; ++j)
+          mbar_wait_bounded(full0 + 8 * (j % p.stages), (j / p.stages) & 1u, nullptr, err);
+      }
+    }
+    __syncwarp();
+    cluster_wait();
+  } else {
+    // ---------------- consumers ----------------
+    pdl_wait();  // A (or qA and s_a) may come from the preceding kernel
+    const int span = ntiles * kTileK;  // bytes of K staged per token (zero beyond K)
+    float s_a;
+    if constexpr (kDynamic) {
+      // max |A| over this rank's slice; the first kRegUnits units per thread stay in registers
+      const int upt = span >> 3;  // 8-element units per token
+      const int units = p.M * upt;
+      uint4 v[kRegUnits];
+      uint32_t m2 = 0;
+#pragma unroll
+      for (int b = 0; b < kRegUnits; ++b) {
+        const int i = threadIdx.x + b * kConsumerThreads;
+        const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
+        v[b] = i < units ? load8_bf16(p.a + (int64_t)m * p.lda, k0 + kk, p.K, p.vec_a) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int b = 0; b < kRegUnits; ++b)
+        m2 = abs_max_u16x2(abs_max_u16x2(abs_max_u16x2(abs_max_u16x2(m2, v[b].x), v[b].y), v[b].z), v[b].w);
+      for (int i0 = threadIdx.x + kRegUnits * kConsumerThreads; i0 < units; i0 += kRegUnits * kConsumerThreads) {
+        uint4 w[kRegUnits];
+#pragma unroll
+        for (int b = 0; b < kRegUnits; ++b) {
+          const int i = i0 + b * kConsumerThreads;
+          const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
+          w[b] = i < units ? load8_bf16(p.a + (int64_t)m * p.lda, k0 + kk, p.K, p.vec_a) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int b = 0; b < kRegUnits; ++b)
+          m2 = abs_max_u16x2(abs_max_u16x2(abs_max_u16x2(abs_max_u16x2(m2, w[b].x), w[b].y), w[b].z), w[b].w);
+      }
+      float mx = warp_max(u16x2_max_to_float(m2));
+      if (lane == 0) red[warp] = mx;
+      consumer_bar_sync();
+      if (threadIdx.x == 0) {
+        for (int w = 1; w < kConsumerWarps; ++w) mx = fmaxf(mx, red[w]);
+        slice_amax = mx;
+      }
+      consumer_bar_sync();
+      cluster_arrive();  // phase 1: publish this rank's slice maximum
+      cluster_wait();
+      float amax = 0.0f;
+      for (uint32_t src = 0; src < nrank; ++src) amax = fmaxf(amax, ld_dsmem_f32(smem_u32(&slice_amax), src));
+      s_a = scale_from_amax(amax);
+      // quantize into act[token][k - k0]; units past K and tokens past M are plain zeros
+      auto put = [&](int i, const uint4& x) {
+        const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
+        uint2 q = make_uint2(0, 0);
+        if (k0 + kk < p.K) q = quant8_bf16(x, s_a);
+        asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(act + m * p.act_stride + kk), "r"(q.x), "r"(q.y)
+                     : "memory");
+      };
+#pragma unroll
+      for (int b = 0; b < kRegUnits; ++b) {
+        const int i = threadIdx.x + b * kConsumerThreads;
+        if (i < units) put(i, v[b]);
+      }
+      for (int i = threadIdx.x + kRegUnits * kConsumerThreads; i < units; i += kConsumerThreads) {
+        const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
+        put(i, load8_bf16(p.a + (int64_t)m * p.lda, k0 + kk, p.K, p.vec_a));
+      }
+      const int zu = span >> 4;  // 16-byte units per padding token
+      for (int i = threadIdx.x; i < (kMaxTokens - p.M) * zu; i += kConsumerThreads) {
+        const int m = p.M + i / zu;
+        const int kk = (i - (i / zu) * zu) << 4;
+        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" :: "r"(act + m * p.act_stride + kk), "r"(0u) : "memory");
+      }
+    } else {
+      cluster_arrive();  // phase 1 is unused here but keeps every thread's phases aligned
+      cluster_wait();
+      s_a = *p.s_a;
+      // activation slice [16 tokens][span] -> smem, zero beyond M and K
+      const int upt = span / 16;
+      const int units = kMaxTokens * upt;
+      const int k16 = (p.K + 15) & ~15;
+      for (int i = threadIdx.x; i < units; i += kConsumerThreads) {
+        const int m = i / upt;
+        const int kk = (i - m * upt) * 16;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (m < p.M && k0 + kk < k16) v = *reinterpret_cast<const uint4*>(p.qa + (int64_t)m * p.ldqa + k0 + kk);
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};"
+                     :: "r"(act + m * p.act_stride + kk), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+      }
+    }
+    if (threadIdx.x == 0) s_a_out = s_a;
+    consumer_bar_sync();
+
+    const int g = lane >> 2, t = lane & 3;
+    const uint32_t row_lo = (warp * 16 + g) * kTileK, row_hi = row_lo + 8 * kTileK;
+    const uint32_t act_lane = act + g * p.act_stride + 16 * t;
+    uint32_t it = 0;
+    for (int r = 0; r < rb_count; ++r) {
+      float acc[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+      for (int kt = 0; kt < ntiles; ++kt, ++it) {
+        const int s = it % p.stages;
+        const uint32_t ph = (it / p.stages) & 1u;
+        const bool ok = mbar_wait_bounded(full0 + 8 * s, ph, ab, err);
+        if (ok) {
+          const uint32_t tile = ring + s * kTileBytes;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            // 16-byte unit (4j + t) of rows g / g+8, at its 128B-swizzled position (row % 8 == g)
+            const uint32_t unit = uint32_t(((4 * j + t) ^ g) * 16);
+            const uint4 wlo = lds_v4(tile + row_lo + unit);
+            const uint4 whi = lds_v4(tile + row_hi + unit);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const uint4 b = lds_v4(act_lane + nt * 8 * p.act_stride + kt * kTileK + 64 * j);
+              mma_e4m3(acc[nt], wlo.x, whi.x, wlo.y, whi.y, b.x, b.y);
+              mma_e4m3(acc[nt], wlo.z, whi.z, wlo.w, whi.w, b.z, b.w);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      }
+      // partials of this row block: part[r][row][token]
+      float* pr = reinterpret_cast<float*>(smem + L.part + r * kPartBytes);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int row = warp * 16 + g, col = nt * 8 + 2 * t;
+        *reinterpret_cast<float2*>(pr + row * kMaxTokens + col) = make_float2(acc[nt][0], acc[nt][1]);
+        *reinterpret_cast<float2*>(pr + (row + 8) * kMaxTokens + col) = make_float2(acc[nt][2], acc[nt][3]);
+      }
     }
   }
-  __syncthreads();
 
-  // --- main loop: stream W, tensor-core dot products against the resident activations
-  float acc[NT][4];
+  cluster_sync_all();  // every rank's partials are written (and every TMA load consumed)
+
+  // ---------------- split-K reduction over the cluster + epilogue ----------------
+  if (warp < kConsumerWarps) {
+    const float s_a = s_a_out;
+    const int rows_per = (kRows + nrank - 1) / nrank;
+    const int r_begin = rank * rows_per;
+    const int r_count = max(0, min(kRows, r_begin + rows_per) - r_begin);
+    const int q_per_row = (p.M + 3) / 4;  // float4 groups of tokens
+    const int items = rb_count * r_count * q_per_row;
+    for (int i = threadIdx.x; i < items; i += kConsumerThreads) {
+      const int q = i % q_per_row;
+      const int rr = (i / q_per_row) % r_count;
+      const int r = i / (q_per_row * r_count);
+      const int row = r_begin + rr;
+      const int n = (cluster + r * p.num_clusters) * kRows + row;
+      if (n >= p.N) continue;
+      const uint32_t off = part + r * kPartBytes + (row * kMaxTokens + 4 * q) * 4;
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (uint32_t src = 0; src < nrank; ++src) {
+        const float4 v = ld_dsmem_v4(off, src);
+        sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+      }
+      const float sc = s_a * p.s_w[p.per_channel ? n : 0];
+      const float b = p.bias ? bf16_bits_to_float(p.bias[n]) : 0.0f;
+      const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
-  const uint32_t act_base = smem_u32(act) + g * p.act_stride + 16 * t;
-  for (int c = 0; c < nchunks; c += kUnroll) {
-    WGroup nxt;
-    const bool more = c + kUnroll < nchunks;
-    if (more) load_wgroup(nxt, wlo, whi, ok_lo, ok_hi, (c + kUnroll) * kChunk, lim);
-    mma_wgroup<NT>(acc, cur, act_base, p.act_stride, c, nchunks);
-    if (more) cur = nxt;
-  }
-
-  // --- partial sums -> shared memory: part[row][token]
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int r = warp * 16 + g, col = nt * 8 + 2 * t;
-    part[r * kMaxTokens + col] = acc[nt][0];
-    part[r * kMaxTokens + col + 1] = acc[nt][1];
-    part[(r + 8) * kMaxTokens + col] = acc[nt][2];
-    part[(r + 8) * kMaxTokens + col + 1] = acc[nt][3];
-  }
-  cluster_sync_all();
-
-  // --- split-K reduction across the cluster (fixed order) + epilogue
-  const uint32_t rank = cluster_ctarank(), nrank = cluster_nctarank();
-  const int rows_per = (kRowsPerCta + nrank - 1) / nrank;
-  const int r_begin = rank * rows_per;
-  const int r_count = max(0, min(kRowsPerCta, r_begin + rows_per) - r_begin);
-  const uint32_t part_base = smem_u32(part);
-  for (int i = threadIdx.x; i < r_count * p.M; i += kThreads) {
-    const int m = i / r_count;
-    const int rl = r_begin + (i - m * r_count);
-    const int n = blockIdx.x * kRowsPerCta + rl;
-    if (n >= p.N) continue;
-    const uint32_t off = (rl * kMaxTokens + m) * 4;
-    float sum = 0.0f;
-    for (uint32_t q = 0; q < nrank; ++q) sum += ld_dsmem_f32(part_base + off, q);
-    const float sw = p.s_w[p.per_channel ? n : 0];
-    const float b = p.bias ? bf16_bits_to_float(p.bias[n]) : 0.0f;
-    const float yv = fmaf(sum, s_a * sw, b);
-    p.y[(int64_t)m * p.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(yv));
+      for (int e = 0; e < 4; ++e) {
+        const int m = 4 * q + e;
+        if (m < p.M) p.y[(int64_t)m * p.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(fmaf(vals[e], sc, b)));
+      }
+    }
   }
   cluster_sync_all();  // peers may still be reading our partials
 }

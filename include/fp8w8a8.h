@@ -75,10 +75,11 @@ typedef enum fp8_status {
 /* Smallest valid leading dimension (bytes) of an FP8 matrix with K columns: K rounded up to 16 (16 for K == 0). */
 int64_t fp8_min_ld(int64_t K);
 
-/* Bytes of workspace fp8_linear / fp8_linear_channelwise need for this shape
- * (partial amax values, the activation scale and, when the shape runs on the
- * GEMM path, the quantized activations qA [M, fp8_min_ld(K)]). Always >=
- * FP8_QUANT_WORKSPACE_BYTES. Host-only, never touches the device. */
+/* Bytes of workspace fp8_linear / fp8_linear_channelwise need for this shape.
+ * 0 for decode shapes (fp8_uses_gemv): the GEMV quantizes A itself. GEMM
+ * shapes need FP8_QUANT_WORKSPACE_BYTES (partial amax values, s_a) plus the
+ * quantized activations qA [M, fp8_min_ld(K)]. 0 when M or K is 0. Host-only,
+ * never touches the device. */
 size_t fp8_workspace_bytes(int64_t M, int64_t K, int64_t N);
 
 /* 1 when fp8_linear takes the decode GEMV path for this shape, 0 for the GEMM path. Host-only. */
@@ -126,11 +127,12 @@ fp8_status fp8_scaled_mm(const uint8_t* qa, int64_t M, int64_t K, int64_t ldqa, 
  * The W8A8 linear with dynamic per-tensor activation quantization and a
  * per-tensor weight scale s_w[0]: amax(A) -> s_a -> e4m3(A/s_a) -> FP8 GEMM
  * (fp32 accumulate) -> s_a*s_w (+bias) epilogue -> bf16 Y.
- * Decode shapes (fp8_uses_gemv) run a split-K GEMV that quantizes A on the fly
- * ("[WIP] FP8 support": LLM decode runs at sequence length < 16 and wants a
- * custom gemv); larger M runs the tcgen05 GEMM. No padding or repacking of A,
- * W or Y happens on any path.
- * ws: >= fp8_workspace_bytes(M, K, N) bytes, 256-byte aligned.
+ * Decode shapes (fp8_uses_gemv) run one persistent split-K GEMV kernel that
+ * quantizes A itself and streams qW once ("[WIP] FP8 support": LLM decode runs
+ * at sequence length < 16 and wants a custom gemv); larger M runs amax + cast
+ * + the tcgen05 GEMM. No padding or repacking of A, W or Y happens on any path.
+ * ws: >= fp8_workspace_bytes(M, K, N) bytes, 256-byte aligned (may be NULL
+ * when that is 0).
  */
 fp8_status fp8_linear(const void* a_bf16, int64_t M, int64_t K, int64_t lda,
                       const uint8_t* qw, int64_t N, int64_t ldqw, const float* s_w,
@@ -159,9 +161,9 @@ fp8_status fp8_linear_channelwise(const void* a_bf16, int64_t M, int64_t K, int6
  *
  * The scratch lives in one fixed array inside the library of
  * FP8_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads the library holds
- * until the process exits. Decode shapes (fp8_uses_gemv) need 4352 bytes of
- * it; GEMM shapes need fp8_workspace_bytes(M, K, N), so M * fp8_min_ld(K) may
- * be at most FP8_NOALLOC_SCRATCH_BYTES - 4352. Larger shapes are refused with
+ * until the process exits. A call needs fp8_workspace_bytes(M, K, N) of it:
+ * nothing for decode shapes, and for GEMM shapes M * fp8_min_ld(K) may be at
+ * most FP8_NOALLOC_SCRATCH_BYTES - 4352. Larger shapes are refused with
  * FP8_ERR_WORKSPACE before anything is enqueued. The call allocates nothing.
  *
  * The first call on a device looks up the array's device address

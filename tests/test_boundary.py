@@ -66,15 +66,15 @@ def test_min_ld(L, K):
 
 def test_workspace_and_dispatch(L):
     base = F.FP8_QUANT_WORKSPACE_BYTES
-    # decode shapes run the GEMV: no activation buffer in the workspace
+    # decode shapes run the GEMV, which quantizes A itself: no workspace
     for M in (1, 2, 8, 15, 16):
         assert F.fp8_uses_gemv(M, 4096, 4096)
-        assert F.fp8_workspace_bytes(M, 4096, 4096) == base
-    # GEMM shapes hold qA [M, min_ld(K)]
+        assert F.fp8_workspace_bytes(M, 4096, 4096) == 0
+    # GEMM shapes hold the partial amax values, s_a and qA [M, min_ld(K)]
     for M, K in ((17, 4096), (16384, 14336), (100, 4100)):
         assert not F.fp8_uses_gemv(M, K, 4096)
         assert F.fp8_workspace_bytes(M, K, 4096) == base + M * F.min_ld(K)
-    assert F.fp8_workspace_bytes(0, 4096, 4096) == base
+    assert F.fp8_workspace_bytes(0, 4096, 4096) == 0
     assert not F.fp8_uses_gemv(4, 40000, 4096)  # K beyond the GEMV's slice budget -> GEMM
 
 
@@ -109,10 +109,10 @@ def test_linear_rejects_bad_arguments(L, channelwise):
     assert lin(L, qw=P + 8, **c) == F.FP8_ERR_MISALIGNED          # FP8 base not 16-byte aligned
     assert lin(L, a=P + 1, **c) == F.FP8_ERR_MISALIGNED           # bf16 base odd
     assert lin(L, bias=P + 1, **c) == F.FP8_ERR_MISALIGNED
-    assert lin(L, ws=None, **c) == F.FP8_ERR_WORKSPACE
-    assert lin(L, ws_bytes=100, **c) == F.FP8_ERR_WORKSPACE
-    assert lin(L, ws=WS + 16, **c) == F.FP8_ERR_WORKSPACE         # not 256-byte aligned
-    # GEMM-path shapes need room for qA
+    # GEMM-path shapes (M > 16) need a workspace with room for qA
+    assert lin(L, M=64, ws=None, **c) == F.FP8_ERR_WORKSPACE
+    assert lin(L, M=64, ws_bytes=100, **c) == F.FP8_ERR_WORKSPACE
+    assert lin(L, M=64, ws=WS + 16, **c) == F.FP8_ERR_WORKSPACE   # not 256-byte aligned
     need = F.fp8_workspace_bytes(64, 64, 32)
     assert lin(L, M=64, ws_bytes=need - 1, **c) == F.FP8_ERR_WORKSPACE
 

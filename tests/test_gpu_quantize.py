@@ -123,3 +123,19 @@ def test_quantization_is_deterministic():
     q2, s2 = F.fp8_quantize_act(a)
     torch.cuda.synchronize()
     assert torch.equal(q1, q2) and torch.equal(s1, s2)
+
+
+def test_all_bf16_values_under_many_scales():
+    """Every finite bf16 value at 40 scales (random amax and powers of two, whose quotients
+    land exactly on e4m3 rounding midpoints): codes and scale bit-exact."""
+    x = all_finite_bf16()
+    g = np.random.default_rng(21)
+    targets = [float(v) for v in g.standard_normal(28) * np.exp2(g.integers(-40, 40, 28))]
+    targets += [448.0 * 2.0 ** k for k in (-20, -9, -6, -3, -1, 0, 1, 2, 5, 9, 17, 30)]
+    for T in targets:
+        T = abs(float(torch.tensor(T).bfloat16().float()))
+        v = x[x.float().abs() <= T]
+        v = torch.cat([v, torch.tensor([T, -T], dtype=torch.bfloat16)])
+        pad = (-v.numel()) % 240
+        a = torch.cat([v, torch.zeros(pad, dtype=torch.bfloat16)]).view(-1, 240)
+        check_act(a, f"all bf16 with amax {T:g}")
