@@ -258,7 +258,11 @@ fp8_status launch_gemv(gemv::Params p, bool dyn, const uint8_t* qw, int64_t ldqw
     const int nrb = (R + C - 1) / C;
     if (nrb > kMaxRowBlocks) continue;
     C = (R + nrb - 1) / nrb;
-    const int cost = nrb * slice_tiles;
+    // streamed tiles of the busiest CTA, plus (dynamic mode) its activation prologue: each
+    // batch of kRegUnits A loads per consumer thread costs about as much as two weight tiles
+    const int units = p.M * (kslice / 8);
+    const int batches = dyn ? (units + kRegUnits * kConsumerThreads - 1) / (kRegUnits * kConsumerThreads) : 0;
+    const int cost = nrb * slice_tiles + 2 * (batches > 1 ? batches : 0);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       bS = S;

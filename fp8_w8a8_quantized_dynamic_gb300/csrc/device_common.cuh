@@ -27,20 +27,55 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   return r;
 }
 
-// Four values -> four e4m3fn bytes (x0 in the lowest byte). The quotient is the IEEE
-// round-to-nearest fp32 division, independent of compiler flags.
-__device__ __forceinline__ uint32_t quant4(float x0, float x1, float x2, float x3, float s) {
-  const uint32_t lo = cvt_e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
-  const uint32_t hi = cvt_e4m3x2(__fdiv_rn(x2, s), __fdiv_rn(x3, s));
-  return lo | (hi << 16);
+// Quantizer for one scale s: e4m3 codes of fl32(x / s), most of the time without a division.
+// y = x * fl32(1/s) carries two roundings, so |y - fl32(x/s)| < 3 ulp(y) (relative error at
+// most 3 * 2^-24 against an ulp of at least 2^-24 |y|). Rounding to e4m3 is monotone and
+// symmetric in sign, so when the magnitudes |y| - 4 ulp and |y| + 4 ulp (4 steps of the fp32
+// bit pattern, at least 2 ulp(y) in either direction) round to the same e4m3 magnitude, that
+// is the magnitude of the exact quotient's code and the sign comes from y. Otherwise the
+// quotient lies within a few ulps of an e4m3 rounding boundary and the IEEE division decides
+// (out of line, so the common path stays short). Scales below 2^-125, where 1/s could
+// overflow, always divide.
+struct Quantizer {
+  float s, r;
+  bool fast;
+};
+
+__device__ __forceinline__ Quantizer make_quantizer(float s) {
+  Quantizer q;
+  q.s = s;
+  q.r = __frcp_rn(s);
+  q.fast = s >= 0x1p-125f && q.r < 0x1p126f;
+  return q;
+}
+
+static __device__ __noinline__ uint32_t quant2_divide(float x0, float x1, float s) {
+  return cvt_e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+}
+
+// Two values -> two e4m3fn bytes (x0 in bits 0..7, x1 in bits 8..15).
+__device__ __forceinline__ uint32_t quant2(float x0, float x1, const Quantizer& q) {
+  if (q.fast) {
+    const uint32_t b0 = __float_as_uint(x0 * q.r), b1 = __float_as_uint(x1 * q.r);
+    const uint32_t a0 = b0 & 0x7FFFFFFFu, a1 = b1 & 0x7FFFFFFFu;
+    const uint32_t lo = cvt_e4m3x2(__uint_as_float(a0 > 4u ? a0 - 4u : 0u), __uint_as_float(a1 > 4u ? a1 - 4u : 0u));
+    const uint32_t hi = cvt_e4m3x2(__uint_as_float(a0 + 4u), __uint_as_float(a1 + 4u));
+    if (lo == hi) return lo | ((b0 >> 31) << 7) | ((b1 >> 31) << 15);
+  }
+  return quant2_divide(x0, x1, q.s);
+}
+
+// Four values -> four e4m3fn bytes (x0 in the lowest byte).
+__device__ __forceinline__ uint32_t quant4(float x0, float x1, float x2, float x3, const Quantizer& q) {
+  return quant2(x0, x1, q) | (quant2(x2, x3, q) << 16);
 }
 
 // Eight bf16 (packed in a uint4) -> eight e4m3fn bytes (uint2).
-__device__ __forceinline__ uint2 quant8_bf16(uint4 v, float s) {
+__device__ __forceinline__ uint2 quant8_bf16(uint4 v, const Quantizer& q) {
   auto f = [](uint32_t w, int hi) { return __uint_as_float(hi ? (w & 0xFFFF0000u) : (w << 16)); };
   uint2 r;
-  r.x = quant4(f(v.x, 0), f(v.x, 1), f(v.y, 0), f(v.y, 1), s);
-  r.y = quant4(f(v.z, 0), f(v.z, 1), f(v.w, 0), f(v.w, 1), s);
+  r.x = quant4(f(v.x, 0), f(v.x, 1), f(v.y, 0), f(v.y, 1), q);
+  r.y = quant4(f(v.z, 0), f(v.z, 1), f(v.w, 0), f(v.w, 1), q);
   return r;
 }
 

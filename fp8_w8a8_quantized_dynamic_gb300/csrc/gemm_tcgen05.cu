@@ -270,7 +270,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       // publishes the column tables; a set abort flag makes all epilogue warps leave together
       if (epi_bar_any(*abort_flag != 0)) break;
       // after a timeout, skip to the next barrier above, which ends the loop uniformly
-      if (!mbar_wait_bounded(smem_u32(&ctl->tfull[ab]), aph, abort_flag, &g_gemm_error)) continue;
+      // one lane waits and the warp follows its verdict: tcgen05.ld needs a converged warp
+      bool ok = lane == 0 ? mbar_wait_bounded(smem_u32(&ctl->tfull[ab]), aph, abort_flag, &g_gemm_error) : true;
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) continue;
       tmem_fence_after();
       const int m = m_idx * BM + row_in_tile;
       uint16_t* yrow = p.y + (int64_t)m * p.ldy;

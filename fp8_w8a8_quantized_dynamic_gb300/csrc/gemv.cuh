@@ -263,11 +263,12 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
       float amax = 0.0f;
       for (uint32_t src = 0; src < nrank; ++src) amax = fmaxf(amax, ld_dsmem_f32(smem_u32(&slice_amax), src));
       s_a = scale_from_amax(amax);
+      const Quantizer qz = make_quantizer(s_a);
       // quantize into act[token][k - k0]; units past K and tokens past M are plain zeros
       auto put = [&](int i, const uint4& x) {
         const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
         uint2 q = make_uint2(0, 0);
-        if (k0 + kk < p.K) q = quant8_bf16(x, s_a);
+        if (k0 + kk < p.K) q = quant8_bf16(x, qz);
         asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(act + m * p.act_stride + kk), "r"(q.x), "r"(q.y)
                      : "memory");
       };
@@ -276,9 +277,18 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
         const int i = threadIdx.x + b * kConsumerThreads;
         if (i < units) put(i, v[b]);
       }
-      for (int i = threadIdx.x + kRegUnits * kConsumerThreads; i < units; i += kConsumerThreads) {
-        const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
-        put(i, load8_bf16(p.a + (int64_t)m * p.lda, k0 + kk, p.K, p.vec_a));
+      // units beyond the register batch: reload kRegUnits at a time (independent loads)
+      for (int i0 = threadIdx.x + kRegUnits * kConsumerThreads; i0 < units; i0 += kRegUnits * kConsumerThreads) {
+        uint4 w[kRegUnits];
+#pragma unroll
+        for (int b = 0; b < kRegUnits; ++b) {
+          const int i = i0 + b * kConsumerThreads;
+          const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
+          w[b] = i < units ? load8_bf16(p.a + (int64_t)m * p.lda, k0 + kk, p.K, p.vec_a) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int b = 0; b < kRegUnits; ++b)
+          if (i0 + b * kConsumerThreads < units) put(i0 + b * kConsumerThreads, w[b]);
       }
       const int zu = span >> 4;  // 16-byte units per padding token
       for (int i = threadIdx.x; i < (kMaxTokens - p.M) * zu; i += kConsumerThreads) {

@@ -92,7 +92,7 @@ amax_partials_kernel(const uint16_t* __restrict__ a, int64_t rows, int64_t cols,
 // Quantize 16 consecutive elements of one row (columns c .. c+15) into 16 e4m3 bytes;
 // columns >= cols give 0x00.
 __device__ __forceinline__ uint4 quant16_row(const uint16_t* __restrict__ src, int64_t c, int64_t cols,
-                                             bool vec, float s) {
+                                             bool vec, const Quantizer& s) {
   uint4 out;
   if (vec && c + 16 <= cols) {
     const uint2 q0 = quant8_bf16(ld_v4(src), s);
@@ -120,8 +120,9 @@ cast_kernel(const uint16_t* __restrict__ a, int64_t rows, int64_t cols, int64_t 
   __shared__ float red[kQuantThreads / 32];
   if (pdl) pdl_trigger();
   pdl_wait();
-  const float s = scale_from_amax(block_max_partials(partials, n_partials, red));
-  if (blockIdx.x == 0 && threadIdx.x == 0) *s_out = s;
+  const float sc = scale_from_amax(block_max_partials(partials, n_partials, red));
+  if (blockIdx.x == 0 && threadIdx.x == 0) *s_out = sc;
+  const Quantizer s = make_quantizer(sc);
   const Idx upr = static_cast<Idx>(ldq >> 4);  // 16-byte output units per row
   const Idx units = static_cast<Idx>(rows) * upr;
   const Idx stride = static_cast<Idx>(gridDim.x) * blockDim.x;
@@ -157,7 +158,7 @@ quantize_rows_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t K, int64
       s_w[r] = s_sh;
     }
     __syncthreads();
-    const float s = s_sh;
+    const Quantizer s = make_quantizer(s_sh);
     for (int64_t c = (int64_t)threadIdx.x << 4; c < ldq; c += (int64_t)blockDim.x << 4)
       *reinterpret_cast<uint4*>(q + r * ldq + c) = quant16_row(row + c, c, K, vec != 0, s);
     __syncthreads();  // s_sh and red are reused by the next row

@@ -220,3 +220,25 @@ def test_back_to_back_layers_on_one_stream():
             torch.cuda.synchronize()
             assert torch.equal(x, chained[i]), f"M={M} layer {i}"
         linear_parity(chained[0], a0, w[0], False, what=f"chain M={M} layer 0")
+
+
+@pytest.mark.parametrize("M,K", [(1, 4096), (5, 1000), (16, 4096), (16, 14336)])
+def test_gemv_in_kernel_quantization_codes(M, K):
+    """The decode GEMV quantizes A inside the kernel. With W = I (per-tensor: s_w = 1/448, code
+    0x7E on the diagonal) each output is a single product, Y[m, n] = bf16(s_a * dec(qA[m, n])):
+    neighbouring e4m3 codes differ by >= 12.5%, far beyond the tolerance, so every code the
+    kernel chose is checked. Row 0 holds all positive e4m3 rounding midpoints and 448 with
+    unit scale, where the quotient sits exactly on a rounding boundary."""
+    from oracle import fp8_oracle as O
+    g = np.random.default_rng(40 + M + K)
+    a = (g.standard_normal((M, K)) * np.exp2(g.integers(-14, 9, (M, K)))).astype(np.float32)
+    pos = np.array([O._decode_code(c) for c in range(0x7F)])
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)
+    a[0, :] = 0.0
+    a[0, :min(K, mids.size)] = mids[:K]
+    a[0, -1] = 448.0
+    if M > 1:
+        a[1:] = np.clip(a[1:], -448, 448)
+    a = I.to_bf16(a)
+    w = torch.eye(K, dtype=torch.bfloat16)
+    check(a, w, False, None, f"identity M={M} K={K}")
