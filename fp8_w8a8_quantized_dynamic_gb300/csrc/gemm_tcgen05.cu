@@ -23,6 +23,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "device_common.cuh"
@@ -127,9 +128,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
          (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
 }
 
-// Tile order: groups of `group_n` column tiles; inside a group the column index runs
-// fastest, so the CTAs resident at one time share a few A row blocks and a W slice that
-// stays in L2 while the group sweeps all rows.
+// Tile order: groups of `group_n` column tiles; inside a group the column index runs fastest,
+// so the CTAs resident at one time share a few qA row blocks and a W slice that stays in L2
+// while the group sweeps all rows: W is read from HBM once, qA once per group.
 __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& m_idx, int& n_idx) {
   const int per_group = p.group_n * p.m_tiles;
   const int gidx = tile / per_group;
@@ -392,7 +393,12 @@ int gemm_launch(const uint8_t* qa, int64_t ldqa, const float* s_a, const uint8_t
   p.ldy = ldy;
   p.m_tiles = (M + BM - 1) / BM;
   p.n_tiles = (N + BN - 1) / BN;
-  p.group_n = p.n_tiles < 16 ? p.n_tiles : 16;
+  // raster: a group of column tiles whose W slice (~26 MB) stays hot in L2 while the group
+  // sweeps all rows; qA is then read once per group. Larger hot sets were measured to be
+  // evicted by the streaming qA and Y traffic.
+  const int64_t slice_budget = int64_t(26) << 20;
+  const int64_t w_tile_bytes = int64_t(BN) * ldqw;
+  p.group_n = int(std::max<int64_t>(1, std::min<int64_t>(p.n_tiles, slice_budget / w_tile_bytes)));
   p.y_vec = (ldy % 8 == 0) && (reinterpret_cast<uintptr_t>(y) % 16 == 0);
 
   const int tiles = p.m_tiles * p.n_tiles;
