@@ -109,9 +109,30 @@ class ClockSampler:
 # workloads
 # ---------------------------------------------------------------------------
 
-def prefill_inputs(M: int):
+def selected_layers(names):
     from fp8_w8a8_quantized_dynamic_gb300 import inputs as I
-    return [(L, I.prefill_activations(i, M=M), I.prefill_weight(i)) for i, L in enumerate(I.LLAMA8B_LAYERS)]
+    return [(i, L) for i, L in enumerate(I.LLAMA8B_LAYERS) if names is None or L.name in names]
+
+
+def prefill_inputs(M: int, names=None):
+    from fp8_w8a8_quantized_dynamic_gb300 import inputs as I
+    return [(L, I.prefill_activations(i, M=M), I.prefill_weight(i)) for i, L in selected_layers(names)]
+
+
+def gemm_traffic(layers):
+    """Mean DRAM bytes per GEMM launch from the committed ncu summary, if that summary was taken
+    on the current GEMM source (else None: the counters no longer describe this kernel)."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "gemm_tcgen05_dram_llama8b_m16384.json")) as f:
+            rec = json.load(f)
+        src = os.path.join(ROOT, "fp8_w8a8_quantized_dynamic_gb300", "csrc", "gemm_tcgen05.cu")
+        if hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["gemm_source_sha256"]:
+            return None, None
+        per = {L.name: rec["per_launch_bytes"][L.name] for L in layers}
+        return sum(per.values()) / len(per), per
+    except (OSError, KeyError, ValueError):
+        return None, None
 
 
 def flops(M, layers):
@@ -158,82 +179,90 @@ def run_ours(args, rank: int, world: int):
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
     M = args.m
-    layers = I.LLAMA8B_LAYERS
-
-    # ---- inputs: bf16 A per layer, FP8 weights quantized once on the device (load time)
-    host = prefill_inputs(M)
-    A = [a.to(dev) for _, a, _ in host]
-    Wq = []
-    for _, _, w in host:
-        qw, s_w = F.fp8_quantize_weight(w.to(dev), per_channel=True)
-        Wq.append((qw, s_w))
-    Y = [torch.empty((M, L.N), dtype=torch.bfloat16, device=dev) for L in layers]
-    ws = torch.empty(max(F.fp8_workspace_bytes(M, L.K, L.N) for L in layers), dtype=torch.uint8, device=dev)
-    torch.cuda.synchronize()
-
-    def step():
-        for i in range(len(layers)):
-            F.fp8_linear_channelwise(A[i], Wq[i][0], Wq[i][1], out=Y[i], ws=ws)
+    names = args.layers.split(",") if args.layers else None
+    layers = [L for _, L in selected_layers(names)]
 
     clocks = ClockSampler(dev.index)
     clocks.start()
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(args.steps):
-        step()
-    t1.record()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    ms = t0.elapsed_time(t1) / args.steps
-    ms_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(t.item())
-    total_flops = flops(M, layers)
-    value = world * total_flops / (ms_max * 1e-3) / 1e12
-    launches = args.steps * len(layers) * 3  # amax, cast, gemm per layer
+    host, value, ms_max, launches, roofline, quant_ms, gemm_ms = [], None, None, 0, None, [], []
+    if not args.no_prefill:
+        # ---- inputs: bf16 A per layer, FP8 weights quantized once on the device (load time)
+        host = prefill_inputs(M, names)
+        A = [a.to(dev) for _, a, _ in host]
+        Wq = []
+        for _, _, w in host:
+            qw, s_w = F.fp8_quantize_weight(w.to(dev), per_channel=True)
+            Wq.append((qw, s_w))
+        Y = [torch.empty((M, L.N), dtype=torch.bfloat16, device=dev) for L in layers]
+        ws = torch.empty(max(F.fp8_workspace_bytes(M, L.K, L.N) for L in layers), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
 
-    # ---- GEMM kernel alone (fp8_scaled_mm on the quantized activations), per layer
-    Q = [F.fp8_quantize_act(a) for a in A]
-    torch.cuda.synchronize()
-    gemm_ms = []
-    for i, L in enumerate(layers):
-        qa, s_a = Q[i]
-        f = lambda i=i, qa=qa, s_a=s_a, L=L: F.fp8_scaled_mm(qa, L.K, s_a, Wq[i][0], Wq[i][1], True, out=Y[i])
-        gemm_ms.append(time_loop(torch, f, max(3, args.steps // 2), 2))
-    quant_ms = []
-    for i, L in enumerate(layers):
-        f = lambda i=i: F.fp8_quantize_act(A[i], ws=ws)
-        quant_ms.append(time_loop(torch, f, max(3, args.steps // 2), 2))
-    del Q
-    gemm_flops = [2.0 * M * L.N * L.K for L in layers]
-    gemm_tflops = sum(gemm_flops) / (sum(gemm_ms) * 1e-3) / 1e12
-    fp8_peak = peaks["bf16_tflops"] * NOMINAL_FP8_OVER_BF16
-    roofline = {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
-                "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4), "traffic": None,
-                "kernel": "gemm_kernel (tcgen05 kind::f8f6f4)",
-                "peak_source": f"{peak_src} bf16 burst x {NOMINAL_FP8_OVER_BF16} nominal fp8/bf16 ratio",
-                "per_layer_ms": {L.name: round(t, 4) for L, t in zip(layers, gemm_ms)}}
+        def step():
+            for i in range(len(layers)):
+                F.fp8_linear_channelwise(A[i], Wq[i][0], Wq[i][1], out=Y[i], ws=ws)
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(args.steps):
+            step()
+        t1.record()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        ms = t0.elapsed_time(t1) / args.steps
+        ms_max = ms
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms_max = float(t.item())
+        total_flops = flops(M, layers)
+        value = world * total_flops / (ms_max * 1e-3) / 1e12
+        launches = args.steps * len(layers) * 3  # amax, cast, gemm per layer
+
+        # ---- GEMM kernel alone (fp8_scaled_mm on the quantized activations), per layer
+        Q = [F.fp8_quantize_act(a) for a in A]
+        torch.cuda.synchronize()
+        gemm_ms = []
+        for i, L in enumerate(layers):
+            qa, s_a = Q[i]
+            f = lambda i=i, qa=qa, s_a=s_a, L=L: F.fp8_scaled_mm(qa, L.K, s_a, Wq[i][0], Wq[i][1], True, out=Y[i])
+            gemm_ms.append(time_loop(torch, f, max(3, args.steps // 2), 2))
+        quant_ms = []
+        for i, L in enumerate(layers):
+            f = lambda i=i: F.fp8_quantize_act(A[i], ws=ws)
+            quant_ms.append(time_loop(torch, f, max(3, args.steps // 2), 2))
+        del Q
+        gemm_flops = [2.0 * M * L.N * L.K for L in layers]
+        gemm_tflops = sum(gemm_flops) / (sum(gemm_ms) * 1e-3) / 1e12
+        fp8_peak = peaks["bf16_tflops"] * NOMINAL_FP8_OVER_BF16
+        traffic, traffic_per = gemm_traffic(layers)
+        roofline = {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
+                    "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
+                    "traffic": None if traffic is None else int(traffic),
+                    "traffic_note": "mean dram__bytes_read.sum + dram__bytes_write.sum per GEMM launch "
+                                    "(ncu, profiles/gemm_tcgen05_dram_llama8b_m16384.json)",
+                    "traffic_per_launch": traffic_per,
+                    "kernel": "gemm_kernel (tcgen05 kind::f8f6f4)",
+                    "peak_source": f"{peak_src} bf16 burst x {NOMINAL_FP8_OVER_BF16} nominal fp8/bf16 ratio",
+                    "per_layer_ms": {L.name: round(t, 4) for L, t in zip(layers, gemm_ms)}}
 
     # ---- decode GEMV: Mistral-7B layers, per-tensor scales, weight copies rotated past L2
     decode = None
     if not args.no_decode:
         copies = args.decode_copies
-        dq = [[F.fp8_quantize_weight(I.decode_weight(i, c).to(dev)) for i in range(len(layers))]
-              for c in range(copies)]
+        li = [i for i, _ in selected_layers(names)]
+        dq = [[F.fp8_quantize_weight(I.decode_weight(i, c).to(dev)) for i in li] for c in range(copies)]
         wbytes_step = copies * sum(L.N * L.K for L in layers)
         yd = [torch.empty((16, L.N), dtype=torch.bfloat16, device=dev) for L in layers]
         per_m = {}
         for Md in I.DECODE_MS:
-            ad = [I.decode_activations(Md, i).to(dev) for i in range(len(layers))]
+            ad = [I.decode_activations(Md, i).to(dev) for i in li]
             ydm = [y[:Md] for y in yd]
 
             def dstep(ad=ad, Md=Md):
@@ -263,7 +292,7 @@ def run_ours(args, rank: int, world: int):
 
     # ---- e2e: host buffers through the C-ABI call, copies inside the timed region
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.no_prefill:
         A_h = [a.pin_memory() for _, a, _ in host]
         Y_h = [torch.empty((M, L.N), dtype=torch.bfloat16).pin_memory() for L in layers]
         A_d = A
@@ -280,14 +309,14 @@ def run_ours(args, rank: int, world: int):
                "d2h_bytes_per_step": int(sum(y.numel() * 2 for y in Y_h)), "ms_per_step": round(te, 3)}
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not args.no_prefill:
         cpu = oracle_sample(host, M, args.cpu_rows, args.cpu_cols)
 
     if rank != 0:
         return None
     return {
-        "metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": None if value is None else round(value, 1), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None if ms_max is None else round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 x e4m3 -> fp32 accumulate, bf16 out", "data": "synthetic",
         "config": {"workload": "prefill: Llama-3-8B linears qkv/o_proj/gate_up/down at M=16384, channelwise "
                                "weight scales, dynamic per-tensor activation scale",
@@ -375,6 +404,8 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=16)
     ap.add_argument("--cpu-cols", type=int, default=512)
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="decode leg only (profiling)")
+    ap.add_argument("--layers", default="", help="comma list of qkv,o_proj,gate_up,down (default all)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
