@@ -11,6 +11,9 @@ Typical use::
     qw, s_w = fp8_quantize_weight(w, per_channel=True)
     y = fp8_linear(a, qw, s_w, bias)                 # every forward; dynamic s_a
     y = fp8_linear_channelwise(a, qw, s_w, bias)
+    y = fp8_linear_static(a, s_a, qw, s_w)           # calibrated activation scale
+    qw, s_w = fp8_quantize_weight(w, fmt="e5m2")     # the other FP8 format
+    y = fp8_linear_ex(a, qw, s_w, fmt_a="e5m2", fmt_w="e5m2")
 """
 
 from __future__ import annotations
@@ -30,6 +33,8 @@ FP8_ERR_CUDA = 4
 FP8_ERR_TIMEOUT = 5
 FP8_ERR_UNSUPPORTED_DEVICE = 6
 FP8_QUANT_WORKSPACE_BYTES = 4352
+FP8_E4M3, FP8_E5M2 = 0, 1
+_FORMATS = {"e4m3": FP8_E4M3, "e5m2": FP8_E5M2}
 FP8_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 _lock = threading.Lock()
@@ -47,6 +52,14 @@ _SIGNATURES = {
     "fp8_linear": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _sz, _vp]),
     "fp8_linear_channelwise": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _sz, _vp]),
     "fp8_linear_noalloc": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _int, _vp, _vp, _i64, _vp]),
+    "fp8_quantize_weight_ex": (_int, [_vp, _i64, _i64, _i64, _int, _int, _vp, _i64, _vp, _vp, _sz, _vp]),
+    "fp8_quantize_act_ex": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _vp, _i64, _vp, _vp, _sz, _vp]),
+    "fp8_scaled_mm_ex": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _int, _i64, _i64, _vp, _int, _vp, _vp,
+                                _i64, _vp]),
+    "fp8_linear_static": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _i64, _vp, _int, _vp, _vp, _i64, _vp,
+                                 _sz, _vp]),
+    "fp8_linear_ex": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _vp, _int, _i64, _i64, _vp, _int, _vp, _vp, _i64,
+                             _vp, _sz, _vp]),
     "fp8_last_device_status": (_int, [_vp]),
     "fp8_status_string": (ctypes.c_char_p, [_int]),
 }
@@ -141,8 +154,15 @@ def workspace(M: int, K: int, N: int, device):
     return torch.empty(fp8_workspace_bytes(M, K, N), dtype=torch.uint8, device=device)
 
 
-def fp8_quantize_weight(w, per_channel: bool = False, ws=None) -> Tuple["torch.Tensor", "torch.Tensor"]:
-    """W bf16 [N, K] -> (qW uint8 [N, min_ld(K)], s_w fp32 [1] or [N])."""
+def _fmt(name: str) -> int:
+    if name not in _FORMATS:
+        raise ValueError(f"unknown FP8 format {name!r} (expected 'e4m3' or 'e5m2')")
+    return _FORMATS[name]
+
+
+def fp8_quantize_weight(w, per_channel: bool = False, ws=None, fmt: str = "e4m3"
+                        ) -> Tuple["torch.Tensor", "torch.Tensor"]:
+    """W bf16 [N, K] -> (qW uint8 [N, min_ld(K)], s_w fp32 [1] or [N]); fmt 'e4m3' or 'e5m2'."""
     torch = _torch()
     _check_bf16_2d(w, "w")
     N, K = w.shape
@@ -150,36 +170,53 @@ def fp8_quantize_weight(w, per_channel: bool = False, ws=None) -> Tuple["torch.T
     s_w = torch.empty((N if per_channel else 1,), dtype=torch.float32, device=w.device)
     if ws is None and not per_channel:
         ws = torch.empty(FP8_QUANT_WORKSPACE_BYTES, dtype=torch.uint8, device=w.device)
-    _check(lib().fp8_quantize_weight(w.data_ptr(), N, K, w.stride(0), int(per_channel), qw.data_ptr(),
-                                     qw.stride(0), s_w.data_ptr(), _ptr(ws), 0 if ws is None else ws.numel(),
-                                     _stream_ptr(w)), "fp8_quantize_weight")
+    args = (w.data_ptr(), N, K, w.stride(0), int(per_channel))
+    tail = (qw.data_ptr(), qw.stride(0), s_w.data_ptr(), _ptr(ws), 0 if ws is None else ws.numel(), _stream_ptr(w))
+    if fmt == "e4m3":
+        _check(lib().fp8_quantize_weight(*args, *tail), "fp8_quantize_weight")
+    else:
+        _check(lib().fp8_quantize_weight_ex(*args, _fmt(fmt), *tail), "fp8_quantize_weight_ex")
     return qw, s_w
 
 
-def fp8_quantize_act(a, ws=None):
-    """A bf16 [M, K] -> (qA uint8 [M, min_ld(K)], s_a fp32 [1]) with s_a = amax(A)/448."""
+def fp8_quantize_act(a, ws=None, fmt: str = "e4m3", s_static=None):
+    """A bf16 [M, K] -> (qA uint8 [M, min_ld(K)], s_a fp32 [1]).
+
+    Dynamic s_a = amax(A) / max(fmt), or the given static scale s_static (device fp32 [1]).
+    """
     torch = _torch()
     _check_bf16_2d(a, "a")
     M, K = a.shape
     qa = torch.empty((M, min_ld(K)), dtype=torch.uint8, device=a.device)
     s_a = torch.empty((1,), dtype=torch.float32, device=a.device)
-    if ws is None:
+    if ws is None and s_static is None:
         ws = torch.empty(FP8_QUANT_WORKSPACE_BYTES, dtype=torch.uint8, device=a.device)
-    _check(lib().fp8_quantize_act(a.data_ptr(), M, K, a.stride(0), qa.data_ptr(), qa.stride(0), s_a.data_ptr(),
-                                  ws.data_ptr(), ws.numel(), _stream_ptr(a)), "fp8_quantize_act")
+    if fmt == "e4m3" and s_static is None:
+        _check(lib().fp8_quantize_act(a.data_ptr(), M, K, a.stride(0), qa.data_ptr(), qa.stride(0), s_a.data_ptr(),
+                                      ws.data_ptr(), ws.numel(), _stream_ptr(a)), "fp8_quantize_act")
+    else:
+        _check(lib().fp8_quantize_act_ex(a.data_ptr(), M, K, a.stride(0), _fmt(fmt), _ptr(s_static), qa.data_ptr(),
+                                         qa.stride(0), s_a.data_ptr(), _ptr(ws), 0 if ws is None else ws.numel(),
+                                         _stream_ptr(a)), "fp8_quantize_act_ex")
     return qa, s_a
 
 
-def fp8_scaled_mm(qa, K: int, s_a, qw, s_w, per_channel: bool = False, bias=None, out=None):
+def fp8_scaled_mm(qa, K: int, s_a, qw, s_w, per_channel: bool = False, bias=None, out=None,
+                  fmt_a: str = "e4m3", fmt_w: str = "e4m3"):
     """Y = bf16(s_a * s_w * (qA @ qW^T) (+ bias)) on already-quantized operands."""
     torch = _torch()
     _check_fp8_2d(qa, K, "qa")
     _check_fp8_2d(qw, K, "qw")
     M, N = qa.shape[0], qw.shape[0]
     y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
-    _check(lib().fp8_scaled_mm(qa.data_ptr(), M, K, qa.stride(0), s_a.data_ptr(), qw.data_ptr(), N, qw.stride(0),
-                               s_w.data_ptr(), int(per_channel), _ptr(bias), y.data_ptr(), y.stride(0),
-                               _stream_ptr(qa)), "fp8_scaled_mm")
+    if fmt_a == "e4m3" and fmt_w == "e4m3":
+        _check(lib().fp8_scaled_mm(qa.data_ptr(), M, K, qa.stride(0), s_a.data_ptr(), qw.data_ptr(), N,
+                                   qw.stride(0), s_w.data_ptr(), int(per_channel), _ptr(bias), y.data_ptr(),
+                                   y.stride(0), _stream_ptr(qa)), "fp8_scaled_mm")
+    else:
+        _check(lib().fp8_scaled_mm_ex(qa.data_ptr(), _fmt(fmt_a), M, K, qa.stride(0), s_a.data_ptr(), qw.data_ptr(),
+                                      _fmt(fmt_w), N, qw.stride(0), s_w.data_ptr(), int(per_channel), _ptr(bias),
+                                      y.data_ptr(), y.stride(0), _stream_ptr(qa)), "fp8_scaled_mm_ex")
     return y
 
 
@@ -208,6 +245,56 @@ def fp8_linear(a, qw, s_w, bias=None, out=None, ws=None):
 def fp8_linear_channelwise(a, qw, s_w, bias=None, out=None, ws=None):
     """Dynamic W8A8 linear, per-output-channel weight scales s_w [N]."""
     return _linear("fp8_linear_channelwise", a, qw, s_w, bias, out, ws)
+
+
+def fp8_quantize_weight_ex(w, fmt: str, per_channel: bool = False, ws=None):
+    """fp8_quantize_weight with an explicit FP8 format."""
+    return fp8_quantize_weight(w, per_channel=per_channel, ws=ws, fmt=fmt)
+
+
+def fp8_quantize_act_ex(a, fmt: str, s_static=None, ws=None):
+    """fp8_quantize_act with an explicit FP8 format and an optional static scale."""
+    return fp8_quantize_act(a, ws=ws, fmt=fmt, s_static=s_static)
+
+
+def fp8_scaled_mm_ex(qa, fmt_a: str, K: int, s_a, qw, fmt_w: str, s_w, per_channel: bool = False, bias=None,
+                     out=None):
+    """fp8_scaled_mm with the FP8 formats of both operands."""
+    return fp8_scaled_mm(qa, K, s_a, qw, s_w, per_channel=per_channel, bias=bias, out=out, fmt_a=fmt_a,
+                         fmt_w=fmt_w)
+
+
+def _prologue(a, qw, out, ws):
+    torch = _torch()
+    _check_bf16_2d(a, "a")
+    M, K = a.shape
+    _check_fp8_2d(qw, K, "qw")
+    N = qw.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    if ws is None:
+        need = lib().fp8_workspace_bytes(M, K, N)
+        ws = workspace(M, K, N, a.device) if need else None
+    return M, K, N, y, ws
+
+
+def fp8_linear_static(a, s_a, qw, s_w, per_channel: bool = False, bias=None, out=None, ws=None):
+    """W8A8 linear with a static (calibrated) activation scale s_a (device fp32 [1])."""
+    M, K, N, y, ws = _prologue(a, qw, out, ws)
+    _check(lib().fp8_linear_static(a.data_ptr(), M, K, a.stride(0), s_a.data_ptr(), qw.data_ptr(), N, qw.stride(0),
+                                   s_w.data_ptr(), int(per_channel), _ptr(bias), y.data_ptr(), y.stride(0),
+                                   _ptr(ws), 0 if ws is None else ws.numel(), _stream_ptr(a)), "fp8_linear_static")
+    return y
+
+
+def fp8_linear_ex(a, qw, s_w, per_channel: bool = False, bias=None, out=None, ws=None,
+                  fmt_a: str = "e4m3", fmt_w: str = "e4m3", s_static=None):
+    """The general linear: FP8 formats of A and W, dynamic (s_static None) or static activation scale."""
+    M, K, N, y, ws = _prologue(a, qw, out, ws)
+    _check(lib().fp8_linear_ex(a.data_ptr(), M, K, a.stride(0), _fmt(fmt_a), _ptr(s_static), qw.data_ptr(),
+                               _fmt(fmt_w), N, qw.stride(0), s_w.data_ptr(), int(per_channel), _ptr(bias),
+                               y.data_ptr(), y.stride(0), _ptr(ws), 0 if ws is None else ws.numel(),
+                               _stream_ptr(a)), "fp8_linear_ex")
+    return y
 
 
 def fp8_linear_noalloc(a, qw, s_w, per_channel: bool = False, bias=None, out=None):

@@ -22,7 +22,7 @@ LIB_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "libfp8w8a8.so"
 LIB_PATH = os.path.join(LIB_DIR, LIB_NAME)
 
-SOURCES = ("api.cu", "gemm_tcgen05.cu")
+SOURCES = ("api.cu", "gemm_tcgen05.cu", "gemv.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               "-I" + INCLUDE, "-I" + CSRC]

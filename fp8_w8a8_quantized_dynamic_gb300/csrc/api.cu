@@ -15,7 +15,7 @@
 #include "fp8w8a8.h"
 #include "device_common.cuh"
 #include "gemm_tcgen05.h"
-#include "gemv.cuh"
+#include "gemv.h"
 #include "quantize.cuh"
 
 #define FP8_API extern "C" __attribute__((visibility("default")))
@@ -134,16 +134,23 @@ fp8_status launch_amax(const BF16Mat& a, float* partials, int grid, cudaStream_t
                 a.cols, a.ld, a.contiguous(), a.vec(), partials, int(pdl));
 }
 
-fp8_status launch_cast(const BF16Mat& a, const float* partials, int n_partials, float* s_out, uint8_t* q,
-                       int64_t ldq, int sms, cudaStream_t st, bool pdl) {
+bool valid_fmt(int f) { return f == kFmtE4M3 || f == kFmtE5M2; }
+
+// Cast of A to FP8 of format `fmt`: dynamic scale from `partials` (n_partials of them), or
+// the static scale *s_static when partials is null. s_out (may be null) receives the scale.
+fp8_status launch_cast(const BF16Mat& a, const float* partials, int n_partials, const float* s_static, float* s_out,
+                       uint8_t* q, int64_t ldq, int fmt, int sms, cudaStream_t st, bool pdl) {
   const int64_t units = a.rows * (ldq / 16);
   const int64_t g = std::max<int64_t>(1, std::min<int64_t>((units + kQuantThreads - 1) / kQuantThreads,
                                                            int64_t(sms) * 8));
-  if (units < (int64_t(1) << 31))
-    return launch(cast_kernel<uint32_t>, dim3(unsigned(g)), dim3(kQuantThreads), 0, st, pdl, dim3(1, 1, 1), a.p,
-                  a.rows, a.cols, a.ld, a.vec(), partials, n_partials, s_out, q, ldq, int(pdl));
-  return launch(cast_kernel<uint64_t>, dim3(unsigned(g)), dim3(kQuantThreads), 0, st, pdl, dim3(1, 1, 1), a.p,
-                a.rows, a.cols, a.ld, a.vec(), partials, n_partials, s_out, q, ldq, int(pdl));
+  const bool narrow = units < (int64_t(1) << 31);
+  auto go = [&](auto kernel) {
+    return launch(kernel, dim3(unsigned(g)), dim3(kQuantThreads), 0, st, pdl, dim3(1, 1, 1), a.p, a.rows, a.cols,
+                  a.ld, a.vec(), partials, n_partials, s_static, s_out, q, ldq, int(pdl));
+  };
+  if (fmt == kFmtE5M2)
+    return narrow ? go(cast_kernel<uint32_t, kFmtE5M2>) : go(cast_kernel<uint64_t, kFmtE5M2>);
+  return narrow ? go(cast_kernel<uint32_t, kFmtE4M3>) : go(cast_kernel<uint64_t, kFmtE4M3>);
 }
 
 fp8_status launch_fill_bias(const void* bias, void* y, int64_t M, int64_t N, int64_t ldy, int sms, cudaStream_t st) {
@@ -172,22 +179,15 @@ gemv::Params gemv_params(const uint8_t* qa, int64_t ldqa, const float* s_a, cons
 
 // Dynamic shared memory the GEMV may use: the device's opt-in per-block limit minus the
 // kernel's static shared memory (set as the kernel attribute on first use; cached).
-const void* gemv_fn(int NT, bool dyn) {
-  if (NT == 1) return dyn ? reinterpret_cast<const void*>(gemv::gemv_kernel<1, true>)
-                          : reinterpret_cast<const void*>(gemv::gemv_kernel<1, false>);
-  return dyn ? reinterpret_cast<const void*>(gemv::gemv_kernel<2, true>)
-             : reinterpret_cast<const void*>(gemv::gemv_kernel<2, false>);
-}
-
-int gemv_smem_limit(int NT, bool dyn) {
+int gemv_smem_limit(gemv::KernelFn kfn) {
   static std::mutex mu;
-  static std::map<std::tuple<int, int, bool>, int> cache;
+  static std::map<std::tuple<int, const void*>, int> cache;
   int dev = 0;
   cudaGetDevice(&dev);
+  const void* fn = reinterpret_cast<const void*>(kfn);
   std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find(std::make_tuple(dev, NT, dyn));
+  auto it = cache.find(std::make_tuple(dev, fn));
   if (it != cache.end()) return it->second;
-  const void* fn = gemv_fn(NT, dyn);
   int optin = 0;
   cudaFuncAttributes fa = {};
   int limit = 0;
@@ -198,21 +198,21 @@ int gemv_smem_limit(int NT, bool dyn) {
                     "gemv smem attribute") != cudaSuccess)
       limit = 0;
   }
-  cache[std::make_tuple(dev, NT, dyn)] = limit;
+  cache[std::make_tuple(dev, fn)] = limit;
   return limit;
 }
 
 // Largest number of co-resident clusters of `S` CTAs for the GEMV at `smem` bytes (cached).
-int gemv_max_clusters(int NT, bool dyn, int S, size_t smem) {
+int gemv_max_clusters(gemv::KernelFn kfn, int S, size_t smem) {
   static std::mutex mu;
-  static std::map<std::tuple<int, int, bool, int, size_t>, int> cache;
+  static std::map<std::tuple<int, const void*, int, size_t>, int> cache;
   int dev = 0;
   cudaGetDevice(&dev);
-  const auto key = std::make_tuple(dev, NT, dyn, S, smem);
+  const void* fn = reinterpret_cast<const void*>(kfn);
+  const auto key = std::make_tuple(dev, fn, S, smem);
   std::lock_guard<std::mutex> lock(mu);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
-  const void* fn = gemv_fn(NT, dyn);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(S * 64);
   cfg.blockDim = dim3(gemv::kThreads);
@@ -233,14 +233,16 @@ int gemv_max_clusters(int NT, bool dyn, int S, size_t smem) {
 // Persistent split-K GEMV on e4m3 activations. Picks the cluster size S (K split) and the
 // number of clusters C so that the CTA with the most work streams as few 16 KB weight tiles
 // as possible, every cluster holds at most kMaxRowBlocks row blocks, and the smem fits.
-fp8_status launch_gemv(gemv::Params p, bool dyn, const uint8_t* qw, int64_t ldqw, cudaStream_t st) {
+fp8_status launch_gemv(gemv::Params p, bool dyn, int fmt_a, int fmt_w, const uint8_t* qw, int64_t ldqw,
+                       cudaStream_t st) {
   using namespace gemv;
   const int R = (p.N + kRows - 1) / kRows;
   const int KT = (p.K + kTileK - 1) / kTileK;
   int best_cost = -1, bS = 1, bC = 1, bstages = kMaxStages, bslice = kTileK;
   size_t bsmem = 0;
   const int NT = p.M <= 8 ? 1 : 2;
-  const int smem_limit = gemv_smem_limit(NT, dyn);
+  const KernelFn kfn = kernel_for(NT, dyn, fmt_a, fmt_w);
+  const int smem_limit = gemv_smem_limit(kfn);
   for (int S : {1, 2, 4, 8}) {
     if (S > KT) break;
     const int slice_tiles = (KT + S - 1) / S;
@@ -252,7 +254,7 @@ fp8_status launch_gemv(gemv::Params p, bool dyn, const uint8_t* qw, int64_t ldqw
     auto smem_for = [&](int stg, int nrb) { return size_t(layout(stg, act_stride, nrb).total) + 1024; };
     while (stages > kMinStages && smem_for(stages, kMaxRowBlocks) > size_t(smem_limit)) --stages;
     if (smem_for(stages, kMaxRowBlocks) > size_t(smem_limit)) continue;
-    const int cmax = gemv_max_clusters(NT, dyn, S, smem_for(stages, kMaxRowBlocks));
+    const int cmax = gemv_max_clusters(kfn, S, smem_for(stages, kMaxRowBlocks));
     if (cmax <= 0) continue;
     int C = std::min(cmax, R);
     const int nrb = (R + C - 1) / C;
@@ -283,12 +285,7 @@ fp8_status launch_gemv(gemv::Params p, bool dyn, const uint8_t* qw, int64_t ldqw
   p.num_clusters = bC;
   CUtensorMap map;
   if (!make_fp8_tensor_map(&map, qw, p.N, p.K, ldqw, kRows)) return FP8_ERR_CUDA;
-  const dim3 grid(bC * bS), block(kThreads), cl(bS, 1, 1);
-  if (NT == 1)
-    return dyn ? launch(gemv_kernel<1, true>, grid, block, bsmem, st, true, cl, map, p)
-               : launch(gemv_kernel<1, false>, grid, block, bsmem, st, true, cl, map, p);
-  return dyn ? launch(gemv_kernel<2, true>, grid, block, bsmem, st, true, cl, map, p)
-             : launch(gemv_kernel<2, false>, grid, block, bsmem, st, true, cl, map, p);
+  return launch(kfn, dim3(bC * bS), dim3(kThreads), bsmem, st, true, dim3(bS, 1, 1), map, p);
 }
 
 // ---------------------------------------------------------------------------
@@ -332,14 +329,15 @@ size_t linear_ws_bytes(int64_t M, int64_t K) {
   return FP8_QUANT_WORKSPACE_BYTES + size_t(M) * size_t(round_up16(K));
 }
 
-fp8_status linear_impl(const void* a, int64_t M, int64_t K, int64_t lda, const uint8_t* qw, int64_t N,
-                       int64_t ldqw, const float* s_w, int per_channel, const void* bias, void* y, int64_t ldy,
-                       void* ws, size_t ws_bytes, fp8_stream_t stream) {
+fp8_status linear_impl(const void* a, int64_t M, int64_t K, int64_t lda, int fmt_a, const float* s_static,
+                       const uint8_t* qw, int fmt_w, int64_t N, int64_t ldqw, const float* s_w, int per_channel,
+                       const void* bias, void* y, int64_t ldy, void* ws, size_t ws_bytes, fp8_stream_t stream) {
+  if (!valid_fmt(fmt_a) || !valid_fmt(fmt_w) || (per_channel != 0 && per_channel != 1)) return FP8_ERR_INVALID_ARG;
   FP8_TRY(check_bf16_mat(a, M, K, lda));
   FP8_TRY(check_fp8_mat(qw, N, K, ldqw));
   FP8_TRY(check_bf16_mat(y, M, N, ldy));
   if (N > 0 && s_w == nullptr) return FP8_ERR_INVALID_ARG;
-  if (!aligned(bias, 2)) return FP8_ERR_MISALIGNED;
+  if (!aligned(bias, 2) || !aligned(s_static, 4)) return FP8_ERR_MISALIGNED;
   if (M == 0 || N == 0) return FP8_OK;
   FP8_TRY(check_ws(ws, ws_bytes, linear_ws_bytes(M, K)));
   int sms = 0;
@@ -347,25 +345,103 @@ fp8_status linear_impl(const void* a, int64_t M, int64_t K, int64_t lda, const u
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (K == 0) return launch_fill_bias(bias, y, M, N, ldy, sms, st);
 
-  uint8_t* wsb = static_cast<uint8_t*>(ws);
-  float* partials = reinterpret_cast<float*>(wsb);
-  float* s_a = reinterpret_cast<float*>(wsb + kWsScaleOffset);
   const BF16Mat A{static_cast<const uint16_t*>(a), M, K, lda};
   if (use_gemv(M, K)) {
-    // decode: one persistent GEMV kernel quantizes A (cluster-wide amax) and streams qW
+    // decode: one persistent GEMV kernel quantizes A (cluster-wide amax, or the static
+    // scale) and streams qW
     gemv::Params p = gemv_params(nullptr, 0, nullptr, s_w, per_channel, bias, y, ldy, M, N, K);
     p.a = A.p;
     p.lda = lda;
     p.vec_a = A.vec();
-    return launch_gemv(p, true, qw, ldqw, st);
+    p.s_static = s_static;
+    return launch_gemv(p, true, fmt_a, fmt_w, qw, ldqw, st);
   }
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* partials = reinterpret_cast<float*>(wsb);
   uint8_t* qa = wsb + kWsQaOffset;
   const int64_t ldqa = round_up16(K);
+  const float* s_a = s_static;
+  if (s_static == nullptr) {
+    float* s_dyn = reinterpret_cast<float*>(wsb + kWsScaleOffset);
+    const int g = amax_grid(A, sms);
+    FP8_TRY(launch_amax(A, partials, g, st, true));
+    FP8_TRY(launch_cast(A, partials, g, nullptr, s_dyn, qa, ldqa, fmt_a, sms, st, true));
+    s_a = s_dyn;
+  } else {
+    FP8_TRY(launch_cast(A, nullptr, 0, s_static, nullptr, qa, ldqa, fmt_a, sms, st, true));
+  }
+  if (gemm_launch(qa, ldqa, s_a, qw, ldqw, s_w, per_channel, static_cast<const uint16_t*>(bias),
+                  static_cast<uint16_t*>(y), ldy, int(M), int(N), int(K), fmt_a, fmt_w, sms, st) != 0)
+    return FP8_ERR_CUDA;
+  return FP8_OK;
+}
+
+fp8_status quantize_weight_impl(const void* w_bf16, int64_t N, int64_t K, int64_t ldw, int per_channel, int fmt,
+                                uint8_t* qw, int64_t ldq, float* s_w, void* ws, size_t ws_bytes,
+                                fp8_stream_t stream) {
+  FP8_TRY(check_bf16_mat(w_bf16, N, K, ldw));
+  FP8_TRY(check_fp8_mat(qw, N, K, ldq));
+  if ((per_channel != 0 && per_channel != 1) || !valid_fmt(fmt)) return FP8_ERR_INVALID_ARG;
+  if (s_w == nullptr) return FP8_ERR_INVALID_ARG;
+  if (!per_channel) FP8_TRY(check_ws(ws, ws_bytes, FP8_QUANT_WORKSPACE_BYTES));
+  if (per_channel && N == 0) return FP8_OK;
+  int sms = 0;
+  FP8_TRY(current_device(&sms));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const BF16Mat W{static_cast<const uint16_t*>(w_bf16), N, K, ldw};
+  // Weight kernels never trigger programmatic launch early: a following linear call may
+  // read qW before its own wait (see the header's launch-ordering note).
+  if (per_channel) {
+    const int g = int(std::min<int64_t>(N, int64_t(sms) * 8));
+    auto go = [&](auto kernel) {
+      return launch(kernel, dim3(g), dim3(kQuantThreads), 0, st, false, dim3(1, 1, 1), W.p, N, K, ldw, W.vec(), qw,
+                    ldq, s_w);
+    };
+    return fmt == kFmtE5M2 ? go(quantize_rows_kernel<kFmtE5M2>) : go(quantize_rows_kernel<kFmtE4M3>);
+  }
+  float* partials = static_cast<float*>(ws);
+  const int g = amax_grid(W, sms);
+  FP8_TRY(launch_amax(W, partials, g, st, false));
+  return launch_cast(W, partials, g, nullptr, s_w, qw, ldq, fmt, sms, st, false);
+}
+
+fp8_status quantize_act_impl(const void* a_bf16, int64_t M, int64_t K, int64_t lda, int fmt, const float* s_static,
+                             uint8_t* qa, int64_t ldq, float* s_a, void* ws, size_t ws_bytes, fp8_stream_t stream) {
+  FP8_TRY(check_bf16_mat(a_bf16, M, K, lda));
+  FP8_TRY(check_fp8_mat(qa, M, K, ldq));
+  if (s_a == nullptr || !valid_fmt(fmt)) return FP8_ERR_INVALID_ARG;
+  if (!aligned(s_static, 4)) return FP8_ERR_MISALIGNED;
+  if (s_static == nullptr) FP8_TRY(check_ws(ws, ws_bytes, FP8_QUANT_WORKSPACE_BYTES));
+  int sms = 0;
+  FP8_TRY(current_device(&sms));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const BF16Mat A{static_cast<const uint16_t*>(a_bf16), M, K, lda};
+  if (s_static != nullptr) return launch_cast(A, nullptr, 0, s_static, s_a, qa, ldq, fmt, sms, st, true);
+  float* partials = static_cast<float*>(ws);
   const int g = amax_grid(A, sms);
   FP8_TRY(launch_amax(A, partials, g, st, true));
-  FP8_TRY(launch_cast(A, partials, g, s_a, qa, ldqa, sms, st, true));
-  if (gemm_launch(qa, ldqa, s_a, qw, ldqw, s_w, per_channel, static_cast<const uint16_t*>(bias),
-                  static_cast<uint16_t*>(y), ldy, int(M), int(N), int(K), sms, st) != 0)
+  return launch_cast(A, partials, g, nullptr, s_a, qa, ldq, fmt, sms, st, true);
+}
+
+fp8_status scaled_mm_impl(const uint8_t* qa, int fmt_a, int64_t M, int64_t K, int64_t ldqa, const float* s_a,
+                          const uint8_t* qw, int fmt_w, int64_t N, int64_t ldqw, const float* s_w, int per_channel,
+                          const void* bias_bf16, void* y_bf16, int64_t ldy, fp8_stream_t stream) {
+  FP8_TRY(check_fp8_mat(qa, M, K, ldqa));
+  FP8_TRY(check_fp8_mat(qw, N, K, ldqw));
+  FP8_TRY(check_bf16_mat(y_bf16, M, N, ldy));
+  if ((per_channel != 0 && per_channel != 1) || !valid_fmt(fmt_a) || !valid_fmt(fmt_w)) return FP8_ERR_INVALID_ARG;
+  if (M > 0 && N > 0 && (s_a == nullptr || s_w == nullptr)) return FP8_ERR_INVALID_ARG;
+  if (!aligned(bias_bf16, 2)) return FP8_ERR_MISALIGNED;
+  if (M == 0 || N == 0) return FP8_OK;
+  int sms = 0;
+  FP8_TRY(current_device(&sms));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return launch_fill_bias(bias_bf16, y_bf16, M, N, ldy, sms, st);
+  if (use_gemv(M, K))
+    return launch_gemv(gemv_params(qa, ldqa, s_a, s_w, per_channel, bias_bf16, y_bf16, ldy, M, N, K), false, fmt_a,
+                       fmt_w, qw, ldqw, st);
+  if (fp8k::gemm_launch(qa, ldqa, s_a, qw, ldqw, s_w, per_channel, static_cast<const uint16_t*>(bias_bf16),
+                        static_cast<uint16_t*>(y_bf16), ldy, int(M), int(N), int(K), fmt_a, fmt_w, sms, st) != 0)
     return FP8_ERR_CUDA;
   return FP8_OK;
 }
@@ -391,88 +467,76 @@ FP8_API int fp8_uses_gemv(int64_t M, int64_t K, int64_t N) {
 FP8_API fp8_status fp8_quantize_weight(const void* w_bf16, int64_t N, int64_t K, int64_t ldw, int per_channel,
                                        uint8_t* qw, int64_t ldq, float* s_w, void* ws, size_t ws_bytes,
                                        fp8_stream_t stream) {
-  FP8_TRY(check_bf16_mat(w_bf16, N, K, ldw));
-  FP8_TRY(check_fp8_mat(qw, N, K, ldq));
-  if (per_channel != 0 && per_channel != 1) return FP8_ERR_INVALID_ARG;
-  if (s_w == nullptr) return FP8_ERR_INVALID_ARG;
-  if (!per_channel) FP8_TRY(check_ws(ws, ws_bytes, FP8_QUANT_WORKSPACE_BYTES));
-  if (per_channel && N == 0) return FP8_OK;
-  int sms = 0;
-  FP8_TRY(current_device(&sms));
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const BF16Mat W{static_cast<const uint16_t*>(w_bf16), N, K, ldw};
-  // Weight kernels never trigger programmatic launch early: a following linear call may
-  // read qW before its own wait (see the header's launch-ordering note).
-  if (per_channel) {
-    const int g = int(std::min<int64_t>(N, int64_t(sms) * 8));
-    return launch(quantize_rows_kernel, dim3(g), dim3(kQuantThreads), 0, st, false, dim3(1, 1, 1), W.p, N, K, ldw,
-                  W.vec(), qw, ldq, s_w);
-  }
-  float* partials = static_cast<float*>(ws);
-  const int g = amax_grid(W, sms);
-  FP8_TRY(launch_amax(W, partials, g, st, false));
-  return launch_cast(W, partials, g, s_w, qw, ldq, sms, st, false);
+  return quantize_weight_impl(w_bf16, N, K, ldw, per_channel, kFmtE4M3, qw, ldq, s_w, ws, ws_bytes, stream);
+}
+
+FP8_API fp8_status fp8_quantize_weight_ex(const void* w_bf16, int64_t N, int64_t K, int64_t ldw, int per_channel,
+                                          fp8_format fmt, uint8_t* qw, int64_t ldq, float* s_w, void* ws,
+                                          size_t ws_bytes, fp8_stream_t stream) {
+  return quantize_weight_impl(w_bf16, N, K, ldw, per_channel, int(fmt), qw, ldq, s_w, ws, ws_bytes, stream);
 }
 
 FP8_API fp8_status fp8_quantize_act(const void* a_bf16, int64_t M, int64_t K, int64_t lda, uint8_t* qa, int64_t ldq,
                                     float* s_a, void* ws, size_t ws_bytes, fp8_stream_t stream) {
-  FP8_TRY(check_bf16_mat(a_bf16, M, K, lda));
-  FP8_TRY(check_fp8_mat(qa, M, K, ldq));
-  if (s_a == nullptr) return FP8_ERR_INVALID_ARG;
-  FP8_TRY(check_ws(ws, ws_bytes, FP8_QUANT_WORKSPACE_BYTES));
-  int sms = 0;
-  FP8_TRY(current_device(&sms));
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const BF16Mat A{static_cast<const uint16_t*>(a_bf16), M, K, lda};
-  float* partials = static_cast<float*>(ws);
-  const int g = amax_grid(A, sms);
-  FP8_TRY(launch_amax(A, partials, g, st, true));
-  return launch_cast(A, partials, g, s_a, qa, ldq, sms, st, true);
+  return quantize_act_impl(a_bf16, M, K, lda, kFmtE4M3, nullptr, qa, ldq, s_a, ws, ws_bytes, stream);
+}
+
+FP8_API fp8_status fp8_quantize_act_ex(const void* a_bf16, int64_t M, int64_t K, int64_t lda, fp8_format fmt,
+                                       const float* s_static, uint8_t* qa, int64_t ldq, float* s_a, void* ws,
+                                       size_t ws_bytes, fp8_stream_t stream) {
+  return quantize_act_impl(a_bf16, M, K, lda, int(fmt), s_static, qa, ldq, s_a, ws, ws_bytes, stream);
 }
 
 FP8_API fp8_status fp8_scaled_mm(const uint8_t* qa, int64_t M, int64_t K, int64_t ldqa, const float* s_a,
                                  const uint8_t* qw, int64_t N, int64_t ldqw, const float* s_w, int per_channel,
                                  const void* bias_bf16, void* y_bf16, int64_t ldy, fp8_stream_t stream) {
-  FP8_TRY(check_fp8_mat(qa, M, K, ldqa));
-  FP8_TRY(check_fp8_mat(qw, N, K, ldqw));
-  FP8_TRY(check_bf16_mat(y_bf16, M, N, ldy));
-  if (per_channel != 0 && per_channel != 1) return FP8_ERR_INVALID_ARG;
-  if (M > 0 && N > 0 && (s_a == nullptr || s_w == nullptr)) return FP8_ERR_INVALID_ARG;
-  if (!aligned(bias_bf16, 2)) return FP8_ERR_MISALIGNED;
-  if (M == 0 || N == 0) return FP8_OK;
-  int sms = 0;
-  FP8_TRY(current_device(&sms));
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (K == 0) return launch_fill_bias(bias_bf16, y_bf16, M, N, ldy, sms, st);
-  if (use_gemv(M, K))
-    return launch_gemv(gemv_params(qa, ldqa, s_a, s_w, per_channel, bias_bf16, y_bf16, ldy, M, N, K), false, qw,
-                       ldqw, st);
-  if (fp8k::gemm_launch(qa, ldqa, s_a, qw, ldqw, s_w, per_channel, static_cast<const uint16_t*>(bias_bf16),
-                        static_cast<uint16_t*>(y_bf16), ldy, int(M), int(N), int(K), sms, st) != 0)
-    return FP8_ERR_CUDA;
-  return FP8_OK;
+  return scaled_mm_impl(qa, kFmtE4M3, M, K, ldqa, s_a, qw, kFmtE4M3, N, ldqw, s_w, per_channel, bias_bf16, y_bf16,
+                        ldy, stream);
+}
+
+FP8_API fp8_status fp8_scaled_mm_ex(const uint8_t* qa, fp8_format fmt_a, int64_t M, int64_t K, int64_t ldqa,
+                                    const float* s_a, const uint8_t* qw, fp8_format fmt_w, int64_t N, int64_t ldqw,
+                                    const float* s_w, int per_channel, const void* bias_bf16, void* y_bf16,
+                                    int64_t ldy, fp8_stream_t stream) {
+  return scaled_mm_impl(qa, int(fmt_a), M, K, ldqa, s_a, qw, int(fmt_w), N, ldqw, s_w, per_channel, bias_bf16,
+                        y_bf16, ldy, stream);
 }
 
 FP8_API fp8_status fp8_linear(const void* a_bf16, int64_t M, int64_t K, int64_t lda, const uint8_t* qw, int64_t N,
                               int64_t ldqw, const float* s_w, const void* bias_bf16, void* y_bf16, int64_t ldy,
                               void* ws, size_t ws_bytes, fp8_stream_t stream) {
-  return linear_impl(a_bf16, M, K, lda, qw, N, ldqw, s_w, 0, bias_bf16, y_bf16, ldy, ws, ws_bytes, stream);
+  return linear_impl(a_bf16, M, K, lda, kFmtE4M3, nullptr, qw, kFmtE4M3, N, ldqw, s_w, 0, bias_bf16, y_bf16, ldy,
+                     ws, ws_bytes, stream);
 }
 
 FP8_API fp8_status fp8_linear_channelwise(const void* a_bf16, int64_t M, int64_t K, int64_t lda, const uint8_t* qw,
                                           int64_t N, int64_t ldqw, const float* s_w, const void* bias_bf16,
                                           void* y_bf16, int64_t ldy, void* ws, size_t ws_bytes,
                                           fp8_stream_t stream) {
-  return linear_impl(a_bf16, M, K, lda, qw, N, ldqw, s_w, 1, bias_bf16, y_bf16, ldy, ws, ws_bytes, stream);
+  return linear_impl(a_bf16, M, K, lda, kFmtE4M3, nullptr, qw, kFmtE4M3, N, ldqw, s_w, 1, bias_bf16, y_bf16, ldy,
+                     ws, ws_bytes, stream);
+}
+
+FP8_API fp8_status fp8_linear_static(const void* a_bf16, int64_t M, int64_t K, int64_t lda, const float* s_a,
+                                     const uint8_t* qw, int64_t N, int64_t ldqw, const float* s_w, int per_channel,
+                                     const void* bias_bf16, void* y_bf16, int64_t ldy, void* ws, size_t ws_bytes,
+                                     fp8_stream_t stream) {
+  if (M > 0 && N > 0 && s_a == nullptr) return FP8_ERR_INVALID_ARG;
+  return linear_impl(a_bf16, M, K, lda, kFmtE4M3, s_a, qw, kFmtE4M3, N, ldqw, s_w, per_channel, bias_bf16, y_bf16,
+                     ldy, ws, ws_bytes, stream);
+}
+
+FP8_API fp8_status fp8_linear_ex(const void* a_bf16, int64_t M, int64_t K, int64_t lda, fp8_format fmt_a,
+                                 const float* s_static, const uint8_t* qw, fp8_format fmt_w, int64_t N, int64_t ldqw,
+                                 const float* s_w, int per_channel, const void* bias_bf16, void* y_bf16, int64_t ldy,
+                                 void* ws, size_t ws_bytes, fp8_stream_t stream) {
+  return linear_impl(a_bf16, M, K, lda, int(fmt_a), s_static, qw, int(fmt_w), N, ldqw, s_w, per_channel, bias_bf16,
+                     y_bf16, ldy, ws, ws_bytes, stream);
 }
 
 FP8_API fp8_status fp8_last_device_status(fp8_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8_ERR_CUDA;
-  unsigned int e = fp8k::gemm_read_and_clear_error();
-  unsigned int ge = 0, zero = 0;
-  if (cudaMemcpyFromSymbol(&ge, gemv::g_gemv_error, sizeof(ge)) == cudaSuccess)
-    cudaMemcpyToSymbol(gemv::g_gemv_error, &zero, sizeof(zero));
-  e |= ge;
+  const unsigned int e = fp8k::gemm_read_and_clear_error() | gemv::read_and_clear_error();
   if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
   return (e & kErrTimeout) ? FP8_ERR_TIMEOUT : FP8_OK;
 }
@@ -530,11 +594,12 @@ FP8_API fp8_status fp8_linear_noalloc(const void* a_bf16, int64_t M, int64_t K, 
   FP8_TRY(check_fp8_mat(qw, N, K, ldqw));
   FP8_TRY(check_bf16_mat(y_bf16, M, N, ldy));
   if (M == 0 || N == 0)
-    return linear_impl(a_bf16, M, K, lda, qw, N, ldqw, s_w, per_channel, bias_bf16, y_bf16, ldy, nullptr, 0, stream);
+    return linear_impl(a_bf16, M, K, lda, kFmtE4M3, nullptr, qw, kFmtE4M3, N, ldqw, s_w, per_channel, bias_bf16,
+                       y_bf16, ldy, nullptr, 0, stream);
   // shapes whose scratch would not fit are refused before anything is enqueued
   if (linear_ws_bytes(M, K) > size_t(FP8_NOALLOC_SCRATCH_BYTES)) return FP8_ERR_WORKSPACE;
   void* scratch = nullptr;
   FP8_TRY(noalloc_scratch(&scratch));
-  return linear_impl(a_bf16, M, K, lda, qw, N, ldqw, s_w, per_channel, bias_bf16, y_bf16, ldy, scratch,
-                     size_t(FP8_NOALLOC_SCRATCH_BYTES), stream);
+  return linear_impl(a_bf16, M, K, lda, kFmtE4M3, nullptr, qw, kFmtE4M3, N, ldqw, s_w, per_channel, bias_bf16,
+                     y_bf16, ldy, scratch, size_t(FP8_NOALLOC_SCRATCH_BYTES), stream);
 }

@@ -16,24 +16,36 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded device wa
 constexpr unsigned int kErrTimeout = 1u;
 
 // ---------------------------------------------------------------------------
-// Quantization arithmetic: q = e4m3(fp32(x / s)), saturating RNE.
+// Quantization arithmetic: q = fp8(fp32(x / s)), saturating RNE.
 // ---------------------------------------------------------------------------
 
-// Two fp32 -> packed e4m3fn pair (round to nearest even, saturate to +-448; NaN stays NaN).
-// `lo` lands in bits 0..7, `hi` in bits 8..15.
-__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+// FP8 formats (values of fp8_format): 0 = e4m3fn (largest finite 448), 1 = e5m2 (57344).
+constexpr int kFmtE4M3 = 0;
+constexpr int kFmtE5M2 = 1;
+constexpr float kE5M2Max = 57344.0f;
+
+template <int F>
+__device__ __forceinline__ constexpr float fp8_max() { return F == kFmtE5M2 ? kE5M2Max : kE4M3Max; }
+
+// Two fp32 -> packed FP8 pair of format F (round to nearest even, saturate to the largest
+// finite value; NaN stays NaN). `lo` lands in bits 0..7, `hi` in bits 8..15.
+template <int F>
+__device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
   uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  if constexpr (F == kFmtE5M2)
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
 
-// Quantizer for one scale s: e4m3 codes of fl32(x / s), most of the time without a division.
+// Quantizer for one scale s: FP8 codes of fl32(x / s), most of the time without a division.
 // y = x * fl32(1/s) carries two roundings, so |y - fl32(x/s)| < 3 ulp(y) (relative error at
-// most 3 * 2^-24 against an ulp of at least 2^-24 |y|). Rounding to e4m3 is monotone and
+// most 3 * 2^-24 against an ulp of at least 2^-24 |y|). Rounding to FP8 is monotone and
 // symmetric in sign, so when the magnitudes |y| - 4 ulp and |y| + 4 ulp (4 steps of the fp32
-// bit pattern, at least 2 ulp(y) in either direction) round to the same e4m3 magnitude, that
+// bit pattern, at least 2 ulp(y) in either direction) round to the same FP8 magnitude, that
 // is the magnitude of the exact quotient's code and the sign comes from y. Otherwise the
-// quotient lies within a few ulps of an e4m3 rounding boundary and the IEEE division decides
+// quotient lies within a few ulps of an FP8 rounding boundary and the IEEE division decides
 // (out of line, so the common path stays short). Scales below 2^-125, where 1/s could
 // overflow, always divide.
 struct Quantizer {
@@ -49,41 +61,47 @@ __device__ __forceinline__ Quantizer make_quantizer(float s) {
   return q;
 }
 
+template <int F>
 static __device__ __noinline__ uint32_t quant2_divide(float x0, float x1, float s) {
-  return cvt_e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+  return cvt_fp8x2<F>(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
 }
 
-// Two values -> two e4m3fn bytes (x0 in bits 0..7, x1 in bits 8..15).
+// Two values -> two FP8 bytes of format F (x0 in bits 0..7, x1 in bits 8..15).
+template <int F>
 __device__ __forceinline__ uint32_t quant2(float x0, float x1, const Quantizer& q) {
   if (q.fast) {
     const uint32_t b0 = __float_as_uint(x0 * q.r), b1 = __float_as_uint(x1 * q.r);
     const uint32_t a0 = b0 & 0x7FFFFFFFu, a1 = b1 & 0x7FFFFFFFu;
-    const uint32_t lo = cvt_e4m3x2(__uint_as_float(a0 > 4u ? a0 - 4u : 0u), __uint_as_float(a1 > 4u ? a1 - 4u : 0u));
-    const uint32_t hi = cvt_e4m3x2(__uint_as_float(a0 + 4u), __uint_as_float(a1 + 4u));
+    const uint32_t lo = cvt_fp8x2<F>(__uint_as_float(a0 > 4u ? a0 - 4u : 0u), __uint_as_float(a1 > 4u ? a1 - 4u : 0u));
+    const uint32_t hi = cvt_fp8x2<F>(__uint_as_float(a0 + 4u), __uint_as_float(a1 + 4u));
     if (lo == hi) return lo | ((b0 >> 31) << 7) | ((b1 >> 31) << 15);
   }
-  return quant2_divide(x0, x1, q.s);
+  return quant2_divide<F>(x0, x1, q.s);
 }
 
-// Four values -> four e4m3fn bytes (x0 in the lowest byte).
+// Four values -> four FP8 bytes (x0 in the lowest byte).
+template <int F>
 __device__ __forceinline__ uint32_t quant4(float x0, float x1, float x2, float x3, const Quantizer& q) {
-  return quant2(x0, x1, q) | (quant2(x2, x3, q) << 16);
+  return quant2<F>(x0, x1, q) | (quant2<F>(x2, x3, q) << 16);
 }
 
-// Eight bf16 (packed in a uint4) -> eight e4m3fn bytes (uint2).
+// Eight bf16 (packed in a uint4) -> eight FP8 bytes (uint2).
+template <int F>
 __device__ __forceinline__ uint2 quant8_bf16(uint4 v, const Quantizer& q) {
   auto f = [](uint32_t w, int hi) { return __uint_as_float(hi ? (w & 0xFFFF0000u) : (w << 16)); };
   uint2 r;
-  r.x = quant4(f(v.x, 0), f(v.x, 1), f(v.y, 0), f(v.y, 1), q);
-  r.y = quant4(f(v.z, 0), f(v.z, 1), f(v.w, 0), f(v.w, 1), q);
+  r.x = quant4<F>(f(v.x, 0), f(v.x, 1), f(v.y, 0), f(v.y, 1), q);
+  r.y = quant4<F>(f(v.z, 0), f(v.z, 1), f(v.w, 0), f(v.w, 1), q);
   return r;
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
 
-// scale = amax / 448 (IEEE fp32 division); 1 when amax is 0 (or the quotient underflows).
+// scale = amax / 448 (57344 for e5m2) by IEEE fp32 division; 1 when amax is 0 (or the
+// quotient underflows).
+template <int F>
 __device__ __forceinline__ float scale_from_amax(float amax) {
-  const float s = __fdiv_rn(amax, kE4M3Max);
+  const float s = __fdiv_rn(amax, fp8_max<F>());
   return s == 0.0f ? 1.0f : s;
 }
 

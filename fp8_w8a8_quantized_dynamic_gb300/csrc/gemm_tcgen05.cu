@@ -5,7 +5,9 @@
 // The W8A8 product the pages run through torch._scaled_mm / CUTLASS ("Prototype FP8Linear
 // W8A8 runtime quantization"; "[Kernel] Implement fallback for FP8 channelwise using
 // torch._scaled_mm"), with the channelwise rescale s_a*s_w[n] applied to the fp32
-// accumulator in the epilogue: (s_a A)(s_w,n W_n)^T = s_a s_w,n (A W_n^T).
+// accumulator in the epilogue: (s_a A)(s_w,n W_n)^T = s_a s_w,n (A W_n^T). qA and qW are
+// each e4m3 or e5m2 ("Fp8 Quantization Support"): the operand formats are fields of the
+// MMA instruction descriptor, so one kernel serves every pairing.
 //
 // Structure (one CTA per SM, persistent over output tiles of 128 x 256):
 //   warp 0      TMA producer: qA tile [128 x 128B] and qW tile [256 x 128B] per stage into a
@@ -36,7 +38,7 @@ __device__ unsigned int g_gemm_error;
 
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int BK = 128;  // bytes (= e4m3 elements) of K per stage: one 128-byte swizzle row
+constexpr int BK = 128;  // bytes (= FP8 elements) of K per stage: one 128-byte swizzle row
 constexpr int kStages = 4;
 constexpr int kAccBufs = 2;
 constexpr int kTmemCols = kAccBufs * BN;  // 512: the whole tensor memory of the SM
@@ -61,9 +63,14 @@ struct SharedCtl {
 
 constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + sizeof(SharedCtl);
 
-// Instruction descriptor, kind::f8f6f4: D fp32 (bits 4-5 = 1), A and B e4m3 (bits 7-9, 10-12 = 0),
-// both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+// Instruction descriptor, kind::f8f6f4: D fp32 (bits 4-5 = 1), A and B format at bits 7-9 and
+// 10-12 (e4m3 = 0, e5m2 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at
+// bits 24-28.
+constexpr uint32_t kIdescBase = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+
+constexpr uint32_t make_idesc(int fmt_a, int fmt_w) {
+  return kIdescBase | (uint32_t(fmt_a) << 7) | (uint32_t(fmt_w) << 10);
+}
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA with 128-byte
 // swizzle: rows of 128 bytes, 8-row swizzle atoms of 1024 bytes (stride byte offset), start
@@ -85,11 +92,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y) : "memory");
 }
 
-__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
-      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate));
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -232,7 +240,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 #pragma unroll
           for (int kk = 0; kk < BK / kMmaK; ++kk) {
             // advance the start address by 32 bytes of K inside the swizzled 128-byte row
-            mma_f8(d_tmem, adesc + uint64_t(kk * kMmaK >> 4), bdesc + uint64_t(kk * kMmaK >> 4),
+            mma_f8(d_tmem, adesc + uint64_t(kk * kMmaK >> 4), bdesc + uint64_t(kk * kMmaK >> 4), p.idesc,
                    (kb | kk) != 0 ? 1u : 0u);
           }
           mma_commit(smem_u32(&ctl->empty[s]));  // frees the stage once these MMAs have read it
@@ -355,7 +363,7 @@ EncodeTiledFn get_encode_fn() {
 
 namespace fp8k {
 
-// 2-D e4m3 tensor map: [rows, K] with row stride ld bytes, box [box_rows, 128 bytes], 128B swizzle.
+// 2-D FP8 (byte) tensor map: [rows, K] with row stride ld bytes, box [box_rows, 128 bytes], 128B swizzle.
 bool make_fp8_tensor_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t K, int64_t ld, uint32_t box_rows) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
@@ -370,7 +378,7 @@ bool make_fp8_tensor_map(CUtensorMap* map, const uint8_t* base, int64_t rows, in
 
 int gemm_launch(const uint8_t* qa, int64_t ldqa, const float* s_a, const uint8_t* qw, int64_t ldqw,
                 const float* s_w, int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy,
-                int M, int N, int K, int num_sms, cudaStream_t stream) {
+                int M, int N, int K, int fmt_a, int fmt_w, int num_sms, cudaStream_t stream) {
   using namespace gemm;
   static bool attr_done = false;  // the attribute is per function, set once per process
   if (!attr_done) {
@@ -400,6 +408,7 @@ int gemm_launch(const uint8_t* qa, int64_t ldqa, const float* s_a, const uint8_t
   const int64_t w_tile_bytes = int64_t(BN) * ldqw;
   p.group_n = int(std::max<int64_t>(1, std::min<int64_t>(p.n_tiles, slice_budget / w_tile_bytes)));
   p.y_vec = (ldy % 8 == 0) && (reinterpret_cast<uintptr_t>(y) % 16 == 0);
+  p.idesc = make_idesc(fmt_a, fmt_w);
 
   const int tiles = p.m_tiles * p.n_tiles;
   cudaLaunchConfig_t cfg = {};

@@ -18,15 +18,17 @@ struct GemmParams {
   int64_t ldy;
   int m_tiles, n_tiles, group_n;
   int y_vec;
+  uint32_t idesc;  // tcgen05 instruction descriptor (carries the two operand formats)
 };
 
 // Enqueues the persistent GEMM. Returns 0 on success, non-zero when the tensor maps could
 // not be encoded or the launch failed. qa/qw: 16-byte aligned, ld multiples of 16.
+// fmt_a / fmt_w: 0 = e4m3, 1 = e5m2.
 int gemm_launch(const uint8_t* qa, int64_t ldqa, const float* s_a, const uint8_t* qw, int64_t ldqw,
                 const float* s_w, int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy,
-                int M, int N, int K, int num_sms, cudaStream_t stream);
+                int M, int N, int K, int fmt_a, int fmt_w, int num_sms, cudaStream_t stream);
 
-// 2-D e4m3 tensor map over [rows, K] (row stride ld bytes), box [box_rows rows x 128 bytes],
+// 2-D FP8 (byte) tensor map over [rows, K] (row stride ld bytes), box [box_rows rows x 128 bytes],
 // 128-byte swizzle, zero fill outside the matrix. False when the encoder is unavailable or fails.
 bool make_fp8_tensor_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t K, int64_t ld,
                          uint32_t box_rows);

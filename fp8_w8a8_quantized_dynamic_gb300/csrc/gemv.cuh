@@ -1,4 +1,6 @@
 // Decode-shape FP8 GEMV: Y[M<=16, N] = bf16(s_a * s_w[n] * sum_k qA[m,k] qW[n,k] (+ bias[n])).
+// qA and qW are e4m3 or e5m2 ("Fp8 Quantization Support", the other FP8 dtype), each
+// operand's format a template parameter of the kernel.
 //
 // "[WIP] FP8 support": LLM decode runs at sequence length < 16 (the batch), which calls
 // for a custom gemv rather than a 16-padded GEMM. The weight matrix is streamed from HBM
@@ -8,8 +10,9 @@
 // together cover all of K, so each rank's max |A| over its own K-slice, combined across the
 // cluster through distributed shared memory, is the global amax. Every CTA derives the same
 // s_a = amax / 448 and quantizes only its own slice, straight from the registers that
-// loaded it, while its TMA ring is already filling with weights. With pre-quantized
-// activations (fp8_scaled_mm) qA and s_a are read instead.
+// loaded it, while its TMA ring is already filling with weights. A static (calibrated)
+// activation scale skips the amax exchange. With pre-quantized activations
+// (fp8_scaled_mm) qA and s_a are read instead.
 //
 // Work split. Rows of W come in blocks of 128; K is split over the S CTAs of a
 // thread-block cluster (rank r owns K-range [r*kslice, (r+1)*kslice)). The grid is
@@ -30,72 +33,30 @@
 #pragma once
 
 #include "device_common.cuh"
+#include "gemv.h"
 
 namespace fp8k {
 namespace gemv {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + one producer warp
-constexpr int kConsumerThreads = 32 * kConsumerWarps;
-constexpr int kRows = 16 * kConsumerWarps;            // 128 rows per row block
-constexpr int kTileK = 128;                           // bytes of K per tile (one swizzle row)
-constexpr int kTileBytes = kRows * kTileK;            // 16 KB
-constexpr int kMaxStages = 8;
-constexpr int kMinStages = 4;
-constexpr int kMaxTokens = 16;
-constexpr int kMaxCluster = 8;
-constexpr int kMaxRowBlocks = 8;                      // per cluster (partials live in smem)
-constexpr int kPartBytes = kRows * kMaxTokens * 4;    // 8 KB per row block
-constexpr int kMaxSlice = 4096;                       // bytes of K per rank
-constexpr int kSmemLimit = 227 * 1024;
-constexpr int kRegUnits = 8;  // 8-element units of A a consumer thread keeps in registers
-
 // Device error bits of the GEMV (bounded waits that expired), read by fp8_last_device_status.
 __device__ unsigned int g_gemv_error;
 
-struct Params {
-  const uint8_t* qa;   // pre-quantized: e4m3 [M, ldqa], bytes [K, ldqa) zero
-  int64_t ldqa;
-  const float* s_a;    // pre-quantized: activation scale (device)
-  const uint16_t* a;   // dynamic: bf16 [M, lda]
-  int64_t lda;
-  int vec_a;           // dynamic: A rows allow 16-byte loads
-  const float* s_w;    // [1] or [N]
-  int per_channel;
-  const uint16_t* bias;  // bf16 [N] or null
-  uint16_t* y;           // bf16 [M, ldy]
-  int64_t ldy;
-  int M, N, K;
-  int kslice;          // bytes of K per rank, multiple of kTileK
-  int act_stride;      // smem row stride of the activation slice (== 64 mod 128)
-  int stages;          // ring depth
-  int row_blocks;      // ceil(N / kRows)
-  int num_clusters;    // C
-};
+// D += W (16 rows x 32 k, format FW) * A^T (32 k x 8 tokens, format FA), fp32 accumulate.
+#define FP8K_MMA_M16N8K32(TW, TA)                                                    \
+  asm volatile("mma.sync.aligned.m16n8k32.row.col.f32." TW "." TA ".f32 "          \
+               "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"              \
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])                      \
+               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1))
 
-// Shared-memory layout (from a 1024-aligned base): ring | act | partials | barriers.
-struct Layout {
-  uint32_t ring, act, part, bars, total;
-};
-
-__host__ __device__ inline Layout layout(int stages, int act_stride, int rb_per_cluster) {
-  Layout L;
-  L.ring = 0;
-  L.act = stages * kTileBytes;
-  L.part = L.act + kMaxTokens * act_stride;
-  L.bars = L.part + rb_per_cluster * kPartBytes;
-  L.total = L.bars + 2 * kMaxStages * 8;
-  return L;
+template <int FW, int FA>
+__device__ __forceinline__ void mma_fp8(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  if constexpr (FW == kFmtE4M3 && FA == kFmtE4M3) FP8K_MMA_M16N8K32("e4m3", "e4m3");
+  else if constexpr (FW == kFmtE4M3) FP8K_MMA_M16N8K32("e4m3", "e5m2");
+  else if constexpr (FA == kFmtE4M3) FP8K_MMA_M16N8K32("e5m2", "e4m3");
+  else FP8K_MMA_M16N8K32("e5m2", "e5m2");
 }
-
-__device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
+#undef FP8K_MMA_M16N8K32
 
 __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
   uint4 v;
@@ -153,8 +114,10 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y) : "memory");
 }
 
-// NT: n8 token tiles (1: M <= 8, 2: M <= 16). kDynamic: A is bf16 and quantized here.
-template <int NT, bool kDynamic>
+// NT: n8 token tiles (1: M <= 8, 2: M <= 16). kDynamic: A is bf16 and quantized here
+// (dynamic scale, or the static one when p.s_static is set). FA / FW: FP8 formats of the
+// activations and the weights.
+template <int NT, bool kDynamic, int FA, int FW>
 __global__ void __launch_bounds__(kThreads, 1)
 gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ Params p) {
   unsigned int* err = &g_gemv_error;
@@ -224,7 +187,8 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     const int span = ntiles * kTileK;  // bytes of K staged per token (zero beyond K)
     float s_a;
     if constexpr (kDynamic) {
-      // max |A| over this rank's slice; the first kRegUnits units per thread stay in registers
+      // max |A| over this rank's slice (dynamic scale); the first kRegUnits units per thread
+      // stay in registers for the quantization below
       const int upt = span >> 3;  // 8-element units per token
       const int units = p.M * upt;
       uint4 v[kRegUnits];
@@ -238,37 +202,43 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
 #pragma unroll
       for (int b = 0; b < kRegUnits; ++b)
         m2 = abs_max_u16x2(abs_max_u16x2(abs_max_u16x2(abs_max_u16x2(m2, v[b].x), v[b].y), v[b].z), v[b].w);
-      for (int i0 = threadIdx.x + kRegUnits * kConsumerThreads; i0 < units; i0 += kRegUnits * kConsumerThreads) {
-        uint4 w[kRegUnits];
+      if (p.s_static == nullptr) {  // dynamic scale: the rest of the slice, for the maximum only
+        for (int i0 = threadIdx.x + kRegUnits * kConsumerThreads; i0 < units; i0 += kRegUnits * kConsumerThreads) {
+          uint4 w[kRegUnits];
 #pragma unroll
-        for (int b = 0; b < kRegUnits; ++b) {
-          const int i = i0 + b * kConsumerThreads;
-          const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
-          w[b] = i < units ? load8_bf16(p.a + (int64_t)m * p.lda, k0 + kk, p.K, p.vec_a) : make_uint4(0, 0, 0, 0);
+          for (int b = 0; b < kRegUnits; ++b) {
+            const int i = i0 + b * kConsumerThreads;
+            const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
+            w[b] = i < units ? load8_bf16(p.a + (int64_t)m * p.lda, k0 + kk, p.K, p.vec_a) : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int b = 0; b < kRegUnits; ++b)
+            m2 = abs_max_u16x2(abs_max_u16x2(abs_max_u16x2(abs_max_u16x2(m2, w[b].x), w[b].y), w[b].z), w[b].w);
         }
-#pragma unroll
-        for (int b = 0; b < kRegUnits; ++b)
-          m2 = abs_max_u16x2(abs_max_u16x2(abs_max_u16x2(abs_max_u16x2(m2, w[b].x), w[b].y), w[b].z), w[b].w);
+        float mx = warp_max(u16x2_max_to_float(m2));
+        if (lane == 0) red[warp] = mx;
+        consumer_bar_sync();
+        if (threadIdx.x == 0) {
+          for (int w = 1; w < kConsumerWarps; ++w) mx = fmaxf(mx, red[w]);
+          slice_amax = mx;
+        }
+        consumer_bar_sync();
       }
-      float mx = warp_max(u16x2_max_to_float(m2));
-      if (lane == 0) red[warp] = mx;
-      consumer_bar_sync();
-      if (threadIdx.x == 0) {
-        for (int w = 1; w < kConsumerWarps; ++w) mx = fmaxf(mx, red[w]);
-        slice_amax = mx;
-      }
-      consumer_bar_sync();
       cluster_arrive();  // phase 1: publish this rank's slice maximum
       cluster_wait();
-      float amax = 0.0f;
-      for (uint32_t src = 0; src < nrank; ++src) amax = fmaxf(amax, ld_dsmem_f32(smem_u32(&slice_amax), src));
-      s_a = scale_from_amax(amax);
+      if (p.s_static == nullptr) {
+        float amax = 0.0f;
+        for (uint32_t src = 0; src < nrank; ++src) amax = fmaxf(amax, ld_dsmem_f32(smem_u32(&slice_amax), src));
+        s_a = scale_from_amax<FA>(amax);
+      } else {
+        s_a = *p.s_static;
+      }
       const Quantizer qz = make_quantizer(s_a);
       // quantize into act[token][k - k0]; units past K and tokens past M are plain zeros
       auto put = [&](int i, const uint4& x) {
         const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
         uint2 q = make_uint2(0, 0);
-        if (k0 + kk < p.K) q = quant8_bf16(x, qz);
+        if (k0 + kk < p.K) q = quant8_bf16<FA>(x, qz);
         asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(act + m * p.act_stride + kk), "r"(q.x), "r"(q.y)
                      : "memory");
       };
@@ -339,8 +309,8 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               const uint4 b = lds_v4(act_lane + nt * 8 * p.act_stride + kt * kTileK + 64 * j);
-              mma_e4m3(acc[nt], wlo.x, whi.x, wlo.y, whi.y, b.x, b.y);
-              mma_e4m3(acc[nt], wlo.z, whi.z, wlo.w, whi.w, b.z, b.w);
+              mma_fp8<FW, FA>(acc[nt], wlo.x, whi.x, wlo.y, whi.y, b.x, b.y);
+              mma_fp8<FW, FA>(acc[nt], wlo.z, whi.z, wlo.w, whi.w, b.z, b.w);
             }
           }
         }

@@ -1,0 +1,73 @@
+// Host-visible interface of the decode GEMV (kernels in gemv.cuh, instantiated in gemv.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace fp8k {
+namespace gemv {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + one producer warp
+constexpr int kConsumerThreads = 32 * kConsumerWarps;
+constexpr int kRows = 16 * kConsumerWarps;            // 128 rows per row block
+constexpr int kTileK = 128;                           // bytes of K per tile (one swizzle row)
+constexpr int kTileBytes = kRows * kTileK;            // 16 KB
+constexpr int kMaxStages = 8;
+constexpr int kMinStages = 4;
+constexpr int kMaxTokens = 16;
+constexpr int kMaxCluster = 8;
+constexpr int kMaxRowBlocks = 8;                      // per cluster (partials live in smem)
+constexpr int kPartBytes = kRows * kMaxTokens * 4;    // 8 KB per row block
+constexpr int kMaxSlice = 4096;                       // bytes of K per rank
+constexpr int kSmemLimit = 227 * 1024;
+constexpr int kRegUnits = 8;  // 8-element units of A a consumer thread keeps in registers
+
+struct Params {
+  const uint8_t* qa;   // pre-quantized: FP8 [M, ldqa], bytes [K, ldqa) zero
+  int64_t ldqa;
+  const float* s_a;    // pre-quantized: activation scale (device)
+  const uint16_t* a;   // quantized here: bf16 [M, lda]
+  int64_t lda;
+  int vec_a;           // quantized here: A rows allow 16-byte loads
+  const float* s_static;  // quantized here: static activation scale (device), or null (dynamic)
+  const float* s_w;    // [1] or [N]
+  int per_channel;
+  const uint16_t* bias;  // bf16 [N] or null
+  uint16_t* y;           // bf16 [M, ldy]
+  int64_t ldy;
+  int M, N, K;
+  int kslice;          // bytes of K per rank, multiple of kTileK
+  int act_stride;      // smem row stride of the activation slice (== 64 mod 128)
+  int stages;          // ring depth
+  int row_blocks;      // ceil(N / kRows)
+  int num_clusters;    // C
+};
+
+// Shared-memory layout (from a 1024-aligned base): ring | act | partials | barriers.
+struct Layout {
+  uint32_t ring, act, part, bars, total;
+};
+
+__host__ __device__ inline Layout layout(int stages, int act_stride, int rb_per_cluster) {
+  Layout L;
+  L.ring = 0;
+  L.act = stages * kTileBytes;
+  L.part = L.act + kMaxTokens * act_stride;
+  L.bars = L.part + rb_per_cluster * kPartBytes;
+  L.total = L.bars + 2 * kMaxStages * 8;
+  return L;
+}
+
+// One instantiation of the kernel: NT n8 token tiles (1: M <= 8, 2: M <= 16), A quantized in
+// the kernel (dyn) or pre-quantized, FP8 formats of the activations (fa) and weights (fw).
+using KernelFn = void (*)(CUtensorMap, Params);
+KernelFn kernel_for(int NT, bool dyn, int fa, int fw);
+
+// Device-side error bits of the GEMV on the current device (read, then cleared).
+unsigned int read_and_clear_error();
+
+}  // namespace gemv
+}  // namespace fp8k

@@ -1,8 +1,10 @@
-// Dynamic FP8 quantization kernels: amax reduction and the saturating RNE cast.
+// FP8 quantization kernels: amax reduction and the saturating RNE cast.
 //
 // Per-tensor scale ("Prototype FP8Linear W8A8 runtime quantization": weights and
 // activations are quantized at run time; "Fp8 Quantization Support": symmetric,
-// strategy "tensor"): s = amax / 448, q = e4m3(x / s).
+// strategy "tensor"): s = amax / 448, q = e4m3(x / s). The format is a template
+// parameter: e5m2 ("Fp8 Quantization Support", the other FP8 dtype) divides amax by
+// 57344 instead. A static (calibrated) activation scale skips the amax pass.
 // Per-output-channel scale ("[Kernel] Implement fallback for FP8 channelwise using
 // torch._scaled_mm"): one s per row of W.
 //
@@ -89,39 +91,41 @@ amax_partials_kernel(const uint16_t* __restrict__ a, int64_t rows, int64_t cols,
   if (threadIdx.x == 0) partials[blockIdx.x] = m;
 }
 
-// Quantize 16 consecutive elements of one row (columns c .. c+15) into 16 e4m3 bytes;
+// Quantize 16 consecutive elements of one row (columns c .. c+15) into 16 FP8 bytes;
 // columns >= cols give 0x00.
+template <int F>
 __device__ __forceinline__ uint4 quant16_row(const uint16_t* __restrict__ src, int64_t c, int64_t cols,
                                              bool vec, const Quantizer& s) {
   uint4 out;
   if (vec && c + 16 <= cols) {
-    const uint2 q0 = quant8_bf16(ld_v4(src), s);
-    const uint2 q1 = quant8_bf16(ld_v4(src + 8), s);
+    const uint2 q0 = quant8_bf16<F>(ld_v4(src), s);
+    const uint2 q1 = quant8_bf16<F>(ld_v4(src + 8), s);
     out = make_uint4(q0.x, q0.y, q1.x, q1.y);
   } else {
     float x[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) x[j] = (c + j < cols) ? bf16_bits_to_float(src[j]) : 0.0f;
-    out.x = quant4(x[0], x[1], x[2], x[3], s);
-    out.y = quant4(x[4], x[5], x[6], x[7], s);
-    out.z = quant4(x[8], x[9], x[10], x[11], s);
-    out.w = quant4(x[12], x[13], x[14], x[15], s);
+    out.x = quant4<F>(x[0], x[1], x[2], x[3], s);
+    out.y = quant4<F>(x[4], x[5], x[6], x[7], s);
+    out.z = quant4<F>(x[8], x[9], x[10], x[11], s);
+    out.w = quant4<F>(x[12], x[13], x[14], x[15], s);
   }
   return out;
 }
 
-// q[r, 0:ldq) = e4m3(A[r, 0:cols) / s) with zero bytes for columns >= cols, where
-// s = scale_from_amax(max of the n_partials partials). CTA 0 stores s to *s_out.
-template <typename Idx>
+// q[r, 0:ldq) = fp8(A[r, 0:cols) / s) with zero bytes for columns >= cols. Dynamic scale
+// (partials != null): s = scale_from_amax(max of the n_partials partials). Static scale
+// (partials == null): s = *s_static. CTA 0 stores s to *s_out unless s_out is null.
+template <typename Idx, int F>
 __global__ void __launch_bounds__(kQuantThreads)
 cast_kernel(const uint16_t* __restrict__ a, int64_t rows, int64_t cols, int64_t ld, int vec,
-            const float* __restrict__ partials, int n_partials, float* __restrict__ s_out,
-            uint8_t* __restrict__ q, int64_t ldq, int pdl) {
+            const float* __restrict__ partials, int n_partials, const float* __restrict__ s_static,
+            float* __restrict__ s_out, uint8_t* __restrict__ q, int64_t ldq, int pdl) {
   __shared__ float red[kQuantThreads / 32];
   if (pdl) pdl_trigger();
   pdl_wait();
-  const float sc = scale_from_amax(block_max_partials(partials, n_partials, red));
-  if (blockIdx.x == 0 && threadIdx.x == 0) *s_out = sc;
+  const float sc = partials ? scale_from_amax<F>(block_max_partials(partials, n_partials, red)) : *s_static;
+  if (s_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *s_out = sc;
   const Quantizer s = make_quantizer(sc);
   const Idx upr = static_cast<Idx>(ldq >> 4);  // 16-byte output units per row
   const Idx units = static_cast<Idx>(rows) * upr;
@@ -129,13 +133,14 @@ cast_kernel(const uint16_t* __restrict__ a, int64_t rows, int64_t cols, int64_t 
   for (Idx u = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x; u < units; u += stride) {
     const Idx r = u / upr;
     const int64_t c = static_cast<int64_t>(u - r * upr) << 4;
-    const uint4 out = quant16_row(a + (int64_t)r * ld + c, c, cols, vec != 0, s);
+    const uint4 out = quant16_row<F>(a + (int64_t)r * ld + c, c, cols, vec != 0, s);
     *reinterpret_cast<uint4*>(q + (int64_t)r * ldq + c) = out;
   }
 }
 
-// Per-row (output channel) weight quantization: CTA per row, s_w[r] = amax(W[r,:]) / 448.
-// The row is read twice; the second read hits L1/L2.
+// Per-row (output channel) weight quantization: CTA per row, s_w[r] = amax(W[r,:]) / 448
+// (57344 for e5m2). The row is read twice; the second read hits L1/L2.
+template <int F>
 __global__ void __launch_bounds__(kQuantThreads)
 quantize_rows_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t K, int64_t ld, int vec,
                      uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s_w) {
@@ -154,13 +159,13 @@ quantize_rows_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t K, int64
     }
     const float m = block_max_to_thread0(u16x2_max_to_float(m2), red);
     if (threadIdx.x == 0) {
-      s_sh = scale_from_amax(m);
+      s_sh = scale_from_amax<F>(m);
       s_w[r] = s_sh;
     }
     __syncthreads();
     const Quantizer s = make_quantizer(s_sh);
     for (int64_t c = (int64_t)threadIdx.x << 4; c < ldq; c += (int64_t)blockDim.x << 4)
-      *reinterpret_cast<uint4*>(q + r * ldq + c) = quant16_row(row + c, c, K, vec != 0, s);
+      *reinterpret_cast<uint4*>(q + r * ldq + c) = quant16_row<F>(row + c, c, K, vec != 0, s);
     __syncthreads();  // s_sh and red are reused by the next row
   }
 }

@@ -67,7 +67,16 @@ typedef enum fp8_status {
   FP8_ERR_UNSUPPORTED_DEVICE = 6  /* current device is not sm_103 */
 } fp8_status;
 
+/* FP8 storage formats. float8_e4m3fn is the pages' format ("Fp8 Quantization
+ * Support": fp8 is assumed to be torch.float8_e4m3fn); float8_e5m2 is the one that
+ * page names as the later extension. Every call without an _ex suffix uses e4m3. */
+typedef enum fp8_format {
+  FP8_E4M3 = 0, /* 1 sign, 4 exponent (bias 7), 3 mantissa bits; max 448; no infinity */
+  FP8_E5M2 = 1  /* 1 sign, 5 exponent (bias 15), 2 mantissa bits; max 57344 */
+} fp8_format;
+
 #define FP8_E4M3_MAX 448.0f
+#define FP8_E5M2_MAX 57344.0f
 #define FP8_LD_ALIGN 16
 /* Workspace needed by fp8_quantize_weight / fp8_quantize_act (partial amax values). */
 #define FP8_QUANT_WORKSPACE_BYTES 4352
@@ -180,6 +189,64 @@ fp8_status fp8_linear_noalloc(const void* a_bf16, int64_t M, int64_t K, int64_t 
                               const uint8_t* qw, int64_t N, int64_t ldqw, const float* s_w,
                               int per_channel, const void* bias_bf16, void* y_bf16, int64_t ldy,
                               fp8_stream_t stream);
+
+/*
+ * ---------------------------------------------------------------------------
+ * Wider calls: the format of each FP8 operand, and a static activation scale.
+ * In all of them, for format F: max(F) = 448 (FP8_E4M3) or 57344 (FP8_E5M2),
+ * dynamic scale = amax / max(F), q = F(x / scale) with the rounding and
+ * saturation rules above (saturation to +-max(F), never infinity).
+ * Invalid format values return FP8_ERR_INVALID_ARG.
+ * ---------------------------------------------------------------------------
+ */
+
+/* fp8_quantize_weight with the weight format `fmt`. */
+fp8_status fp8_quantize_weight_ex(const void* w_bf16, int64_t N, int64_t K, int64_t ldw,
+                                  int per_channel, fp8_format fmt, uint8_t* qw, int64_t ldq,
+                                  float* s_w, void* ws, size_t ws_bytes, fp8_stream_t stream);
+
+/*
+ * fp8_quantize_act with the activation format `fmt` and an optional static
+ * scale. s_static == NULL: dynamic, s_a[0] = amax(A) / max(fmt); ws as for
+ * fp8_quantize_act. s_static != NULL (device fp32 [1], 4-byte aligned): the
+ * calibrated scale is used as given ("Fp8 Quantization Support": the recipe
+ * quantizes input activations per tensor with scales from the calibration
+ * run), no amax pass runs, s_a[0] receives a copy of it and ws may be NULL.
+ * Elements beyond s * max(fmt) saturate. The scale must be positive and finite.
+ */
+fp8_status fp8_quantize_act_ex(const void* a_bf16, int64_t M, int64_t K, int64_t lda,
+                               fp8_format fmt, const float* s_static, uint8_t* qa, int64_t ldq,
+                               float* s_a, void* ws, size_t ws_bytes, fp8_stream_t stream);
+
+/* fp8_scaled_mm with the formats of qA (fmt_a) and qW (fmt_w); any pairing. */
+fp8_status fp8_scaled_mm_ex(const uint8_t* qa, fp8_format fmt_a, int64_t M, int64_t K, int64_t ldqa,
+                            const float* s_a, const uint8_t* qw, fp8_format fmt_w, int64_t N,
+                            int64_t ldqw, const float* s_w, int per_channel, const void* bias_bf16,
+                            void* y_bf16, int64_t ldy, fp8_stream_t stream);
+
+/*
+ * The W8A8 linear with a static (calibrated) per-tensor activation scale s_a
+ * (device fp32 [1]) instead of the dynamic one: qA = e4m3(A / s_a), then the
+ * same product and epilogue as fp8_linear (per_channel == 0) or
+ * fp8_linear_channelwise (per_channel == 1). No amax is computed. Workspace as
+ * for fp8_linear (fp8_workspace_bytes).
+ */
+fp8_status fp8_linear_static(const void* a_bf16, int64_t M, int64_t K, int64_t lda,
+                             const float* s_a, const uint8_t* qw, int64_t N, int64_t ldqw,
+                             const float* s_w, int per_channel, const void* bias_bf16,
+                             void* y_bf16, int64_t ldy, void* ws, size_t ws_bytes,
+                             fp8_stream_t stream);
+
+/*
+ * The general linear: activation format fmt_a, weight format fmt_w (qW as
+ * written by fp8_quantize_weight_ex with that format), dynamic activation
+ * scale when s_static is NULL, else the static one; per_channel selects the
+ * weight-scale mode. Workspace as for fp8_linear.
+ */
+fp8_status fp8_linear_ex(const void* a_bf16, int64_t M, int64_t K, int64_t lda, fp8_format fmt_a,
+                         const float* s_static, const uint8_t* qw, fp8_format fmt_w, int64_t N,
+                         int64_t ldqw, const float* s_w, int per_channel, const void* bias_bf16,
+                         void* y_bf16, int64_t ldy, void* ws, size_t ws_bytes, fp8_stream_t stream);
 
 /*
  * Synchronizes `stream`, then reports and clears device-side errors recorded

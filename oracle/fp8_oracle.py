@@ -252,7 +252,9 @@ def quantize_with_scale(x: np.ndarray, s, fmt: str = "e4m3") -> np.ndarray:
     With a static (calibrated) s this is the whole activation quantization: values
     beyond s * 448 (s * 57344) saturate."""
     x = np.asarray(x, dtype=np.float32)
-    return encode((x / np.asarray(s, dtype=np.float32)).astype(np.float32), fmt)
+    with np.errstate(over="ignore"):  # an fp32 quotient may overflow to inf; it then saturates
+        q = (x / np.asarray(s, dtype=np.float32)).astype(np.float32)
+    return encode(q, fmt)
 
 
 def quantize_per_tensor(x: np.ndarray, fmt: str = "e4m3") -> Tuple[np.ndarray, np.float32]:

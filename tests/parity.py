@@ -13,21 +13,22 @@ def f32(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy()
 
 
-def oracle_weight(w: torch.Tensor, per_channel: bool, rows: Optional[np.ndarray] = None):
+def oracle_weight(w: torch.Tensor, per_channel: bool, rows: Optional[np.ndarray] = None, fmt: str = "e4m3"):
     """Oracle qW/s_w for the selected rows (per-tensor scale from the full W)."""
     w32 = f32(w)
     sel = w32 if rows is None else w32[rows]
     if per_channel:
-        return O.quantize_per_row(sel)
-    s = np.float32(O.scale_from_amax(O.amax(w32)))
-    return O.quantize_with_scale(sel, s), s
+        return O.quantize_per_row(sel, fmt)
+    s = np.float32(O.scale_from_amax(O.amax(w32), fmt))
+    return O.quantize_with_scale(sel, s, fmt), s
 
 
-def oracle_act(a: torch.Tensor, rows: Optional[np.ndarray] = None):
+def oracle_act(a: torch.Tensor, rows: Optional[np.ndarray] = None, fmt: str = "e4m3", s_static=None):
+    """Oracle qA/s_a for the selected rows: dynamic scale from all of A, or the static one."""
     a32 = f32(a)
-    s = np.float32(O.scale_from_amax(O.amax(a32)))
+    s = np.float32(O.scale_from_amax(O.amax(a32), fmt)) if s_static is None else np.float32(s_static)
     sel = a32 if rows is None else a32[rows]
-    return O.quantize_with_scale(sel, s), s
+    return O.quantize_with_scale(sel, s, fmt), s
 
 
 def assert_codes_equal(q_gpu: torch.Tensor, q_ref: np.ndarray, K: int, what: str):
@@ -46,9 +47,10 @@ def assert_scale_equal(s_gpu: torch.Tensor, s_ref, what: str):
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), f"{what}: scale {got[:4]} != {want[:4]}"
 
 
-def assert_y_within_tolerance(y_gpu: np.ndarray, qa, s_a, qw, s_w, bias: Optional[np.ndarray], what: str):
-    y_ref = O.scaled_mm(qa, s_a, qw, s_w, bias)
-    tol = O.tolerance(qa, s_a, qw, s_w, y_ref)
+def assert_y_within_tolerance(y_gpu: np.ndarray, qa, s_a, qw, s_w, bias: Optional[np.ndarray], what: str,
+                              fmt_a: str = "e4m3", fmt_w: str = "e4m3"):
+    y_ref = O.scaled_mm(qa, s_a, qw, s_w, bias, fmt_a=fmt_a, fmt_w=fmt_w)
+    tol = O.tolerance(qa, s_a, qw, s_w, y_ref, fmt_a, fmt_w)
     err = np.abs(y_gpu.astype(np.float64) - y_ref.astype(np.float64))
     bad = np.argwhere(~(err <= tol))
     assert bad.size == 0, (f"{what}: {len(bad)} of {err.size} outputs outside tolerance; first "
@@ -59,15 +61,16 @@ def assert_y_within_tolerance(y_gpu: np.ndarray, qa, s_a, qw, s_w, bias: Optiona
 
 def linear_parity(y: torch.Tensor, a: torch.Tensor, w: torch.Tensor, per_channel: bool,
                   bias: Optional[torch.Tensor] = None, rows: Optional[Sequence[int]] = None,
-                  cols: Optional[Sequence[int]] = None, what: str = "Y") -> float:
+                  cols: Optional[Sequence[int]] = None, what: str = "Y", fmt_a: str = "e4m3",
+                  fmt_w: str = "e4m3", s_static=None) -> float:
     """Compare the library's Y (full [M, N] on device) with the oracle on rows x cols."""
     rows = np.arange(a.shape[0]) if rows is None else np.asarray(rows)
     cols = np.arange(w.shape[0]) if cols is None else np.asarray(cols)
-    qa, s_a = oracle_act(a, rows)
-    qw, s_w = oracle_weight(w, per_channel, cols)
+    qa, s_a = oracle_act(a, rows, fmt_a, s_static)
+    qw, s_w = oracle_weight(w, per_channel, cols, fmt_w)
     b = None if bias is None else f32(bias)[cols]
     y_gpu = f32(y)[np.ix_(rows, cols)]
-    return assert_y_within_tolerance(y_gpu, qa, s_a, qw, s_w, b, what)
+    return assert_y_within_tolerance(y_gpu, qa, s_a, qw, s_w, b, what, fmt_a, fmt_w)
 
 
 def guarded(shape, dtype, device, guard: int = 64, fill: int = 0x5A):

@@ -147,3 +147,34 @@ def test_valid_call_without_gpu_reports_cuda_error(L):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert lin(L) in (F.FP8_ERR_CUDA, F.FP8_ERR_UNSUPPORTED_DEVICE)
+
+
+def test_wider_calls_reject_bad_formats_and_scales(L):
+    """Format values other than FP8_E4M3 / FP8_E5M2 and a missing static scale are refused
+    before anything touches a device."""
+    ex = L.fp8_linear_ex
+    args = lambda fa, fw, s=None, pc=0: (P, 4, 64, 64, fa, s, P, fw, 32, 64, P, pc, None, P, 32, WS, 1 << 20, None)
+    for fa, fw in ((2, 0), (0, 2), (-1, 1), (1, 7)):
+        assert ex(*args(fa, fw)) == F.FP8_ERR_INVALID_ARG
+    assert ex(*args(0, 0, pc=2)) == F.FP8_ERR_INVALID_ARG
+    assert ex(*args(0, 0, s=P + 2)) == F.FP8_ERR_MISALIGNED      # static scale not 4-byte aligned
+    st = L.fp8_linear_static
+    assert st(P, 4, 64, 64, None, P, 32, 64, P, 0, None, P, 32, WS, 1 << 20, None) == F.FP8_ERR_INVALID_ARG
+    qw = L.fp8_quantize_weight_ex
+    assert qw(P, 8, 64, 64, 0, 3, P, 64, P, WS, 1 << 16, None) == F.FP8_ERR_INVALID_ARG
+    qa = L.fp8_quantize_act_ex
+    assert qa(P, 8, 64, 64, 5, None, P, 64, P, WS, 1 << 16, None) == F.FP8_ERR_INVALID_ARG
+    assert qa(P, 8, 64, 64, 1, None, P, 64, P, WS, 16, None) == F.FP8_ERR_WORKSPACE   # dynamic needs ws
+    assert qa(P, 8, 64, 64, 1, P + 1, P, 64, P, None, 0, None) == F.FP8_ERR_MISALIGNED
+    sm = L.fp8_scaled_mm_ex
+    assert sm(P, 9, 4, 64, 64, P, P, 0, 8, 64, P, 0, None, P, 8, None) == F.FP8_ERR_INVALID_ARG
+    assert sm(P, 0, 4, 64, 64, P, P, 9, 8, 64, P, 0, None, P, 8, None) == F.FP8_ERR_INVALID_ARG
+
+
+def test_static_quantize_needs_no_workspace(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # static scale: validation passes without a workspace; only the device query fails here
+    assert L.fp8_quantize_act_ex(P, 8, 64, 64, 0, P, P, 64, P, None, 0, None) in (
+        F.FP8_ERR_CUDA, F.FP8_ERR_UNSUPPORTED_DEVICE)
