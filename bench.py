@@ -164,6 +164,75 @@ def graph_of(torch, fn):
     return g
 
 
+def measure_variants(torch, F, I, args, dev, layers, names, host, A, Y, ws, M):
+    """Prefill TFLOP/s and decode weight GB/s of the wider calls on the headline workloads:
+    float8_e5m2 for both operands (dynamic scale), e4m3 with a static activation scale (the
+    calibrated value is the dynamic scale of the same activations), and the weight-only path
+    (bf16 activations, e4m3 weights up-converted to bf16)."""
+    out = {}
+    steps = max(3, args.steps // 4)
+    W5 = [F.fp8_quantize_weight_ex(w.to(dev), "e5m2", per_channel=True) for _, _, w in host]
+    W4 = [F.fp8_quantize_weight(w.to(dev), per_channel=True) for _, _, w in host]
+    S = [F.fp8_quantize_act(a)[1] for a in A]
+    torch.cuda.synchronize()
+    total = flops(M, layers)
+
+    def pre_e5m2():
+        for i in range(len(layers)):
+            F.fp8_linear_ex(A[i], W5[i][0], W5[i][1], per_channel=True, out=Y[i], ws=ws, fmt_a="e5m2",
+                            fmt_w="e5m2")
+
+    def pre_static():
+        for i in range(len(layers)):
+            F.fp8_linear_static(A[i], S[i], W4[i][0], W4[i][1], per_channel=True, out=Y[i], ws=ws)
+
+    ws_wo = torch.empty(max(F.fp8_weight_only_workspace_bytes(M, L.K, L.N) for L in layers), dtype=torch.uint8,
+                        device=dev)
+
+    def pre_weight_only():
+        for i in range(len(layers)):
+            F.fp8_linear_weight_only(A[i], W4[i][0], W4[i][1], per_channel=True, out=Y[i], ws=ws_wo)
+
+    for name, fn in (("e5m2_dynamic", pre_e5m2), ("e4m3_static", pre_static), ("weight_only_e4m3", pre_weight_only)):
+        t = time_loop(torch, fn, steps, 2)
+        out[name] = {"prefill_tflops": round(total / (t * 1e-3) / 1e12, 1), "prefill_ms_per_step": round(t, 4)}
+    out["weight_only_e4m3"]["note"] = ("bf16 A x up-converted bf16 W on tcgen05 kind::f16 (the up-conversion pass "
+                                       "is inside the step); compare with the bf16 peak, not the FP8 one")
+    del W5, W4, ws_wo
+    if not args.no_decode:
+        li = [i for i, _ in selected_layers(names)]
+        copies = args.decode_copies
+        wbytes = copies * sum(L.N * L.K for L in layers)
+        d5 = [[F.fp8_quantize_weight_ex(I.decode_weight(i, c).to(dev), "e5m2") for i in li] for c in range(copies)]
+        d4 = [[F.fp8_quantize_weight(I.decode_weight(i, c).to(dev)) for i in li] for c in range(copies)]
+        yd = [torch.empty((16, L.N), dtype=torch.bfloat16, device=dev) for L in layers]
+        for Md in (1, 15):
+            ad = [I.decode_activations(Md, i).to(dev) for i in li]
+            sd = [F.fp8_quantize_act(a)[1] for a in ad]
+
+            def d_e5m2(ad=ad, Md=Md):
+                for c in range(copies):
+                    for i in range(len(layers)):
+                        F.fp8_linear_ex(ad[i], d5[c][i][0], d5[c][i][1], out=yd[i][:Md], fmt_a="e5m2", fmt_w="e5m2")
+
+            def d_static(ad=ad, sd=sd, Md=Md):
+                for c in range(copies):
+                    for i in range(len(layers)):
+                        F.fp8_linear_static(ad[i], sd[i], d4[c][i][0], d4[c][i][1], out=yd[i][:Md])
+
+            def d_weight_only(ad=ad, Md=Md):
+                for c in range(copies):
+                    for i in range(len(layers)):
+                        F.fp8_linear_weight_only(ad[i], d4[c][i][0], d4[c][i][1], out=yd[i][:Md])
+
+            for name, fn in (("e5m2_dynamic", d_e5m2), ("e4m3_static", d_static), ("weight_only_e4m3", d_weight_only)):
+                t = time_loop(torch, graph_of(torch, fn).replay, max(5, args.steps), 3)
+                out[name][f"decode_M{Md}_weight_gbs"] = round(wbytes / (t * 1e-3) / 1e9, 1)
+        del d5, d4
+    torch.cuda.synchronize()
+    return out
+
+
 def run_ours(args, rank: int, world: int):
     import torch
     import fp8_w8a8_quantized_dynamic_gb300 as F
@@ -252,6 +321,11 @@ def run_ours(args, rank: int, world: int):
                     "peak_source": f"{peak_src} bf16 burst x {NOMINAL_FP8_OVER_BF16} nominal fp8/bf16 ratio",
                     "per_layer_ms": {L.name: round(t, 4) for L, t in zip(layers, gemm_ms)}}
 
+    # ---- wider rows on the same workloads: e5m2 operands, static activation scale
+    variants = None
+    if not args.no_variants and not args.no_prefill:
+        variants = measure_variants(torch, F, I, args, dev, layers, names, host, A, Y, ws, M)
+
     # ---- decode GEMV: Mistral-7B layers, per-tensor scales, weight copies rotated past L2
     decode = None
     if not args.no_decode:
@@ -326,7 +400,7 @@ def run_ours(args, rank: int, world: int):
                          "1.4 GB of outputs across four layers"},
         "roofline": roofline, "kernels_ms": {"quantize_act(amax+cast)": [round(t, 4) for t in quant_ms],
                                              "gemm": [round(t, 4) for t in gemm_ms]},
-        "decode": decode, "e2e": e2e, "gpu_launches": launches,
+        "decode": decode, "variants": variants, "e2e": e2e, "gpu_launches": launches,
         "gpu_launches_note": "timed prefill region: 3 kernels per layer per step (amax, cast, GEMM)",
         "clocks": clk, "cpu_baseline": cpu,
     }
@@ -407,6 +481,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="decode leg only (profiling)")
     ap.add_argument("--layers", default="", help="comma list of qkv,o_proj,gate_up,down (default all)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-variants", action="store_true", help="skip the e5m2 / static-scale legs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
 

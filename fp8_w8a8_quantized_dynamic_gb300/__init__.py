@@ -14,6 +14,7 @@ Typical use::
     y = fp8_linear_static(a, s_a, qw, s_w)           # calibrated activation scale
     qw, s_w = fp8_quantize_weight(w, fmt="e5m2")     # the other FP8 format
     y = fp8_linear_ex(a, qw, s_w, fmt_a="e5m2", fmt_w="e5m2")
+    y = fp8_linear_weight_only(a, qw, s_w, fmt_w="e5m2")  # bf16 A, FP8 weights up-converted
 """
 
 from __future__ import annotations
@@ -60,6 +61,9 @@ _SIGNATURES = {
                                  _sz, _vp]),
     "fp8_linear_ex": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _vp, _int, _i64, _i64, _vp, _int, _vp, _vp, _i64,
                              _vp, _sz, _vp]),
+    "fp8_weight_only_workspace_bytes": (_sz, [_i64, _i64, _i64]),
+    "fp8_linear_weight_only": (_int, [_vp, _i64, _i64, _i64, _vp, _int, _i64, _i64, _vp, _int, _vp, _vp, _i64,
+                                      _vp, _sz, _vp]),
     "fp8_last_device_status": (_int, [_vp]),
     "fp8_status_string": (ctypes.c_char_p, [_int]),
 }
@@ -294,6 +298,29 @@ def fp8_linear_ex(a, qw, s_w, per_channel: bool = False, bias=None, out=None, ws
                                _fmt(fmt_w), N, qw.stride(0), s_w.data_ptr(), int(per_channel), _ptr(bias),
                                y.data_ptr(), y.stride(0), _ptr(ws), 0 if ws is None else ws.numel(),
                                _stream_ptr(a)), "fp8_linear_ex")
+    return y
+
+
+def fp8_weight_only_workspace_bytes(M: int, K: int, N: int) -> int:
+    return int(lib().fp8_weight_only_workspace_bytes(M, K, N))
+
+
+def fp8_linear_weight_only(a, qw, s_w, per_channel: bool = False, bias=None, out=None, ws=None,
+                           fmt_w: str = "e4m3"):
+    """Weight-only FP8 linear: bf16 A times the exactly up-converted FP8 weights, scaled by s_w."""
+    torch = _torch()
+    _check_bf16_2d(a, "a")
+    M, K = a.shape
+    _check_fp8_2d(qw, K, "qw")
+    N = qw.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    if ws is None:
+        need = fp8_weight_only_workspace_bytes(M, K, N)
+        ws = torch.empty(need, dtype=torch.uint8, device=a.device) if need else None
+    _check(lib().fp8_linear_weight_only(a.data_ptr(), M, K, a.stride(0), qw.data_ptr(), _fmt(fmt_w), N,
+                                        qw.stride(0), s_w.data_ptr(), int(per_channel), _ptr(bias), y.data_ptr(),
+                                        y.stride(0), _ptr(ws), 0 if ws is None else ws.numel(), _stream_ptr(a)),
+           "fp8_linear_weight_only")
     return y
 
 

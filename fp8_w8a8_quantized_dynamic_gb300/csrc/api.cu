@@ -233,7 +233,15 @@ int gemv_max_clusters(gemv::KernelFn kfn, int S, size_t smem) {
 // Persistent split-K GEMV on e4m3 activations. Picks the cluster size S (K split) and the
 // number of clusters C so that the CTA with the most work streams as few 16 KB weight tiles
 // as possible, every cluster holds at most kMaxRowBlocks row blocks, and the smem fits.
-fp8_status launch_gemv(gemv::Params p, bool dyn, int fmt_a, int fmt_w, const uint8_t* qw, int64_t ldqw,
+// Shared-memory row stride (bytes) of a K-slice of activations: FP8 rows are padded to 64 mod
+// 128, bf16 rows (two bytes an element) to 16 mod 128, so the fragment loads of a warp spread
+// over all banks.
+int gemv_act_stride(int mode, int kslice) {
+  if (mode == gemv::kModeBf16) return 2 * kslice + 16;
+  return kslice % 128 == 0 ? kslice + 64 : kslice;
+}
+
+fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uint8_t* qw, int64_t ldqw,
                        cudaStream_t st) {
   using namespace gemv;
   const int R = (p.N + kRows - 1) / kRows;
@@ -241,15 +249,17 @@ fp8_status launch_gemv(gemv::Params p, bool dyn, int fmt_a, int fmt_w, const uin
   int best_cost = -1, bS = 1, bC = 1, bstages = kMaxStages, bslice = kTileK;
   size_t bsmem = 0;
   const int NT = p.M <= 8 ? 1 : 2;
-  const KernelFn kfn = kernel_for(NT, dyn, fmt_a, fmt_w);
+  const bool dyn = mode == gemv::kModeQuantize;
+  const int max_slice = mode == gemv::kModeBf16 ? kMaxSliceBf16 : kMaxSlice;
+  const KernelFn kfn = kernel_for(NT, mode, fmt_a, fmt_w);
   const int smem_limit = gemv_smem_limit(kfn);
   for (int S : {1, 2, 4, 8}) {
     if (S > KT) break;
     const int slice_tiles = (KT + S - 1) / S;
     if ((KT + slice_tiles - 1) / slice_tiles != S) continue;  // every rank must own tiles
     const int kslice = slice_tiles * kTileK;
-    if (kslice > kMaxSlice) continue;
-    const int act_stride = kslice % 128 == 0 ? kslice + 64 : kslice;
+    if (kslice > max_slice) continue;
+    const int act_stride = gemv_act_stride(mode, kslice);
     int stages = kMaxStages;
     auto smem_for = [&](int stg, int nrb) { return size_t(layout(stg, act_stride, nrb).total) + 1024; };
     while (stages > kMinStages && smem_for(stages, kMaxRowBlocks) > size_t(smem_limit)) --stages;
@@ -279,7 +289,7 @@ fp8_status launch_gemv(gemv::Params p, bool dyn, int fmt_a, int fmt_w, const uin
     return FP8_ERR_CUDA;
   }
   p.kslice = bslice;
-  p.act_stride = bslice % 128 == 0 ? bslice + 64 : bslice;
+  p.act_stride = gemv_act_stride(mode, bslice);
   p.stages = bstages;
   p.row_blocks = R;
   p.num_clusters = bC;
@@ -354,7 +364,7 @@ fp8_status linear_impl(const void* a, int64_t M, int64_t K, int64_t lda, int fmt
     p.lda = lda;
     p.vec_a = A.vec();
     p.s_static = s_static;
-    return launch_gemv(p, true, fmt_a, fmt_w, qw, ldqw, st);
+    return launch_gemv(p, gemv::kModeQuantize, fmt_a, fmt_w, qw, ldqw, st);
   }
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* partials = reinterpret_cast<float*>(wsb);
@@ -438,10 +448,84 @@ fp8_status scaled_mm_impl(const uint8_t* qa, int fmt_a, int64_t M, int64_t K, in
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (K == 0) return launch_fill_bias(bias_bf16, y_bf16, M, N, ldy, sms, st);
   if (use_gemv(M, K))
-    return launch_gemv(gemv_params(qa, ldqa, s_a, s_w, per_channel, bias_bf16, y_bf16, ldy, M, N, K), false, fmt_a,
-                       fmt_w, qw, ldqw, st);
+    return launch_gemv(gemv_params(qa, ldqa, s_a, s_w, per_channel, bias_bf16, y_bf16, ldy, M, N, K), gemv::kModePrequant,
+                       fmt_a, fmt_w, qw, ldqw, st);
   if (fp8k::gemm_launch(qa, ldqa, s_a, qw, ldqw, s_w, per_channel, static_cast<const uint16_t*>(bias_bf16),
                         static_cast<uint16_t*>(y_bf16), ldy, int(M), int(N), int(K), fmt_a, fmt_w, sms, st) != 0)
+    return FP8_ERR_CUDA;
+  return FP8_OK;
+}
+
+// ---------------------------------------------------------------------------
+// weight-only FP8 linear: bf16 activations, FP8 weights up-converted to bf16
+// ---------------------------------------------------------------------------
+
+int64_t round_up8(int64_t k) { return (k + 7) / 8 * 8; }
+size_t round_up256(size_t b) { return (b + 255) / 256 * 256; }
+
+// Decode shapes stream the FP8 weights through the GEMV, up-converting each tile in registers
+// (bf16 activation slices of at most kMaxSliceBf16 per rank); larger shapes up-convert W once
+// into the workspace and run the bf16 tcgen05 GEMM.
+bool use_gemv_weight_only(int64_t M, int64_t K) {
+  return M <= gemv_max_m() && K <= int64_t(gemv::kMaxCluster) * gemv::kMaxSliceBf16;
+}
+
+// GEMM path: up-converted W [N, round_up8(K)] bf16, then room for a 16-byte-aligned copy of A
+// [M, round_up8(K)] (used only when A's rows are not 16-byte aligned).
+size_t weight_only_ws_bytes(int64_t M, int64_t K, int64_t N) {
+  if (M <= 0 || K <= 0 || N <= 0 || use_gemv_weight_only(M, K)) return 0;
+  return round_up256(size_t(N) * size_t(round_up8(K)) * 2) + size_t(M) * size_t(round_up8(K)) * 2;
+}
+
+fp8_status weight_only_impl(const void* a, int64_t M, int64_t K, int64_t lda, const uint8_t* qw, int fmt_w,
+                            int64_t N, int64_t ldqw, const float* s_w, int per_channel, const void* bias, void* y,
+                            int64_t ldy, void* ws, size_t ws_bytes, fp8_stream_t stream) {
+  if (!valid_fmt(fmt_w) || (per_channel != 0 && per_channel != 1)) return FP8_ERR_INVALID_ARG;
+  FP8_TRY(check_bf16_mat(a, M, K, lda));
+  FP8_TRY(check_fp8_mat(qw, N, K, ldqw));
+  FP8_TRY(check_bf16_mat(y, M, N, ldy));
+  if (N > 0 && s_w == nullptr) return FP8_ERR_INVALID_ARG;
+  if (!aligned(bias, 2)) return FP8_ERR_MISALIGNED;
+  if (M == 0 || N == 0) return FP8_OK;
+  FP8_TRY(check_ws(ws, ws_bytes, weight_only_ws_bytes(M, K, N)));
+  int sms = 0;
+  FP8_TRY(current_device(&sms));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return launch_fill_bias(bias, y, M, N, ldy, sms, st);
+
+  const BF16Mat A{static_cast<const uint16_t*>(a), M, K, lda};
+  if (use_gemv_weight_only(M, K)) {
+    gemv::Params p = gemv_params(nullptr, 0, nullptr, s_w, per_channel, bias, y, ldy, M, N, K);
+    p.a = A.p;
+    p.lda = lda;
+    p.vec_a = A.vec();
+    return launch_gemv(p, gemv::kModeBf16, kFmtE4M3, fmt_w, qw, ldqw, st);
+  }
+  const int64_t ldk = round_up8(K);
+  uint16_t* wb = static_cast<uint16_t*>(ws);
+  {
+    const int64_t units = N * (ldk / 8);
+    const int g = int(std::max<int64_t>(1, std::min<int64_t>((units + kQuantThreads - 1) / kQuantThreads,
+                                                             int64_t(sms) * 8)));
+    auto go = [&](auto kernel) {
+      return launch(kernel, dim3(g), dim3(kQuantThreads), 0, st, true, dim3(1, 1, 1), qw, N, K, ldqw, wb, ldk);
+    };
+    FP8_TRY(fmt_w == kFmtE5M2 ? go(upconvert_kernel<kFmtE5M2>) : go(upconvert_kernel<kFmtE4M3>));
+  }
+  const uint16_t* a_tma = A.p;
+  int64_t lda_tma = lda;
+  if ((lda * 2) % 16 != 0 || !aligned(A.p, 16)) {
+    uint16_t* acopy = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + round_up256(size_t(N) * ldk * 2));
+    const int64_t units = M * (ldk / 8);
+    const int g = int(std::max<int64_t>(1, std::min<int64_t>((units + kQuantThreads - 1) / kQuantThreads,
+                                                             int64_t(sms) * 8)));
+    FP8_TRY(launch(copy_rows_bf16_kernel, dim3(g), dim3(kQuantThreads), 0, st, true, dim3(1, 1, 1), A.p, M, K, lda,
+                   A.vec(), acopy, ldk, 1));
+    a_tma = acopy;
+    lda_tma = ldk;
+  }
+  if (gemm_bf16_launch(a_tma, lda_tma, wb, ldk, s_w, per_channel, static_cast<const uint16_t*>(bias),
+                       static_cast<uint16_t*>(y), ldy, int(M), int(N), int(K), sms, st) != 0)
     return FP8_ERR_CUDA;
   return FP8_OK;
 }
@@ -532,6 +616,18 @@ FP8_API fp8_status fp8_linear_ex(const void* a_bf16, int64_t M, int64_t K, int64
                                  void* ws, size_t ws_bytes, fp8_stream_t stream) {
   return linear_impl(a_bf16, M, K, lda, int(fmt_a), s_static, qw, int(fmt_w), N, ldqw, s_w, per_channel, bias_bf16,
                      y_bf16, ldy, ws, ws_bytes, stream);
+}
+
+FP8_API size_t fp8_weight_only_workspace_bytes(int64_t M, int64_t K, int64_t N) {
+  return weight_only_ws_bytes(M, K, N);
+}
+
+FP8_API fp8_status fp8_linear_weight_only(const void* a_bf16, int64_t M, int64_t K, int64_t lda, const uint8_t* qw,
+                                          fp8_format fmt_w, int64_t N, int64_t ldqw, const float* s_w,
+                                          int per_channel, const void* bias_bf16, void* y_bf16, int64_t ldy,
+                                          void* ws, size_t ws_bytes, fp8_stream_t stream) {
+  return weight_only_impl(a_bf16, M, K, lda, qw, int(fmt_w), N, ldqw, s_w, per_channel, bias_bf16, y_bf16, ldy, ws,
+                          ws_bytes, stream);
 }
 
 FP8_API fp8_status fp8_last_device_status(fp8_stream_t stream) {

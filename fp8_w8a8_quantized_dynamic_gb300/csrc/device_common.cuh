@@ -3,6 +3,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace fp8k {
 
@@ -37,6 +38,21 @@ __device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
   else
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Two FP8 codes of format F (bits 0..7 and 8..15) -> the same two values as bf16x2 (exact:
+// every e4m3 and e5m2 value is a bf16 value), via the exact FP8 -> f16 conversion.
+template <int F>
+__device__ __forceinline__ uint32_t fp8x2_to_bf16x2(uint32_t codes) {
+  uint32_t h;
+  const uint16_t c = uint16_t(codes);
+  if constexpr (F == kFmtE5M2)
+    asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h) : "h"(c));
+  else
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(c));
+  const float lo = __half2float(__ushort_as_half(uint16_t(h))), hi = __half2float(__ushort_as_half(uint16_t(h >> 16)));
+  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&b);
 }
 
 // Quantizer for one scale s: FP8 codes of fl32(x / s), most of the time without a division.

@@ -9,6 +9,12 @@
 // each e4m3 or e5m2 ("Fp8 Quantization Support"): the operand formats are fields of the
 // MMA instruction descriptor, so one kernel serves every pairing.
 //
+// The same kernel, instantiated with kBf16, runs the weight-only product (bf16 A times the
+// up-converted bf16 weights, "Prototype FP8Linear W8A8 runtime quantization") on
+// tcgen05.mma kind::f16: a stage still holds 128-byte rows, now of 64 bf16 elements, and
+// one MMA still consumes 32 bytes of K (16 elements), so tiles, descriptors and the ring
+// are unchanged.
+//
 // Structure (one CTA per SM, persistent over output tiles of 128 x 256):
 //   warp 0      TMA producer: qA tile [128 x 128B] and qW tile [256 x 128B] per stage into a
 //               4-stage ring of 128B-swizzled shared memory, completion on an mbarrier.
@@ -38,7 +44,7 @@ __device__ unsigned int g_gemm_error;
 
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int BK = 128;  // bytes (= FP8 elements) of K per stage: one 128-byte swizzle row
+constexpr int BK = 128;  // bytes of K per stage: one 128-byte swizzle row (128 FP8 / 64 bf16 elements)
 constexpr int kStages = 4;
 constexpr int kAccBufs = 2;
 constexpr int kTmemCols = kAccBufs * BN;  // 512: the whole tensor memory of the SM
@@ -47,7 +53,7 @@ constexpr int kEpiThreads = 128;
 constexpr uint32_t kABytes = BM * BK;
 constexpr uint32_t kBBytes = BN * BK;
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr int kMmaK = 32;  // K of one kind::f8f6f4 MMA
+constexpr int kMmaK = 32;  // bytes of K of one MMA (32 FP8 elements, kind::f8f6f4; 16 bf16, kind::f16)
 
 struct SharedCtl {
   uint64_t full[kStages];
@@ -72,6 +78,9 @@ constexpr uint32_t make_idesc(int fmt_a, int fmt_w) {
   return kIdescBase | (uint32_t(fmt_a) << 7) | (uint32_t(fmt_w) << 10);
 }
 
+// kind::f16 with bf16 A and B: the format fields hold BF16 = 1.
+constexpr uint32_t kIdescBf16 = kIdescBase | (1u << 7) | (1u << 10);
+
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA with 128-byte
 // swizzle: rows of 128 bytes, 8-row swizzle atoms of 1024 bytes (stride byte offset), start
 // address >> 4 in bits 0-13, descriptor version 1 at bit 46, swizzle mode 2 (128B) at bits 61-63.
@@ -92,12 +101,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y) : "memory");
 }
 
-__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
-      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+template <bool kBf16>
+__device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  if constexpr (kBf16)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -149,9 +165,12 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& 
   n_idx = n_first + (r - m_idx * gn);
 }
 
+// kBf16: operands are bf16 (weight-only product) instead of FP8.
+template <bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
             const __grid_constant__ GemmParams p) {
+  constexpr int kElemsPerStage = kBf16 ? BK / 2 : BK;  // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-aligned for the 128B swizzle
@@ -162,7 +181,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_tiles = p.m_tiles * p.n_tiles;
-  const int num_kb = (p.K + BK - 1) / BK;
+  const int num_kb = (p.K + kElemsPerStage - 1) / kElemsPerStage;
   volatile int* abort_flag = &ctl->abort_flag;
 
   if (threadIdx.x == 0) {
@@ -208,8 +227,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
           if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, &g_gemm_error)) { ok = false; break; }
           const uint32_t fb = smem_u32(&ctl->full[s]);
           mbar_arrive_expect_tx(fb, kStageBytes);
-          tma_load_2d(a_stage(s), &tmap_a, fb, kb * BK, m_idx * BM);
-          tma_load_2d(b_stage(s), &tmap_b, fb, kb * BK, n_idx * BN);
+          tma_load_2d(a_stage(s), &tmap_a, fb, kb * kElemsPerStage, m_idx * BM);
+          tma_load_2d(b_stage(s), &tmap_b, fb, kb * kElemsPerStage, n_idx * BN);
         }
       }
       if (!ok) {
@@ -240,8 +259,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 #pragma unroll
           for (int kk = 0; kk < BK / kMmaK; ++kk) {
             // advance the start address by 32 bytes of K inside the swizzled 128-byte row
-            mma_f8(d_tmem, adesc + uint64_t(kk * kMmaK >> 4), bdesc + uint64_t(kk * kMmaK >> 4), p.idesc,
-                   (kb | kk) != 0 ? 1u : 0u);
+            mma_issue<kBf16>(d_tmem, adesc + uint64_t(kk * kMmaK >> 4), bdesc + uint64_t(kk * kMmaK >> 4),
+                             p.idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           mma_commit(smem_u32(&ctl->empty[s]));  // frees the stage once these MMAs have read it
         }
@@ -257,7 +276,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     const int q = warp & 3;                    // TMEM lane quarter this warp may access
     const int row_in_tile = q * 32 + lane;
     const int et = threadIdx.x - 64;           // 0..127
-    const float s_a = *p.s_a;
+    const float s_a = p.s_a ? *p.s_a : 1.0f;
     uint32_t acc_it = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++acc_it) {
       int m_idx, n_idx;
@@ -363,31 +382,43 @@ EncodeTiledFn get_encode_fn() {
 
 namespace fp8k {
 
-// 2-D FP8 (byte) tensor map: [rows, K] with row stride ld bytes, box [box_rows, 128 bytes], 128B swizzle.
-bool make_fp8_tensor_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t K, int64_t ld, uint32_t box_rows) {
+// 2-D tensor map over a row-major matrix [rows, K] of FP8 bytes or bf16 elements (row stride
+// ld bytes), box [box_rows rows x 128 bytes], 128-byte swizzle, zero fill outside the matrix.
+static bool make_tensor_map(CUtensorMap* map, const void* base, bool bf16, int64_t rows, int64_t K, int64_t ld,
+                            uint32_t box_rows) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
   const cuuint64_t strides[1] = {cuuint64_t(ld)};
-  const cuuint32_t box[2] = {uint32_t(fp8k::gemm::BK), box_rows};
+  const cuuint32_t box[2] = {uint32_t(bf16 ? fp8k::gemm::BK / 2 : fp8k::gemm::BK), box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int gemm_launch(const uint8_t* qa, int64_t ldqa, const float* s_a, const uint8_t* qw, int64_t ldqw,
-                const float* s_w, int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy,
-                int M, int N, int K, int fmt_a, int fmt_w, int num_sms, cudaStream_t stream) {
+bool make_fp8_tensor_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t K, int64_t ld, uint32_t box_rows) {
+  return make_tensor_map(map, base, false, rows, K, ld, box_rows);
+}
+
+namespace {
+
+// Shared launch: operands are FP8 (ld in bytes) or bf16 (ld in bytes as well).
+int launch_gemm(bool bf16, const void* a, int64_t lda_bytes, const float* s_a, const void* w, int64_t ldw_bytes,
+                const float* s_w, int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy, int M, int N,
+                int K, uint32_t idesc, int num_sms, cudaStream_t stream) {
   using namespace gemm;
-  static bool attr_done = false;  // the attribute is per function, set once per process
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes)) != cudaSuccess)
+  auto kernel = bf16 ? gemm_kernel<true> : gemm_kernel<false>;
+  static bool attr_done[2] = {false, false};  // the attribute is per function, set once per process
+  if (!attr_done[bf16]) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes)) != cudaSuccess)
       return 1;
-    attr_done = true;
+    attr_done[bf16] = true;
   }
   CUtensorMap ma, mb;
-  if (!make_fp8_tensor_map(&ma, qa, M, K, ldqa, BM) || !make_fp8_tensor_map(&mb, qw, N, K, ldqw, BN)) return 2;
+  if (!make_tensor_map(&ma, a, bf16, M, K, lda_bytes, BM) || !make_tensor_map(&mb, w, bf16, N, K, ldw_bytes, BN))
+    return 2;
 
   GemmParams p;
   p.M = M;
@@ -405,10 +436,10 @@ int gemm_launch(const uint8_t* qa, int64_t ldqa, const float* s_a, const uint8_t
   // sweeps all rows; qA is then read once per group. Larger hot sets were measured to be
   // evicted by the streaming qA and Y traffic.
   const int64_t slice_budget = int64_t(26) << 20;
-  const int64_t w_tile_bytes = int64_t(BN) * ldqw;
+  const int64_t w_tile_bytes = int64_t(BN) * ldw_bytes;
   p.group_n = int(std::max<int64_t>(1, std::min<int64_t>(p.n_tiles, slice_budget / w_tile_bytes)));
   p.y_vec = (ldy % 8 == 0) && (reinterpret_cast<uintptr_t>(y) % 16 == 0);
-  p.idesc = make_idesc(fmt_a, fmt_w);
+  p.idesc = idesc;
 
   const int tiles = p.m_tiles * p.n_tiles;
   cudaLaunchConfig_t cfg = {};
@@ -421,7 +452,23 @@ int gemm_launch(const uint8_t* qa, int64_t ldqa, const float* s_a, const uint8_t
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel, ma, mb, p) == cudaSuccess ? 0 : 3;
+  return cudaLaunchKernelEx(&cfg, kernel, ma, mb, p) == cudaSuccess ? 0 : 3;
+}
+
+}  // namespace
+
+int gemm_launch(const uint8_t* qa, int64_t ldqa, const float* s_a, const uint8_t* qw, int64_t ldqw,
+                const float* s_w, int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy,
+                int M, int N, int K, int fmt_a, int fmt_w, int num_sms, cudaStream_t stream) {
+  return launch_gemm(false, qa, ldqa, s_a, qw, ldqw, s_w, per_channel, bias, y, ldy, M, N, K,
+                     gemm::make_idesc(fmt_a, fmt_w), num_sms, stream);
+}
+
+int gemm_bf16_launch(const uint16_t* a, int64_t lda, const uint16_t* w, int64_t ldw, const float* s_w,
+                     int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy, int M, int N, int K,
+                     int num_sms, cudaStream_t stream) {
+  return launch_gemm(true, a, lda * 2, nullptr, w, ldw * 2, s_w, per_channel, bias, y, ldy, M, N, K,
+                     gemm::kIdescBf16, num_sms, stream);
 }
 
 unsigned int gemm_read_and_clear_error() {

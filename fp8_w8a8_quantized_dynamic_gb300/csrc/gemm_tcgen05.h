@@ -10,7 +10,7 @@ namespace fp8k {
 
 struct GemmParams {
   int M, N, K;
-  const float* s_a;
+  const float* s_a;  // null: 1 (weight-only product)
   const float* s_w;
   int per_channel;
   const uint16_t* bias;
@@ -27,6 +27,13 @@ struct GemmParams {
 int gemm_launch(const uint8_t* qa, int64_t ldqa, const float* s_a, const uint8_t* qw, int64_t ldqw,
                 const float* s_w, int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy,
                 int M, int N, int K, int fmt_a, int fmt_w, int num_sms, cudaStream_t stream);
+
+// bf16 x bf16 GEMM on the same kernel (tcgen05 kind::f16) for the weight-only product:
+//   Y[m, n] = bf16( s_w[n] * sum_k A[m, k] W[n, k]  (+ bias[n]) ).
+// a, w: bf16, 16-byte aligned, lda / ldw in elements with lda * 2 and ldw * 2 multiples of 16.
+int gemm_bf16_launch(const uint16_t* a, int64_t lda, const uint16_t* w, int64_t ldw, const float* s_w,
+                     int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy, int M, int N, int K,
+                     int num_sms, cudaStream_t stream);
 
 // 2-D FP8 (byte) tensor map over [rows, K] (row stride ld bytes), box [box_rows rows x 128 bytes],
 // 128-byte swizzle, zero fill outside the matrix. False when the encoder is unavailable or fails.

@@ -9,17 +9,28 @@ namespace gemv {
 
 namespace {
 
-template <int NT, bool D>
+template <int NT, int Mode>
 KernelFn pick(int fa, int fw) {
-  if (fa == kFmtE4M3) return fw == kFmtE4M3 ? gemv_kernel<NT, D, kFmtE4M3, kFmtE4M3> : gemv_kernel<NT, D, kFmtE4M3, kFmtE5M2>;
-  return fw == kFmtE4M3 ? gemv_kernel<NT, D, kFmtE5M2, kFmtE4M3> : gemv_kernel<NT, D, kFmtE5M2, kFmtE5M2>;
+  if constexpr (Mode == kModeBf16) {
+    return fw == kFmtE4M3 ? gemv_kernel<NT, Mode, kFmtE4M3, kFmtE4M3> : gemv_kernel<NT, Mode, kFmtE4M3, kFmtE5M2>;
+  } else {
+    if (fa == kFmtE4M3)
+      return fw == kFmtE4M3 ? gemv_kernel<NT, Mode, kFmtE4M3, kFmtE4M3> : gemv_kernel<NT, Mode, kFmtE4M3, kFmtE5M2>;
+    return fw == kFmtE4M3 ? gemv_kernel<NT, Mode, kFmtE5M2, kFmtE4M3> : gemv_kernel<NT, Mode, kFmtE5M2, kFmtE5M2>;
+  }
+}
+
+template <int NT>
+KernelFn pick_mode(int mode, int fa, int fw) {
+  if (mode == kModeQuantize) return pick<NT, kModeQuantize>(fa, fw);
+  if (mode == kModeBf16) return pick<NT, kModeBf16>(fa, fw);
+  return pick<NT, kModePrequant>(fa, fw);
 }
 
 }  // namespace
 
-KernelFn kernel_for(int NT, bool dyn, int fa, int fw) {
-  if (NT == 1) return dyn ? pick<1, true>(fa, fw) : pick<1, false>(fa, fw);
-  return dyn ? pick<2, true>(fa, fw) : pick<2, false>(fa, fw);
+KernelFn kernel_for(int NT, int mode, int fa, int fw) {
+  return NT == 1 ? pick_mode<1>(mode, fa, fw) : pick_mode<2>(mode, fa, fw);
 }
 
 unsigned int read_and_clear_error() {

@@ -41,6 +41,16 @@ namespace gemv {
 // Device error bits of the GEMV (bounded waits that expired), read by fp8_last_device_status.
 __device__ unsigned int g_gemv_error;
 
+// D += W (16 rows x 16 k) * A^T (16 k x 8 tokens), bf16 operands, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // D += W (16 rows x 32 k, format FW) * A^T (32 k x 8 tokens, format FA), fp32 accumulate.
 #define FP8K_MMA_M16N8K32(TW, TA)                                                    \
   asm volatile("mma.sync.aligned.m16n8k32.row.col.f32." TW "." TA ".f32 "          \
@@ -114,10 +124,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y) : "memory");
 }
 
-// NT: n8 token tiles (1: M <= 8, 2: M <= 16). kDynamic: A is bf16 and quantized here
-// (dynamic scale, or the static one when p.s_static is set). FA / FW: FP8 formats of the
+// NT: n8 token tiles (1: M <= 8, 2: M <= 16). kMode: kModeQuantize (A is bf16 and quantized
+// here, dynamic scale or the static one when p.s_static is set), kModePrequant (qA and s_a
+// given) or kModeBf16 (weight-only: A stays bf16, each weight tile is up-converted to bf16 in
+// registers and multiplied with bf16 MMAs; s_a is 1). FA / FW: FP8 formats of the
 // activations and the weights.
-template <int NT, bool kDynamic, int FA, int FW>
+template <int NT, int kMode, int FA, int FW>
 __global__ void __launch_bounds__(kThreads, 1)
 gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ Params p) {
   unsigned int* err = &g_gemv_error;
@@ -186,7 +198,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     pdl_wait();  // A (or qA and s_a) may come from the preceding kernel
     const int span = ntiles * kTileK;  // bytes of K staged per token (zero beyond K)
     float s_a;
-    if constexpr (kDynamic) {
+    if constexpr (kMode == kModeQuantize) {
       // max |A| over this rank's slice (dynamic scale); the first kRegUnits units per thread
       // stay in registers for the quantization below
       const int upt = span >> 3;  // 8-element units per token
@@ -266,6 +278,34 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
         const int kk = (i - (i / zu) * zu) << 4;
         asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" :: "r"(act + m * p.act_stride + kk), "r"(0u) : "memory");
       }
+    } else if constexpr (kMode == kModeBf16) {
+      cluster_arrive();  // phase 1 is unused here but keeps every thread's phases aligned
+      cluster_wait();
+      s_a = 1.0f;
+      // bf16 activation slice [16 tokens][span] -> smem (2 bytes an element), zero beyond M and K;
+      // kRegUnits independent 16-byte loads per thread in flight at a time
+      const int upt = span >> 3;  // 8-element units per token
+      const int units = kMaxTokens * upt;
+      for (int i0 = threadIdx.x; i0 < units; i0 += kRegUnits * kConsumerThreads) {
+        uint4 v[kRegUnits];
+#pragma unroll
+        for (int b = 0; b < kRegUnits; ++b) {
+          const int i = i0 + b * kConsumerThreads;
+          const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
+          v[b] = (i < units && m < p.M) ? load8_bf16(p.a + (int64_t)m * p.lda, k0 + kk, p.K, p.vec_a)
+                                        : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int b = 0; b < kRegUnits; ++b) {
+          const int i = i0 + b * kConsumerThreads;
+          if (i < units) {
+            const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};"
+                         :: "r"(act + m * p.act_stride + 2 * kk), "r"(v[b].x), "r"(v[b].y), "r"(v[b].z),
+                            "r"(v[b].w) : "memory");
+          }
+        }
+      }
     } else {
       cluster_arrive();  // phase 1 is unused here but keeps every thread's phases aligned
       cluster_wait();
@@ -288,7 +328,8 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
 
     const int g = lane >> 2, t = lane & 3;
     const uint32_t row_lo = (warp * 16 + g) * kTileK, row_hi = row_lo + 8 * kTileK;
-    const uint32_t act_lane = act + g * p.act_stride + 16 * t;
+    // this lane's activation fragment: token g, the 16 K of unit (4j + t) of each half-row j
+    const uint32_t act_lane = act + g * p.act_stride + (kMode == kModeBf16 ? 32 : 16) * t;
     uint32_t it = 0;
     for (int r = 0; r < rb_count; ++r) {
       float acc[NT][4];
@@ -306,11 +347,35 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
             const uint32_t unit = uint32_t(((4 * j + t) ^ g) * 16);
             const uint4 wlo = lds_v4(tile + row_lo + unit);
             const uint4 whi = lds_v4(tile + row_hi + unit);
+            if constexpr (kMode == kModeBf16) {
+              // 4-byte group i of the unit feeds one k16 MMA: bytes (4i, 4i+1) are its K pair
+              // (2t, 2t+1) and bytes (4i+2, 4i+3) its pair (2t+8, 2t+9); the activations use the
+              // same order, 8 consecutive bytes of bf16 per MMA
+              const uint32_t wl[4] = {wlo.x, wlo.y, wlo.z, wlo.w}, wh[4] = {whi.x, whi.y, whi.z, whi.w};
+              uint32_t fa[4][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              const uint4 b = lds_v4(act_lane + nt * 8 * p.act_stride + kt * kTileK + 64 * j);
-              mma_fp8<FW, FA>(acc[nt], wlo.x, whi.x, wlo.y, whi.y, b.x, b.y);
-              mma_fp8<FW, FA>(acc[nt], wlo.z, whi.z, wlo.w, whi.w, b.z, b.w);
+              for (int i = 0; i < 4; ++i) {
+                fa[i][0] = fp8x2_to_bf16x2<FW>(wl[i]);
+                fa[i][1] = fp8x2_to_bf16x2<FW>(wh[i]);
+                fa[i][2] = fp8x2_to_bf16x2<FW>(wl[i] >> 16);
+                fa[i][3] = fp8x2_to_bf16x2<FW>(wh[i] >> 16);
+              }
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                const uint32_t boff = act_lane + nt * 8 * p.act_stride + 2 * (kt * kTileK + 64 * j);
+                const uint4 b0 = lds_v4(boff), b1 = lds_v4(boff + 16);
+                mma_bf16(acc[nt], fa[0][0], fa[0][1], fa[0][2], fa[0][3], b0.x, b0.y);
+                mma_bf16(acc[nt], fa[1][0], fa[1][1], fa[1][2], fa[1][3], b0.z, b0.w);
+                mma_bf16(acc[nt], fa[2][0], fa[2][1], fa[2][2], fa[2][3], b1.x, b1.y);
+                mma_bf16(acc[nt], fa[3][0], fa[3][1], fa[3][2], fa[3][3], b1.z, b1.w);
+              }
+            } else {
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                const uint4 b = lds_v4(act_lane + nt * 8 * p.act_stride + kt * kTileK + 64 * j);
+                mma_fp8<FW, FA>(acc[nt], wlo.x, whi.x, wlo.y, whi.y, b.x, b.y);
+                mma_fp8<FW, FA>(acc[nt], wlo.z, whi.z, wlo.w, whi.w, b.z, b.w);
+              }
             }
           }
         }

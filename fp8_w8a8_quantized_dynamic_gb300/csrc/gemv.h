@@ -24,6 +24,12 @@ constexpr int kPartBytes = kRows * kMaxTokens * 4;    // 8 KB per row block
 constexpr int kMaxSlice = 4096;                       // bytes of K per rank
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kRegUnits = 8;  // 8-element units of A a consumer thread keeps in registers
+constexpr int kMaxSliceBf16 = 2048;                   // bytes of K per rank with bf16 activations
+
+// Activation modes of the kernel.
+constexpr int kModePrequant = 0;  // qA and s_a given (fp8_scaled_mm)
+constexpr int kModeQuantize = 1;  // bf16 A quantized in the kernel (dynamic or static scale)
+constexpr int kModeBf16 = 2;      // bf16 A used as is: weight-only product, W up-converted to bf16
 
 struct Params {
   const uint8_t* qa;   // pre-quantized: FP8 [M, ldqa], bytes [K, ldqa) zero
@@ -40,7 +46,8 @@ struct Params {
   int64_t ldy;
   int M, N, K;
   int kslice;          // bytes of K per rank, multiple of kTileK
-  int act_stride;      // smem row stride of the activation slice (== 64 mod 128)
+  int act_stride;      // smem row stride (bytes) of the activation slice: == 64 mod 128 for FP8
+                       // activations, == 16 mod 128 for bf16 (conflict-free fragment loads)
   int stages;          // ring depth
   int row_blocks;      // ceil(N / kRows)
   int num_clusters;    // C
@@ -61,10 +68,10 @@ __host__ __device__ inline Layout layout(int stages, int act_stride, int rb_per_
   return L;
 }
 
-// One instantiation of the kernel: NT n8 token tiles (1: M <= 8, 2: M <= 16), A quantized in
-// the kernel (dyn) or pre-quantized, FP8 formats of the activations (fa) and weights (fw).
+// One instantiation of the kernel: NT n8 token tiles (1: M <= 8, 2: M <= 16), activation
+// mode (kMode*), FP8 formats of the activations (fa, unused for kModeBf16) and weights (fw).
 using KernelFn = void (*)(CUtensorMap, Params);
-KernelFn kernel_for(int NT, bool dyn, int fa, int fw);
+KernelFn kernel_for(int NT, int mode, int fa, int fw);
 
 // Device-side error bits of the GEMV on the current device (read, then cleared).
 unsigned int read_and_clear_error();

@@ -170,6 +170,49 @@ quantize_rows_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t K, int64
   }
 }
 
+// Weight-only up-conversion ("Prototype FP8Linear W8A8 runtime quantization": without FP8
+// tensor cores the FP8 weights are up-converted to the original dtype): wb[n, k] =
+// bf16(decode(qw[n, k])) for k < K, exact; the weight scale is applied by the GEMM epilogue.
+// Columns [K, ldwb) of wb are written as zero. ldwb: multiple of 8 elements.
+template <int F>
+__global__ void __launch_bounds__(kQuantThreads)
+upconvert_kernel(const uint8_t* __restrict__ qw, int64_t N, int64_t K, int64_t ldqw, uint16_t* __restrict__ wb,
+                 int64_t ldwb) {
+  pdl_trigger();  // the GEMM that follows waits for this kernel before reading wb
+  pdl_wait();     // wb may still be read by the previous call's GEMM
+  const int64_t upr = ldwb >> 3;  // 8-element (16-byte output) units per row
+  const int64_t units = N * upr;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = u / upr;
+    const int64_t c = (u - r * upr) << 3;
+    uint2 codes = make_uint2(0, 0);
+    if (c < K) codes = *reinterpret_cast<const uint2*>(qw + r * ldqw + c);  // ldqw % 16 == 0, c % 8 == 0
+    // bytes [K, ldqw) of a quantized row are zero, which up-converts to +0 as required
+    uint4 out;
+    out.x = fp8x2_to_bf16x2<F>(codes.x);
+    out.y = fp8x2_to_bf16x2<F>(codes.x >> 16);
+    out.z = fp8x2_to_bf16x2<F>(codes.y);
+    out.w = fp8x2_to_bf16x2<F>(codes.y >> 16);
+    *reinterpret_cast<uint4*>(wb + r * ldwb + c) = out;
+  }
+}
+
+// Copy of bf16 A [rows, cols] (any stride) into a 16-byte-aligned buffer with stride ldo
+// (a multiple of 8 elements), zero in columns [cols, ldo): the layout TMA needs.
+__global__ void __launch_bounds__(kQuantThreads)
+copy_rows_bf16_kernel(const uint16_t* __restrict__ a, int64_t rows, int64_t cols, int64_t ld, int vec,
+                      uint16_t* __restrict__ out, int64_t ldo, int pdl) {
+  if (pdl) pdl_trigger();
+  pdl_wait();
+  const int64_t upr = ldo >> 3;
+  const int64_t units = rows * upr;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = u / upr;
+    const int c = int((u - r * upr) << 3);
+    *reinterpret_cast<uint4*>(out + r * ldo + c) = load8_bf16(a + r * ld, c, int(cols), vec);
+  }
+}
+
 // Y[m, :] = bias (or 0) for all m: the K == 0 product.
 __global__ void fill_bias_kernel(const uint16_t* __restrict__ bias, uint16_t* __restrict__ y,
                                  int64_t M, int64_t N, int64_t ldy, int pdl) {

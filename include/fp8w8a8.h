@@ -249,6 +249,36 @@ fp8_status fp8_linear_ex(const void* a_bf16, int64_t M, int64_t K, int64_t lda, 
                          void* y_bf16, int64_t ldy, void* ws, size_t ws_bytes, fp8_stream_t stream);
 
 /*
+ * ---------------------------------------------------------------------------
+ * Weight-only FP8: the FP8 weights are kept for memory and up-converted to the
+ * original dtype for the product ("Prototype FP8Linear W8A8 runtime
+ * quantization": the path below compute capability 9.0, where weights are
+ * dequantized into higher precision with no compute savings). A stays bf16:
+ *   Y[m, n] = bf16( s_w[n or 0] * sum_k A[m, k] * decode(qW[n, k]) (+ bias[n]) ).
+ * Every e4m3 / e5m2 value is a bf16 value, so the up-conversion is exact; the
+ * weight scale multiplies the fp32 accumulator in the epilogue, as in the
+ * channelwise identity (s_w,n W_n) A = s_w,n (W_n A).
+ * Decode shapes (M <= 16, K <= 16384) run the split-K GEMV, which up-converts
+ * each weight tile in registers and needs no workspace; larger shapes
+ * up-convert W into the workspace once per call and run a bf16 tcgen05 GEMM.
+ * ---------------------------------------------------------------------------
+ */
+
+/* Workspace fp8_linear_weight_only needs: 0 for decode shapes; otherwise the
+ * up-converted weights (N * round_up(K, 8) bf16, rounded up to 256 bytes) plus
+ * M * round_up(K, 8) bf16 for an aligned copy of A, used only when A's row
+ * stride or base address is not a multiple of 16 bytes. Host-only. */
+size_t fp8_weight_only_workspace_bytes(int64_t M, int64_t K, int64_t N);
+
+/* qw, s_w from fp8_quantize_weight(_ex) with format fmt_w; per_channel as
+ * there; other arguments and rules as for fp8_linear. */
+fp8_status fp8_linear_weight_only(const void* a_bf16, int64_t M, int64_t K, int64_t lda,
+                                  const uint8_t* qw, fp8_format fmt_w, int64_t N, int64_t ldqw,
+                                  const float* s_w, int per_channel, const void* bias_bf16,
+                                  void* y_bf16, int64_t ldy, void* ws, size_t ws_bytes,
+                                  fp8_stream_t stream);
+
+/*
  * Synchronizes `stream`, then reports and clears device-side errors recorded
  * by the library's kernels on the current device since the last query
  * (FP8_ERR_TIMEOUT when a bounded wait expired), or FP8_ERR_CUDA when the

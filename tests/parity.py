@@ -90,3 +90,23 @@ def assert_guards_intact(buf: torch.Tensor, base: int, row_bytes: int, used: int
     for r in range(rows):
         mask[base + r * row_bytes: base + r * row_bytes + used] = False
     assert np.all(b[mask] == fill), "write outside the output region"
+
+
+def weight_only_parity(y: torch.Tensor, a: torch.Tensor, w: torch.Tensor, per_channel: bool,
+                       bias: Optional[torch.Tensor] = None, rows: Optional[Sequence[int]] = None,
+                       cols: Optional[Sequence[int]] = None, what: str = "Y", fmt_w: str = "e4m3") -> float:
+    """Weight-only linear against the oracle (bf16 A, FP8 W quantized by the oracle) on rows x cols."""
+    rows = np.arange(a.shape[0]) if rows is None else np.asarray(rows)
+    cols = np.arange(w.shape[0]) if cols is None else np.asarray(cols)
+    a_sel = f32(a)[rows]
+    qw, s_w = oracle_weight(w, per_channel, cols, fmt_w)
+    b = None if bias is None else f32(bias)[cols]
+    y_ref = O.linear_weight_only(a_sel, qw, s_w, b, fmt_w)
+    tol = O.tolerance_weight_only(a_sel, qw, s_w, y_ref, fmt_w)
+    y_gpu = f32(y)[np.ix_(rows, cols)]
+    err = np.abs(y_gpu.astype(np.float64) - y_ref.astype(np.float64))
+    bad = np.argwhere(~(err <= tol))
+    assert bad.size == 0, (f"{what}: {len(bad)} of {err.size} outputs outside tolerance; first "
+                           f"{bad[:3].tolist()} got {y_gpu[tuple(bad[:3].T)]} want {y_ref[tuple(bad[:3].T)]} "
+                           f"tol {tol[tuple(bad[:3].T)]}")
+    return float(np.max(err / tol)) if err.size else 0.0
