@@ -71,6 +71,17 @@ int gemv_max_m() {
 
 bool use_gemv(int64_t M, int64_t K) { return M <= gemv_max_m() && K <= kGemvMaxK; }
 
+// Weight tiles the GEMV issues before its activation loads have landed (FP8W8A8_GEMV_HEAD
+// overrides the default of 4; 0 holds the whole stream, gemv::kMaxStages lets it run free).
+int gemv_head_tiles() {
+  static const int v = [] {
+    const char* e = std::getenv("FP8W8A8_GEMV_HEAD");
+    const int x = e ? std::atoi(e) : 4;
+    return std::max(0, std::min(x, 1 << 20));
+  }();
+  return v;
+}
+
 int64_t round_up16(int64_t k) { return (k + 15) / 16 * 16; }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -246,25 +257,29 @@ fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uin
   using namespace gemv;
   const int R = (p.N + kRows - 1) / kRows;
   const int KT = (p.K + kTileK - 1) / kTileK;
-  int best_cost = -1, bS = 1, bC = 1, bstages = kMaxStages, bslice = kTileK;
-  size_t bsmem = 0;
+  const bool dyn = mode == kModeQuantize;
+  const int max_slice = mode == kModeBf16 ? kMaxSliceBf16 : kMaxSlice;
   const int NT = p.M <= 8 ? 1 : 2;
-  const bool dyn = mode == gemv::kModeQuantize;
-  const int max_slice = mode == gemv::kModeBf16 ? kMaxSliceBf16 : kMaxSlice;
+  const int act_rows = 8 * NT;
   const KernelFn kfn = kernel_for(NT, mode, fmt_a, fmt_w);
   const int smem_limit = gemv_smem_limit(kfn);
-  for (int S : {1, 2, 4, 8}) {
+  auto smem_for = [&](int stg, int act_stride, int nrb) {
+    return size_t(layout(stg, act_stride, act_rows, nrb).total) + 1024;
+  };
+  int best_cost = -1, bS = 1, bC = 1, bstages = kMinStages, bslice = kTileK;
+  size_t bsmem = 0;
+  for (int S = 1; S <= kMaxCluster; ++S) {
     if (S > KT) break;
     const int slice_tiles = (KT + S - 1) / S;
     if ((KT + slice_tiles - 1) / slice_tiles != S) continue;  // every rank must own tiles
     const int kslice = slice_tiles * kTileK;
     if (kslice > max_slice) continue;
     const int act_stride = gemv_act_stride(mode, kslice);
+    // deepest ring that fits with room for the most row blocks a cluster may own
     int stages = kMaxStages;
-    auto smem_for = [&](int stg, int nrb) { return size_t(layout(stg, act_stride, nrb).total) + 1024; };
-    while (stages > kMinStages && smem_for(stages, kMaxRowBlocks) > size_t(smem_limit)) --stages;
-    if (smem_for(stages, kMaxRowBlocks) > size_t(smem_limit)) continue;
-    const int cmax = gemv_max_clusters(kfn, S, smem_for(stages, kMaxRowBlocks));
+    while (stages > kMinStages && smem_for(stages, act_stride, kMaxRowBlocks) > size_t(smem_limit)) --stages;
+    if (smem_for(stages, act_stride, kMaxRowBlocks) > size_t(smem_limit)) continue;
+    const int cmax = gemv_max_clusters(kfn, S, smem_for(stages, act_stride, kMaxRowBlocks));
     if (cmax <= 0) continue;
     int C = std::min(cmax, R);
     const int nrb = (R + C - 1) / C;
@@ -276,12 +291,15 @@ fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uin
     const int batches = dyn ? (units + kRegUnits * kConsumerThreads - 1) / (kRegUnits * kConsumerThreads) : 0;
     const int cost = nrb * slice_tiles + 2 * (batches > 1 ? batches : 0);
     if (best_cost < 0 || cost < best_cost) {
+      // with the row blocks known, deepen the ring into the smem they leave free
+      int stg = stages;
+      while (stg < kMaxStages && smem_for(stg + 1, act_stride, nrb) <= size_t(smem_limit)) ++stg;
       best_cost = cost;
       bS = S;
       bC = C;
-      bstages = stages;
+      bstages = stg;
       bslice = kslice;
-      bsmem = smem_for(stages, nrb);
+      bsmem = smem_for(stg, act_stride, nrb);
     }
   }
   if (best_cost < 0) {
@@ -290,9 +308,39 @@ fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uin
   }
   p.kslice = bslice;
   p.act_stride = gemv_act_stride(mode, bslice);
+  p.act_rows = act_rows;
+  p.head_tiles = gemv_head_tiles();
+  // dynamic scale: every CTA reads all of A when that is at most two load batches per thread
+  // (no cluster exchange on the critical path); larger A exchanges the ranks' slice maxima
+  const int64_t units_all = int64_t(p.M) * ((p.K + 7) / 8);
+  p.cluster_amax = (bS > 1 && units_all > 2 * kRegUnits * kConsumerThreads) ? 1 : 0;
+  if (bS == 1) p.cluster_amax = 1;  // one rank: its slice is all of A
+  // quantize mode with row-aligned A: bulk-copy A (all of it for the dynamic maximum when it
+  // fits, else this rank's slice) into the ring stages that stay idle until the stream is
+  // released, so the prologue reads it from shared memory with no per-thread round trips
+  p.scratch_a = 0;
+  if (mode == kModeQuantize && p.vec_a && p.K % 8 == 0) {
+    const int64_t free_bytes = p.head_tiles < bstages ? int64_t(bstages - p.head_tiles) * kTileBytes : 0;
+    const int64_t full_bytes = int64_t(p.M) * p.K * 2;
+    const int64_t slice_bytes = int64_t(p.M) * bslice * 2;
+    if (p.s_static != nullptr) {
+      if (slice_bytes <= free_bytes) p.scratch_a = 2;
+    } else if (full_bytes <= free_bytes) {
+      p.scratch_a = 1;
+      p.cluster_amax = 0;
+    } else if (slice_bytes <= free_bytes) {
+      p.scratch_a = 2;
+      p.cluster_amax = 1;
+    }
+  }
   p.stages = bstages;
   p.row_blocks = R;
   p.num_clusters = bC;
+  static const bool debug = std::getenv("FP8W8A8_DEBUG") != nullptr;
+  if (debug)
+    std::fprintf(stderr, "fp8w8a8: gemv M=%d N=%d K=%d mode=%d cluster=%d clusters=%d stages=%d kslice=%d smem=%zu "
+                 "scratch=%d cluster_amax=%d\n", p.M, p.N, p.K, mode, bS, bC, bstages, bslice, bsmem, p.scratch_a,
+                 p.cluster_amax);
   CUtensorMap map;
   if (!make_fp8_tensor_map(&map, qw, p.N, p.K, ldqw, kRows)) return FP8_ERR_CUDA;
   return launch(kfn, dim3(bC * bS), dim3(kThreads), bsmem, st, true, dim3(bS, 1, 1), map, p);

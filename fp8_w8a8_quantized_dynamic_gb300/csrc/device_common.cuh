@@ -126,6 +126,14 @@ __device__ __forceinline__ uint32_t abs_max_u16x2(uint32_t acc, uint32_t w) {
   return __vmaxu2(acc, w & 0x7FFF7FFFu);
 }
 
+// max |x| over eight bf16 values (a uint4), folded into two 16-bit magnitudes.
+__device__ __forceinline__ uint32_t abs_max_v4(uint32_t m2, uint4 v) {
+  m2 = abs_max_u16x2(m2, v.x);
+  m2 = abs_max_u16x2(m2, v.y);
+  m2 = abs_max_u16x2(m2, v.z);
+  return abs_max_u16x2(m2, v.w);
+}
+
 __device__ __forceinline__ float u16x2_max_to_float(uint32_t m2) {
   const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
   return __uint_as_float(m << 16);

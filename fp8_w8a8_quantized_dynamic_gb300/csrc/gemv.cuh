@@ -74,12 +74,9 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
   return v;
 }
 
-__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t local_addr, uint32_t rank) {
-  uint32_t remote;
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
   float4 v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote) : "memory");
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
   return v;
 }
 
@@ -101,6 +98,12 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
   return r;
 }
 
+__device__ __forceinline__ void st_dsmem_v2(uint32_t local_addr, uint32_t rank, float a, float b) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1,%2};" :: "r"(remote), "f"(a), "f"(b) : "memory");
+}
+
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
   uint32_t remote;
   float v;
@@ -112,10 +115,18 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank
 // Split-phase cluster barrier: every thread of every CTA arrives once per phase and waits
 // before arriving again.
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+// Arrival that publishes nothing (no release fence): only says "this thread is running".
+__device__ __forceinline__ void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
 __device__ __forceinline__ void consumer_bar_sync() {
   asm volatile("bar.sync 1, %0;" :: "n"(kConsumerThreads) : "memory");
+}
+
+// Contiguous global -> shared copy of `bytes` (16-byte aligned ends), completing on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
@@ -124,11 +135,38 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y) : "memory");
 }
 
+// Loads the 8-element units [i0 + b * kConsumerThreads, b < kRegUnits) of a [rows][upt units]
+// bf16 slice starting at column k0 (zero past `units`, past row M and past K) into v.
+__device__ __forceinline__ void load_units(uint4 (&v)[kRegUnits], const Params& p, int i0, int units, int upt,
+                                           int k0) {
+#pragma unroll
+  for (int b = 0; b < kRegUnits; ++b) {
+    const int i = i0 + b * kConsumerThreads;
+    const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
+    v[b] = (i < units && m < p.M) ? load8_bf16(p.a + (int64_t)m * p.lda, k0 + kk, p.K, p.vec_a)
+                                  : make_uint4(0, 0, 0, 0);
+  }
+}
+
+__device__ __forceinline__ uint32_t abs_max_units(uint32_t m2, const uint4 (&v)[kRegUnits]) {
+#pragma unroll
+  for (int b = 0; b < kRegUnits; ++b)
+    m2 = abs_max_u16x2(abs_max_u16x2(abs_max_u16x2(abs_max_u16x2(m2, v[b].x), v[b].y), v[b].z), v[b].w);
+  return m2;
+}
+
 // NT: n8 token tiles (1: M <= 8, 2: M <= 16). kMode: kModeQuantize (A is bf16 and quantized
 // here, dynamic scale or the static one when p.s_static is set), kModePrequant (qA and s_a
 // given) or kModeBf16 (weight-only: A stays bf16, each weight tile is up-converted to bf16 in
 // registers and multiplied with bf16 MMAs; s_a is 1). FA / FW: FP8 formats of the
 // activations and the weights.
+//
+// Start-up order. The producer issues its first p.head_tiles weight tiles at once (they
+// never depend on the preceding kernel), then holds the stream until every consumer warp
+// has all of its activation loads back: while the weight stream saturates HBM, each
+// dependent activation round trip takes several times longer. The dynamic amax is the maximum
+// over all of A computed by every CTA (p.cluster_amax == 0, small M*K), or each rank's slice
+// maximum exchanged over the cluster through distributed shared memory.
 template <int NT, int kMode, int FA, int FW>
 __global__ void __launch_bounds__(kThreads, 1)
 gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ Params p) {
@@ -141,28 +179,35 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
   const uint32_t rank = cluster_ctarank(), nrank = cluster_nctarank();
   const int cluster = blockIdx.x / nrank;
   const int rb_count = (p.row_blocks - cluster + p.num_clusters - 1) / p.num_clusters;  // row blocks of this cluster
-  const Layout L = layout(p.stages, p.act_stride, rb_count);
+  const Layout L = layout(p.stages, p.act_stride, p.act_rows, rb_count);
   const uint32_t ring = base + L.ring, act = base + L.act, part = base + L.part;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
+  const uint32_t aready = smem_u32(bars + 2 * kMaxStages);
+  const uint32_t abar = smem_u32(bars + 2 * kMaxStages + 1);  // bulk copy of A landed
 
+  const int rows_per = (kRows + nrank - 1) / nrank;  // rows of a row block each rank reduces
   const int k0 = int(rank) * p.kslice;
   const int kspan = max(0, min(p.kslice, p.K - k0));
   const int ntiles = (kspan + kTileK - 1) / kTileK;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool cluster_amax = kMode == kModeQuantize && p.s_static == nullptr && p.cluster_amax;
 
   __shared__ int abort_flag;
   __shared__ float s_a_out;
   __shared__ float slice_amax;
   __shared__ float red[kConsumerWarps];
+  if (warp == kConsumerWarps && lane == 0)  // fetch the descriptor while the barriers are set up
+    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, kConsumerWarps);
     }
+    mbar_init(aready, kConsumerWarps);
+    mbar_init(abar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
   pdl_trigger();
@@ -170,14 +215,17 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
 
   if (warp == kConsumerWarps) {
     // ---------------- producer: weights never depend on the preceding kernel ----------------
-    cluster_arrive();  // phase 1 (the amax exchange) never waits for the weight stream
+    cluster_arrive_relaxed();  // phase 1 (start / amax exchange) never waits for the weight stream
     if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
       uint32_t it = 0;
-      bool ok = true;
+      bool ok = true, held = false;
       for (int r = 0; r < rb_count && ok; ++r) {
         const int rb = cluster + r * p.num_clusters;
         for (int kt = 0; kt < ntiles; ++kt, ++it) {
+          if (!held && it == uint32_t(p.head_tiles)) {
+            held = true;
+            if (!mbar_wait_bounded(aready, 0, ab, err)) { ok = false; break; }
+          }
           const int s = it % p.stages;
           const uint32_t ph = (it / p.stages) & 1u;
           if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1u, ab, err)) { ok = false; break; }
@@ -195,106 +243,153 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     cluster_wait();
   } else {
     // ---------------- consumers ----------------
+    // phase 1 of the cluster barrier: the amax exchange (cluster_amax), otherwise only the
+    // proof that every CTA of the cluster runs before partials are pushed into its memory
+    if (!cluster_amax) cluster_arrive_relaxed();
     pdl_wait();  // A (or qA and s_a) may come from the preceding kernel
     const int span = ntiles * kTileK;  // bytes of K staged per token (zero beyond K)
+    // every warp reports once that its activation loads are back, which releases the stream
+    auto loads_back = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(aready);
+    };
     float s_a;
     if constexpr (kMode == kModeQuantize) {
-      // max |A| over this rank's slice (dynamic scale); the first kRegUnits units per thread
-      // stay in registers for the quantization below
-      const int upt = span >> 3;  // 8-element units per token
-      const int units = p.M * upt;
-      uint4 v[kRegUnits];
-      uint32_t m2 = 0;
-#pragma unroll
-      for (int b = 0; b < kRegUnits; ++b) {
-        const int i = threadIdx.x + b * kConsumerThreads;
-        const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
-        v[b] = i < units ? load8_bf16(p.a + (int64_t)m * p.lda, k0 + kk, p.K, p.vec_a) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int b = 0; b < kRegUnits; ++b)
-        m2 = abs_max_u16x2(abs_max_u16x2(abs_max_u16x2(abs_max_u16x2(m2, v[b].x), v[b].y), v[b].z), v[b].w);
-      if (p.s_static == nullptr) {  // dynamic scale: the rest of the slice, for the maximum only
-        for (int i0 = threadIdx.x + kRegUnits * kConsumerThreads; i0 < units; i0 += kRegUnits * kConsumerThreads) {
-          uint4 w[kRegUnits];
-#pragma unroll
-          for (int b = 0; b < kRegUnits; ++b) {
-            const int i = i0 + b * kConsumerThreads;
-            const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
-            w[b] = i < units ? load8_bf16(p.a + (int64_t)m * p.lda, k0 + kk, p.K, p.vec_a) : make_uint4(0, 0, 0, 0);
-          }
-#pragma unroll
-          for (int b = 0; b < kRegUnits; ++b)
-            m2 = abs_max_u16x2(abs_max_u16x2(abs_max_u16x2(abs_max_u16x2(m2, w[b].x), w[b].y), w[b].z), w[b].w);
-        }
-        float mx = warp_max(u16x2_max_to_float(m2));
-        if (lane == 0) red[warp] = mx;
-        consumer_bar_sync();
+      if (p.scratch_a != 0) {
+        // A (all of it, or this rank's slice) arrives by bulk copies, one per token row, in ring
+        // stages the producer will not fill before aready; max and quantization read it there
+        const bool full = p.scratch_a == 1;
+        const int rowlen = full ? p.K : kspan;  // elements per copied row (a multiple of 8)
+        const int col0 = full ? 0 : k0;
+        const uint32_t scratch = ring + p.head_tiles * kTileBytes;
         if (threadIdx.x == 0) {
-          for (int w = 1; w < kConsumerWarps; ++w) mx = fmaxf(mx, red[w]);
-          slice_amax = mx;
+          mbar_arrive_expect_tx(abar, uint32_t(p.M) * uint32_t(rowlen) * 2u);
+          for (int m = 0; m < p.M; ++m)
+            bulk_load(scratch + uint32_t(m * rowlen) * 2u, p.a + (int64_t)m * p.lda + col0, uint32_t(rowlen) * 2u, abar);
         }
-        consumer_bar_sync();
-      }
-      cluster_arrive();  // phase 1: publish this rank's slice maximum
-      cluster_wait();
-      if (p.s_static == nullptr) {
-        float amax = 0.0f;
-        for (uint32_t src = 0; src < nrank; ++src) amax = fmaxf(amax, ld_dsmem_f32(smem_u32(&slice_amax), src));
-        s_a = scale_from_amax<FA>(amax);
-      } else {
-        s_a = *p.s_static;
-      }
-      const Quantizer qz = make_quantizer(s_a);
-      // quantize into act[token][k - k0]; units past K and tokens past M are plain zeros
-      auto put = [&](int i, const uint4& x) {
-        const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
-        uint2 q = make_uint2(0, 0);
-        if (k0 + kk < p.K) q = quant8_bf16<FA>(x, qz);
-        asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(act + m * p.act_stride + kk), "r"(q.x), "r"(q.y)
-                     : "memory");
-      };
+        mbar_wait_bounded(abar, 0, ab, err);
+        const int ru = rowlen >> 3;  // 16-byte units per copied row
+        if (p.s_static != nullptr) {
+          s_a = *p.s_static;
+        } else {
+          uint32_t m2 = 0;
+          for (int i = threadIdx.x; i < p.M * ru; i += kConsumerThreads)
+            m2 = abs_max_v4(m2, lds_v4(scratch + uint32_t(i) * 16u));
+          float mx = warp_max(u16x2_max_to_float(m2));
+          if (lane == 0) red[warp] = mx;
+          consumer_bar_sync();
+          if (threadIdx.x == 0) {
+            for (int w = 1; w < kConsumerWarps; ++w) mx = fmaxf(mx, red[w]);
+            slice_amax = mx;
+          }
+          consumer_bar_sync();
+          float amax = slice_amax;
+          if (cluster_amax) {
+            cluster_arrive();  // phase 1: publish this rank's slice maximum
+            cluster_wait();
+            float part_max[kMaxCluster];
 #pragma unroll
-      for (int b = 0; b < kRegUnits; ++b) {
-        const int i = threadIdx.x + b * kConsumerThreads;
-        if (i < units) put(i, v[b]);
-      }
-      // units beyond the register batch: reload kRegUnits at a time (independent loads)
-      for (int i0 = threadIdx.x + kRegUnits * kConsumerThreads; i0 < units; i0 += kRegUnits * kConsumerThreads) {
-        uint4 w[kRegUnits];
+            for (int src = 0; src < kMaxCluster; ++src)
+              part_max[src] = src < int(nrank) ? ld_dsmem_f32(smem_u32(&slice_amax), src) : 0.0f;
+#pragma unroll
+            for (int src = 0; src < kMaxCluster; ++src) amax = fmaxf(amax, part_max[src]);
+          }
+          s_a = scale_from_amax<FA>(amax);
+        }
+        const Quantizer qz = make_quantizer(s_a);
+        const int upt = span >> 3;  // 8-element units per token of this rank's slice
+        for (int i = threadIdx.x; i < p.M * upt; i += kConsumerThreads) {
+          const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
+          uint2 q = make_uint2(0, 0);
+          if (k0 + kk < p.K)
+            q = quant8_bf16<FA>(lds_v4(scratch + uint32_t(m * rowlen + (full ? k0 : 0) + kk) * 2u), qz);
+          asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(act + m * p.act_stride + kk), "r"(q.x), "r"(q.y)
+                       : "memory");
+        }
+      } else {
+        const int upt = span >> 3;  // 8-element units per token of this rank's slice
+        const int units = p.M * upt;
+        uint4 v[kRegUnits];  // the first kRegUnits units per thread stay in registers
+        load_units(v, p, threadIdx.x, units, upt, k0);
+        if (p.s_static != nullptr) {
+          s_a = *p.s_static;
+        } else {
+          uint32_t m2 = abs_max_units(0u, v);
+          if (!cluster_amax) {
+            // the maximum over all of A, read by every CTA (small M * K)
+            const int upt_all = (p.K + 7) >> 3;
+            const int units_all = p.M * upt_all;
+            for (int i0 = threadIdx.x; i0 < units_all; i0 += kRegUnits * kConsumerThreads) {
+              uint4 w[kRegUnits];
+              load_units(w, p, i0, units_all, upt_all, 0);
+              m2 = abs_max_units(m2, w);
+            }
+          } else {
+            for (int i0 = threadIdx.x + kRegUnits * kConsumerThreads; i0 < units; i0 += kRegUnits * kConsumerThreads) {
+              uint4 w[kRegUnits];
+              load_units(w, p, i0, units, upt, k0);
+              m2 = abs_max_units(m2, w);
+            }
+          }
+          float mx = warp_max(u16x2_max_to_float(m2));
+          if (lane == 0) red[warp] = mx;
+          consumer_bar_sync();
+          if (threadIdx.x == 0) {
+            for (int w = 1; w < kConsumerWarps; ++w) mx = fmaxf(mx, red[w]);
+            slice_amax = mx;
+          }
+          consumer_bar_sync();
+          float amax = slice_amax;
+          if (cluster_amax) {
+            cluster_arrive();  // phase 1: publish this rank's slice maximum
+            cluster_wait();
+            float part_max[kMaxCluster];
+#pragma unroll
+            for (int src = 0; src < kMaxCluster; ++src)
+              part_max[src] = src < int(nrank) ? ld_dsmem_f32(smem_u32(&slice_amax), src) : 0.0f;
+#pragma unroll
+            for (int src = 0; src < kMaxCluster; ++src) amax = fmaxf(amax, part_max[src]);
+          }
+          s_a = scale_from_amax<FA>(amax);
+        }
+        const Quantizer qz = make_quantizer(s_a);
+        // quantize into act[token][k - k0]; units past K and tokens past M are plain zeros
+        auto put = [&](int i, const uint4& x) {
+          const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
+          uint2 q = make_uint2(0, 0);
+          if (k0 + kk < p.K) q = quant8_bf16<FA>(x, qz);
+          asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(act + m * p.act_stride + kk), "r"(q.x), "r"(q.y)
+                       : "memory");
+        };
 #pragma unroll
         for (int b = 0; b < kRegUnits; ++b) {
-          const int i = i0 + b * kConsumerThreads;
-          const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
-          w[b] = i < units ? load8_bf16(p.a + (int64_t)m * p.lda, k0 + kk, p.K, p.vec_a) : make_uint4(0, 0, 0, 0);
+          const int i = threadIdx.x + b * kConsumerThreads;
+          if (i < units) put(i, v[b]);
         }
+        // units beyond the register batch: reload kRegUnits at a time (independent loads)
+        for (int i0 = threadIdx.x + kRegUnits * kConsumerThreads; i0 < units; i0 += kRegUnits * kConsumerThreads) {
+          uint4 w[kRegUnits];
+          load_units(w, p, i0, units, upt, k0);
 #pragma unroll
-        for (int b = 0; b < kRegUnits; ++b)
-          if (i0 + b * kConsumerThreads < units) put(i0 + b * kConsumerThreads, w[b]);
+          for (int b = 0; b < kRegUnits; ++b)
+            if (i0 + b * kConsumerThreads < units) put(i0 + b * kConsumerThreads, w[b]);
+        }
       }
+      loads_back();  // every activation load of the prologue has landed (and the scratch is free)
       const int zu = span >> 4;  // 16-byte units per padding token
-      for (int i = threadIdx.x; i < (kMaxTokens - p.M) * zu; i += kConsumerThreads) {
+      for (int i = threadIdx.x; i < (p.act_rows - p.M) * zu; i += kConsumerThreads) {
         const int m = p.M + i / zu;
         const int kk = (i - (i / zu) * zu) << 4;
         asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" :: "r"(act + m * p.act_stride + kk), "r"(0u) : "memory");
       }
     } else if constexpr (kMode == kModeBf16) {
-      cluster_arrive();  // phase 1 is unused here but keeps every thread's phases aligned
-      cluster_wait();
       s_a = 1.0f;
-      // bf16 activation slice [16 tokens][span] -> smem (2 bytes an element), zero beyond M and K;
-      // kRegUnits independent 16-byte loads per thread in flight at a time
+      // bf16 activation slice [tokens][span] -> smem (2 bytes an element), zero beyond M and K
       const int upt = span >> 3;  // 8-element units per token
-      const int units = kMaxTokens * upt;
+      const int units = p.act_rows * upt;
       for (int i0 = threadIdx.x; i0 < units; i0 += kRegUnits * kConsumerThreads) {
         uint4 v[kRegUnits];
-#pragma unroll
-        for (int b = 0; b < kRegUnits; ++b) {
-          const int i = i0 + b * kConsumerThreads;
-          const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
-          v[b] = (i < units && m < p.M) ? load8_bf16(p.a + (int64_t)m * p.lda, k0 + kk, p.K, p.vec_a)
-                                        : make_uint4(0, 0, 0, 0);
-        }
+        load_units(v, p, i0, units, upt, k0);
 #pragma unroll
         for (int b = 0; b < kRegUnits; ++b) {
           const int i = i0 + b * kConsumerThreads;
@@ -306,26 +401,39 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
           }
         }
       }
+      loads_back();
     } else {
-      cluster_arrive();  // phase 1 is unused here but keeps every thread's phases aligned
-      cluster_wait();
       s_a = *p.s_a;
-      // activation slice [16 tokens][span] -> smem, zero beyond M and K
+      // activation slice [tokens][span] of qA -> smem, zero beyond M and K, kRegUnits
+      // independent 16-byte loads per thread in flight at a time
       const int upt = span / 16;
-      const int units = kMaxTokens * upt;
+      const int units = p.act_rows * upt;
       const int k16 = (p.K + 15) & ~15;
-      for (int i = threadIdx.x; i < units; i += kConsumerThreads) {
-        const int m = i / upt;
-        const int kk = (i - m * upt) * 16;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (m < p.M && k0 + kk < k16) v = *reinterpret_cast<const uint4*>(p.qa + (int64_t)m * p.ldqa + k0 + kk);
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};"
-                     :: "r"(act + m * p.act_stride + kk), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+      for (int i0 = threadIdx.x; i0 < units; i0 += kRegUnits * kConsumerThreads) {
+        uint4 v[kRegUnits];
+#pragma unroll
+        for (int b = 0; b < kRegUnits; ++b) {
+          const int i = i0 + b * kConsumerThreads;
+          const int m = i / upt, kk = (i - (i / upt) * upt) * 16;
+          v[b] = make_uint4(0, 0, 0, 0);
+          if (i < units && m < p.M && k0 + kk < k16)
+            v[b] = *reinterpret_cast<const uint4*>(p.qa + (int64_t)m * p.ldqa + k0 + kk);
+        }
+#pragma unroll
+        for (int b = 0; b < kRegUnits; ++b) {
+          const int i = i0 + b * kConsumerThreads;
+          if (i < units) {
+            const int m = i / upt, kk = (i - (i / upt) * upt) * 16;
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};"
+                         :: "r"(act + m * p.act_stride + kk), "r"(v[b].x), "r"(v[b].y), "r"(v[b].z), "r"(v[b].w)
+                         : "memory");
+          }
+        }
       }
+      loads_back();
     }
     if (threadIdx.x == 0) s_a_out = s_a;
     consumer_bar_sync();
-
     const int g = lane >> 2, t = lane & 3;
     const uint32_t row_lo = (warp * 16 + g) * kTileK, row_hi = row_lo + 8 * kTileK;
     // this lane's activation fragment: token g, the 16 K of unit (4j + t) of each half-row j
@@ -382,42 +490,66 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * s);
       }
-      // partials of this row block: part[r][row][token]
-      float* pr = reinterpret_cast<float*>(smem + L.part + r * kPartBytes);
+      // push the partials of this row block to the ranks that own their rows:
+      // part[r][source rank][row - owner's first row][token] in the owner's shared memory
+      if (r == 0 && !cluster_amax) cluster_wait();  // every CTA of the cluster is running
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const int row = warp * 16 + g, col = nt * 8 + 2 * t;
-        *reinterpret_cast<float2*>(pr + row * kMaxTokens + col) = make_float2(acc[nt][0], acc[nt][1]);
-        *reinterpret_cast<float2*>(pr + (row + 8) * kMaxTokens + col) = make_float2(acc[nt][2], acc[nt][3]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int row = warp * 16 + g + 8 * h, col = nt * 8 + 2 * t;
+          const int owner = row / rows_per;
+          const uint32_t dst = part + r * kPartBytes +
+                               ((rank * rows_per + (row - owner * rows_per)) * kMaxTokens + col) * 4;
+          st_dsmem_v2(dst, owner, acc[nt][2 * h], acc[nt][2 * h + 1]);
+        }
       }
+    }
+    if (rb_count == 0 && !cluster_amax) cluster_wait();
+  }
+
+  // split-K reduction work of this rank: its share of the rows of every row block
+  const int r_begin = rank * rows_per;
+  const int r_count = max(0, min(kRows, r_begin + rows_per) - r_begin);
+  const int q_per_row = (p.M + 3) / 4;  // float4 groups of tokens
+  const int items = rb_count * r_count * q_per_row;
+  auto item_n = [&](int i, int& q, int& r, int& row) {
+    q = i % q_per_row;
+    r = i / (q_per_row * r_count);
+    row = r_begin + (i / q_per_row) % r_count;
+    return (cluster + r * p.num_clusters) * kRows + row;
+  };
+  // the weight scale and bias of this thread's first output are weights: load them before the
+  // barrier so their latency hides behind it
+  float sw0 = 0.0f, b0 = 0.0f;
+  if (warp < kConsumerWarps && int(threadIdx.x) < items) {
+    int q, r, row;
+    const int n = item_n(threadIdx.x, q, r, row);
+    if (n < p.N) {
+      sw0 = p.s_w[p.per_channel ? n : 0];
+      b0 = p.bias ? bf16_bits_to_float(p.bias[n]) : 0.0f;
     }
   }
 
-  cluster_sync_all();  // every rank's partials are written (and every TMA load consumed)
+  cluster_sync_all();  // every rank's partials have arrived (and every TMA load is consumed)
 
   // ---------------- split-K reduction over the cluster + epilogue ----------------
   if (warp < kConsumerWarps) {
     const float s_a = s_a_out;
-    const int rows_per = (kRows + nrank - 1) / nrank;
-    const int r_begin = rank * rows_per;
-    const int r_count = max(0, min(kRows, r_begin + rows_per) - r_begin);
-    const int q_per_row = (p.M + 3) / 4;  // float4 groups of tokens
-    const int items = rb_count * r_count * q_per_row;
     for (int i = threadIdx.x; i < items; i += kConsumerThreads) {
-      const int q = i % q_per_row;
-      const int rr = (i / q_per_row) % r_count;
-      const int r = i / (q_per_row * r_count);
-      const int row = r_begin + rr;
-      const int n = (cluster + r * p.num_clusters) * kRows + row;
+      int q, r, row;
+      const int n = item_n(i, q, r, row);
       if (n >= p.N) continue;
-      const uint32_t off = part + r * kPartBytes + (row * kMaxTokens + 4 * q) * 4;
+      const uint32_t off = part + r * kPartBytes + ((row - r_begin) * kMaxTokens + 4 * q) * 4;
+      // every source rank's partials are local now; summed in rank order (deterministic)
       float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
       for (uint32_t src = 0; src < nrank; ++src) {
-        const float4 v = ld_dsmem_v4(off, src);
+        const float4 v = lds_f4(off + src * rows_per * kMaxTokens * 4);
         sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
       }
-      const float sc = s_a * p.s_w[p.per_channel ? n : 0];
-      const float b = p.bias ? bf16_bits_to_float(p.bias[n]) : 0.0f;
+      const bool first = i == int(threadIdx.x);
+      const float sc = s_a * (first ? sw0 : p.s_w[p.per_channel ? n : 0]);
+      const float b = first ? b0 : (p.bias ? bf16_bits_to_float(p.bias[n]) : 0.0f);
       const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -426,7 +558,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
       }
     }
   }
-  cluster_sync_all();  // peers may still be reading our partials
+  // no rank reads another's shared memory after the barrier above, so no second barrier
 }
 
 }  // namespace gemv

@@ -15,12 +15,14 @@ constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kRows = 16 * kConsumerWarps;            // 128 rows per row block
 constexpr int kTileK = 128;                           // bytes of K per tile (one swizzle row)
 constexpr int kTileBytes = kRows * kTileK;            // 16 KB
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;
 constexpr int kMinStages = 4;
 constexpr int kMaxTokens = 16;
 constexpr int kMaxCluster = 8;
 constexpr int kMaxRowBlocks = 8;                      // per cluster (partials live in smem)
-constexpr int kPartBytes = kRows * kMaxTokens * 4;    // 8 KB per row block
+// partials a rank receives for one row block: [source rank][its rows][16 tokens] fp32, at most
+// (kRows + kMaxCluster) rows in total (rows per rank rounded up)
+constexpr int kPartBytes = (kRows + kMaxCluster) * kMaxTokens * 4;
 constexpr int kMaxSlice = 4096;                       // bytes of K per rank
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kRegUnits = 8;  // 8-element units of A a consumer thread keeps in registers
@@ -51,6 +53,12 @@ struct Params {
   int stages;          // ring depth
   int row_blocks;      // ceil(N / kRows)
   int num_clusters;    // C
+  int act_rows;        // token rows staged in smem: 8 * NT
+  int head_tiles;      // weight tiles issued before the activation loads have landed
+  int cluster_amax;    // dynamic scale: 1 = exchange slice maxima over the cluster, 0 = every CTA reads all of A
+  int scratch_a;       // quantize mode: 0 = A read with per-thread loads; 1 = all of A, 2 = this rank's
+                       // slice, bulk-copied into ring stages [head_tiles, stages) that are idle until
+                       // the stream is released
 };
 
 // Shared-memory layout (from a 1024-aligned base): ring | act | partials | barriers.
@@ -58,13 +66,13 @@ struct Layout {
   uint32_t ring, act, part, bars, total;
 };
 
-__host__ __device__ inline Layout layout(int stages, int act_stride, int rb_per_cluster) {
+__host__ __device__ inline Layout layout(int stages, int act_stride, int act_rows, int rb_per_cluster) {
   Layout L;
   L.ring = 0;
   L.act = stages * kTileBytes;
-  L.part = L.act + kMaxTokens * act_stride;
+  L.part = L.act + act_rows * act_stride;
   L.bars = L.part + rb_per_cluster * kPartBytes;
-  L.total = L.bars + 2 * kMaxStages * 8;
+  L.total = L.bars + (2 * kMaxStages + 2) * 8;
   return L;
 }
 

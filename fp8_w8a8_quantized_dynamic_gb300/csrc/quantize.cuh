@@ -28,13 +28,6 @@ __device__ __forceinline__ uint4 ld_v4(const void* p) {
   return v;
 }
 
-__device__ __forceinline__ uint32_t abs_max_v4(uint32_t m2, uint4 v) {
-  m2 = abs_max_u16x2(m2, v.x);
-  m2 = abs_max_u16x2(m2, v.y);
-  m2 = abs_max_u16x2(m2, v.z);
-  return abs_max_u16x2(m2, v.w);
-}
-
 // Block-wide max of a non-negative float; the result is valid in thread 0.
 __device__ __forceinline__ float block_max_to_thread0(float v, float* red) {
   v = warp_max(v);
