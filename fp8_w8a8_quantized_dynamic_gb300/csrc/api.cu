@@ -318,18 +318,24 @@ fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uin
   // quantize mode with row-aligned A: bulk-copy A (all of it for the dynamic maximum when it
   // fits, else this rank's slice) into the ring stages that stay idle until the stream is
   // released, so the prologue reads it from shared memory with no per-thread round trips
+  // (the head shrinks, down to one tile, when that makes the copy fit)
   p.scratch_a = 0;
   if (mode == kModeQuantize && p.vec_a && p.K % 8 == 0) {
-    const int64_t free_bytes = p.head_tiles < bstages ? int64_t(bstages - p.head_tiles) * kTileBytes : 0;
+    auto head_for = [&](int64_t bytes) {  // largest head <= the default that leaves `bytes` free
+      const int64_t slots = (bytes + kTileBytes - 1) / kTileBytes;
+      return int(std::min<int64_t>(p.head_tiles, bstages - slots));
+    };
     const int64_t full_bytes = int64_t(p.M) * p.K * 2;
     const int64_t slice_bytes = int64_t(p.M) * bslice * 2;
     if (p.s_static != nullptr) {
-      if (slice_bytes <= free_bytes) p.scratch_a = 2;
-    } else if (full_bytes <= free_bytes) {
+      if (head_for(slice_bytes) >= 1) { p.scratch_a = 2; p.head_tiles = head_for(slice_bytes); }
+    } else if (head_for(full_bytes) >= 1) {
       p.scratch_a = 1;
+      p.head_tiles = head_for(full_bytes);
       p.cluster_amax = 0;
-    } else if (slice_bytes <= free_bytes) {
+    } else if (head_for(slice_bytes) >= 1) {
       p.scratch_a = 2;
+      p.head_tiles = head_for(slice_bytes);
       p.cluster_amax = 1;
     }
   }

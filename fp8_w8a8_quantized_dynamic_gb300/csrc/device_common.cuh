@@ -101,14 +101,64 @@ __device__ __forceinline__ uint32_t quant4(float x0, float x1, float x2, float x
   return quant2<F>(x0, x1, q) | (quant2<F>(x2, x3, q) << 16);
 }
 
+// Bracketed fast codes of two values: the codes of |x*r| (sign bits attached) and, in
+// `mismatch`, a non-zero bit when |y| - 4 ulp and |y| + 4 ulp round differently.
+template <int F>
+__device__ __forceinline__ uint32_t bracket2(float x0, float x1, float r, uint32_t& mismatch) {
+  const uint32_t b0 = __float_as_uint(x0 * r), b1 = __float_as_uint(x1 * r);
+  const uint32_t a0 = b0 & 0x7FFFFFFFu, a1 = b1 & 0x7FFFFFFFu;
+  const uint32_t lo = cvt_fp8x2<F>(__uint_as_float(max(a0, 4u) - 4u), __uint_as_float(max(a1, 4u) - 4u));
+  const uint32_t hi = cvt_fp8x2<F>(__uint_as_float(a0 + 4u), __uint_as_float(a1 + 4u));
+  mismatch |= lo ^ hi;
+  return lo | ((b0 >> 31) << 7) | ((b1 >> 31) << 15);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Eight bf16 (packed in a uint4) -> eight FP8 bytes with no branch: `ok` is false when the
+// scale is outside the fast range or a value lies within a few ulps of a rounding boundary,
+// and then the caller takes quant8_bf16_exact. Straight-line code lets a thread interleave
+// several units.
+template <int F>
+__device__ __forceinline__ uint2 quant8_bf16_try(uint4 v, const Quantizer& q, bool& ok) {
+  uint32_t mm = 0;
+  const uint32_t w0 = bracket2<F>(bf16_lo(v.x), bf16_hi(v.x), q.r, mm);
+  const uint32_t w1 = bracket2<F>(bf16_lo(v.y), bf16_hi(v.y), q.r, mm);
+  const uint32_t w2 = bracket2<F>(bf16_lo(v.z), bf16_hi(v.z), q.r, mm);
+  const uint32_t w3 = bracket2<F>(bf16_lo(v.w), bf16_hi(v.w), q.r, mm);
+  ok = q.fast && mm == 0;
+  return make_uint2(w0 | (w1 << 16), w2 | (w3 << 16));
+}
+
+// The same eight codes for a unit the fast path refused (out of line: rarely taken). A value
+// whose product y = x * fl(1/s) satisfies y * s == x exactly has the quotient x / s == y, so
+// its code is that of y; the fma residual proves it. This settles the common refusals: with a
+// scale of few significant bits (amax / 448 when amax's mantissa is a multiple of 7) many
+// quotients are exact and land on rounding midpoints, where only the tie rule decides. The
+// residual is exact when ulp(y) * ulp(s) >= 2^-126 (both at least 2^-40 in magnitude);
+// every other value takes the IEEE division.
+template <int F>
+static __device__ __noinline__ uint2 quant8_bf16_exact(uint4 v, float s, float r) {
+  const float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                      bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+  float y[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float ye = x[e] * r;  // r may be infinite for a tiny scale: zeros keep their own sign
+    const bool exact = fabsf(ye) >= 0x1p-40f && fabsf(ye) < 0x1p100f && s >= 0x1p-40f && fmaf(ye, s, -x[e]) == 0.0f;
+    y[e] = x[e] == 0.0f ? x[e] : (exact ? ye : __fdiv_rn(x[e], s));
+  }
+  return make_uint2(cvt_fp8x2<F>(y[0], y[1]) | (cvt_fp8x2<F>(y[2], y[3]) << 16),
+                    cvt_fp8x2<F>(y[4], y[5]) | (cvt_fp8x2<F>(y[6], y[7]) << 16));
+}
+
 // Eight bf16 (packed in a uint4) -> eight FP8 bytes (uint2).
 template <int F>
 __device__ __forceinline__ uint2 quant8_bf16(uint4 v, const Quantizer& q) {
-  auto f = [](uint32_t w, int hi) { return __uint_as_float(hi ? (w & 0xFFFF0000u) : (w << 16)); };
-  uint2 r;
-  r.x = quant4<F>(f(v.x, 0), f(v.x, 1), f(v.y, 0), f(v.y, 1), q);
-  r.y = quant4<F>(f(v.z, 0), f(v.z, 1), f(v.w, 0), f(v.w, 1), q);
-  return r;
+  bool ok;
+  const uint2 r = quant8_bf16_try<F>(v, q, ok);
+  return ok ? r : quant8_bf16_exact<F>(v, q.s, q.r);
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }

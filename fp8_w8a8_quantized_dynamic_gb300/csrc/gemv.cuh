@@ -197,10 +197,13 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
   __shared__ float s_a_out;
   __shared__ float slice_amax;
   __shared__ float red[kConsumerWarps];
+  __shared__ int n_exact;                 // units queued for exact division
+  __shared__ int exact_units[kExactSlots];
   if (warp == kConsumerWarps && lane == 0)  // fetch the descriptor while the barriers are set up
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
   if (threadIdx.x == 0) {
     abort_flag = 0;
+    n_exact = 0;
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, kConsumerWarps);
@@ -297,13 +300,54 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
           s_a = scale_from_amax<FA>(amax);
         }
         const Quantizer qz = make_quantizer(s_a);
+        // quantize the slice: kQuantUnroll units per thread per round, fast codes of all of
+        // them first (independent, branch-free), exact division only for flagged units
         const int upt = span >> 3;  // 8-element units per token of this rank's slice
-        for (int i = threadIdx.x; i < p.M * upt; i += kConsumerThreads) {
-          const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
-          uint2 q = make_uint2(0, 0);
-          if (k0 + kk < p.K)
-            q = quant8_bf16<FA>(lds_v4(scratch + uint32_t(m * rowlen + (full ? k0 : 0) + kk) * 2u), qz);
-          asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(act + m * p.act_stride + kk), "r"(q.x), "r"(q.y)
+        const int total = p.M * upt;
+        const float inv_upt = 1.0f / float(upt);  // unit -> token by float: exact for these sizes
+        for (int i0 = threadIdx.x; i0 < total; i0 += kQuantUnroll * kConsumerThreads) {
+          uint4 x[kQuantUnroll];
+          uint32_t dst[kQuantUnroll];
+          bool inside[kQuantUnroll];
+#pragma unroll
+          for (int j = 0; j < kQuantUnroll; ++j) {
+            const int i = i0 + j * kConsumerThreads;
+            const int m = int((float(i) + 0.5f) * inv_upt), kk = (i - m * upt) << 3;
+            inside[j] = i < total && k0 + kk < p.K;
+            dst[j] = i < total ? act + m * p.act_stride + kk : 0u;
+            x[j] = inside[j] ? lds_v4(scratch + uint32_t(m * rowlen + (full ? k0 : 0) + kk) * 2u)
+                             : make_uint4(0, 0, 0, 0);
+          }
+          uint2 q[kQuantUnroll];
+          bool ok[kQuantUnroll];
+#pragma unroll
+          for (int j = 0; j < kQuantUnroll; ++j) q[j] = quant8_bf16_try<FA>(x[j], qz, ok[j]);
+#pragma unroll
+          for (int j = 0; j < kQuantUnroll; ++j) {
+            if (!inside[j]) {
+              q[j] = make_uint2(0, 0);
+            } else if (!ok[j]) {
+              // a value next to a rounding boundary: queue the unit for the division pass below
+              // (one divergent division per warp round would stall all of its lanes)
+              const int slot = atomicAdd(&n_exact, 1);
+              if (slot < kExactSlots) {
+                exact_units[slot] = i0 + j * kConsumerThreads;
+                continue;
+              }
+              q[j] = quant8_bf16_exact<FA>(x[j], qz.s, qz.r);
+            }
+            if (i0 + j * kConsumerThreads < total)
+              asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(dst[j]), "r"(q[j].x), "r"(q[j].y) : "memory");
+          }
+        }
+        consumer_bar_sync();  // the queue is complete
+        const int n_queued = min(n_exact, kExactSlots);
+        for (int e = threadIdx.x; e < n_queued; e += kConsumerThreads) {
+          const int i = exact_units[e];
+          const int m = int((float(i) + 0.5f) * inv_upt), kk = (i - m * upt) << 3;
+          const uint2 qe = quant8_bf16_exact<FA>(
+              lds_v4(scratch + uint32_t(m * rowlen + (full ? k0 : 0) + kk) * 2u), qz.s, qz.r);
+          asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(act + m * p.act_stride + kk), "r"(qe.x), "r"(qe.y)
                        : "memory");
         }
       } else {

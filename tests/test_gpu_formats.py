@@ -206,3 +206,25 @@ def test_invalid_format_rejected():
     st = F.lib().fp8_linear_ex(a.data_ptr(), 2, 32, 32, 2, None, qw.data_ptr(), 0, 8, qw.stride(0), s_w.data_ptr(),
                                0, None, y.data_ptr(), 8, None, 0, torch.cuda.current_stream().cuda_stream)
     assert st == F.FP8_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("M", [1, 7, 16])
+def test_gemv_quantizer_on_rounding_boundaries(fmt, M):
+    """Activations made of FP8 rounding midpoints with amax = max(fmt), so s_a = 1 and every
+    quotient lies exactly on a boundary: the in-kernel quantizer's fast path must refuse every
+    unit and the exact division (queued, and inline once the queue is full) must decide.
+    Identity weights make every chosen code visible in Y."""
+    K = 4096
+    g = np.random.default_rng(400 + M)
+    table = O.E4M3_DECODE[:0x7F] if fmt == "e4m3" else O.E5M2_DECODE[:0x7C]
+    mids = ((table[:-1] + table[1:]) / 2).astype(np.float32)
+    mids = mids[np.abs(mids) < O.fp8_max(fmt)]
+    a = g.choice(mids, size=(M, K)) * np.where(g.random((M, K)) < 0.5, -1, 1).astype(np.float32)
+    a[0, 0] = O.fp8_max(fmt)
+    a = I.to_bf16(a.astype(np.float32))
+    assert float(O.amax(f32(a))) == O.fp8_max(fmt)
+    w = torch.eye(K, dtype=torch.bfloat16)
+    y = run_ex(a, w, fmt, "e4m3", False, None, check_w=False)
+    cols = np.sort(g.choice(K, 512, replace=False))
+    linear_parity(y, a, w, False, cols=cols, what=f"boundaries {fmt} M={M}", fmt_a=fmt, fmt_w="e4m3")
