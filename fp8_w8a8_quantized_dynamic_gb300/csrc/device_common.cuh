@@ -101,64 +101,110 @@ __device__ __forceinline__ uint32_t quant4(float x0, float x1, float x2, float x
   return quant2<F>(x0, x1, q) | (quant2<F>(x2, x3, q) << 16);
 }
 
-// Bracketed fast codes of two values: the codes of |x*r| (sign bits attached) and, in
-// `mismatch`, a non-zero bit when |y| - 4 ulp and |y| + 4 ulp round differently.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Bracketed fast codes of two values: the codes of |x*r| with sign bits attached; `bad` is
+// non-zero when |y| - 4 ulp and |y| + 4 ulp round differently.
 template <int F>
-__device__ __forceinline__ uint32_t bracket2(float x0, float x1, float r, uint32_t& mismatch) {
+__device__ __forceinline__ uint32_t bracket2(float x0, float x1, float r, uint32_t& bad) {
   const uint32_t b0 = __float_as_uint(x0 * r), b1 = __float_as_uint(x1 * r);
   const uint32_t a0 = b0 & 0x7FFFFFFFu, a1 = b1 & 0x7FFFFFFFu;
   const uint32_t lo = cvt_fp8x2<F>(__uint_as_float(max(a0, 4u) - 4u), __uint_as_float(max(a1, 4u) - 4u));
   const uint32_t hi = cvt_fp8x2<F>(__uint_as_float(a0 + 4u), __uint_as_float(a1 + 4u));
-  mismatch |= lo ^ hi;
+  bad = lo ^ hi;
   return lo | ((b0 >> 31) << 7) | ((b1 >> 31) << 15);
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Eight bf16 (packed in a uint4) -> eight FP8 bytes with no branch: `ok` is false when the
-// scale is outside the fast range or a value lies within a few ulps of a rounding boundary,
-// and then the caller takes quant8_bf16_exact. Straight-line code lets a thread interleave
-// several units.
+// Eight bf16 (packed in a uint4) -> eight FP8 bytes with no branch. `bad` gets bit p set for
+// each pair p (values 2p, 2p+1) the fast path cannot settle: a value within a few ulps of a
+// rounding boundary, or every pair when the scale is outside the fast range. Straight-line
+// code lets a thread interleave several units; quant8_bf16_fix settles the flagged pairs.
 template <int F>
-__device__ __forceinline__ uint2 quant8_bf16_try(uint4 v, const Quantizer& q, bool& ok) {
-  uint32_t mm = 0;
-  const uint32_t w0 = bracket2<F>(bf16_lo(v.x), bf16_hi(v.x), q.r, mm);
-  const uint32_t w1 = bracket2<F>(bf16_lo(v.y), bf16_hi(v.y), q.r, mm);
-  const uint32_t w2 = bracket2<F>(bf16_lo(v.z), bf16_hi(v.z), q.r, mm);
-  const uint32_t w3 = bracket2<F>(bf16_lo(v.w), bf16_hi(v.w), q.r, mm);
-  ok = q.fast && mm == 0;
+__device__ __forceinline__ uint2 quant8_bf16_try(uint4 v, const Quantizer& q, uint32_t& bad) {
+  uint32_t b0, b1, b2, b3;
+  const uint32_t w0 = bracket2<F>(bf16_lo(v.x), bf16_hi(v.x), q.r, b0);
+  const uint32_t w1 = bracket2<F>(bf16_lo(v.y), bf16_hi(v.y), q.r, b1);
+  const uint32_t w2 = bracket2<F>(bf16_lo(v.z), bf16_hi(v.z), q.r, b2);
+  const uint32_t w3 = bracket2<F>(bf16_lo(v.w), bf16_hi(v.w), q.r, b3);
+  bad = q.fast ? (uint32_t(b0 != 0) | (uint32_t(b1 != 0) << 1) | (uint32_t(b2 != 0) << 2) | (uint32_t(b3 != 0) << 3))
+               : 0xFu;
   return make_uint2(w0 | (w1 << 16), w2 | (w3 << 16));
 }
 
-// The same eight codes for a unit the fast path refused (out of line: rarely taken). A value
-// whose product y = x * fl(1/s) satisfies y * s == x exactly has the quotient x / s == y, so
-// its code is that of y; the fma residual proves it. This settles the common refusals: with a
-// scale of few significant bits (amax / 448 when amax's mantissa is a multiple of 7) many
-// quotients are exact and land on rounding midpoints, where only the tie rule decides. The
-// residual is exact when ulp(y) * ulp(s) >= 2^-126 (both at least 2^-40 in magnitude);
-// every other value takes the IEEE division.
+// Quotients the fast path refused. When y = x * fl(1/s) satisfies y * s == x exactly, the
+// quotient x / s is y itself; the fma residual proves it, and is exact when
+// ulp(y) * ulp(s) >= 2^-126 (both at least 2^-40 in magnitude). That settles most refusals:
+// with a scale of few significant bits (amax / 448 when amax's mantissa is a multiple of 7),
+// or values whose mantissa shares the scale's factors, many quotients are exact and sit on
+// rounding midpoints, where only the tie rule decides. Zeros keep their sign (r may be
+// infinite for a tiny scale).
+__device__ __forceinline__ bool quotient_is_product(float x, float y, float s) {
+  return x == 0.0f || (fabsf(y) >= 0x1p-40f && fabsf(y) < 0x1p100f && s >= 0x1p-40f && fmaf(y, s, -x) == 0.0f);
+}
+
+// Exact codes for the pairs flagged in `bad` that the residual settles, in line (short code,
+// taken by the lanes that need it); returns the pairs still unsettled.
 template <int F>
-static __device__ __noinline__ uint2 quant8_bf16_exact(uint4 v, float s, float r) {
-  const float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                      bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-  float y[8];
+__device__ __forceinline__ uint32_t quant8_bf16_settle(uint4 v, uint2& codes, uint32_t bad, float s, float r) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t c[2] = {codes.x, codes.y};
+  uint32_t left = 0;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const float ye = x[e] * r;  // r may be infinite for a tiny scale: zeros keep their own sign
-    const bool exact = fabsf(ye) >= 0x1p-40f && fabsf(ye) < 0x1p100f && s >= 0x1p-40f && fmaf(ye, s, -x[e]) == 0.0f;
-    y[e] = x[e] == 0.0f ? x[e] : (exact ? ye : __fdiv_rn(x[e], s));
+  for (int p = 0; p < 4; ++p) {
+    if (bad & (1u << p)) {
+      const float x0 = bf16_lo(w[p]), x1 = bf16_hi(w[p]);
+      const float y0 = x0 == 0.0f ? x0 : x0 * r, y1 = x1 == 0.0f ? x1 : x1 * r;
+      if (quotient_is_product(x0, y0, s) && quotient_is_product(x1, y1, s)) {
+        const int sh = (p & 1) * 16;
+        c[p >> 1] = (c[p >> 1] & ~(0xFFFFu << sh)) | (cvt_fp8x2<F>(y0, y1) << sh);
+      } else {
+        left |= 1u << p;
+      }
+    }
   }
-  return make_uint2(cvt_fp8x2<F>(y[0], y[1]) | (cvt_fp8x2<F>(y[2], y[3]) << 16),
-                    cvt_fp8x2<F>(y[4], y[5]) | (cvt_fp8x2<F>(y[6], y[7]) << 16));
+  codes = make_uint2(c[0], c[1]);
+  return left;
+}
+
+// Codes of the flagged pairs by IEEE division (out of line: rarely taken).
+template <int F>
+static __device__ __noinline__ uint2 quant8_bf16_divide(uint4 v, uint2 codes, uint32_t left, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t c[2] = {codes.x, codes.y};
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    if (left & (1u << p)) {
+      const uint32_t pair = cvt_fp8x2<F>(__fdiv_rn(bf16_lo(w[p]), s), __fdiv_rn(bf16_hi(w[p]), s));
+      const int sh = (p & 1) * 16;
+      c[p >> 1] = (c[p >> 1] & ~(0xFFFFu << sh)) | (pair << sh);
+    }
+  }
+  return make_uint2(c[0], c[1]);
+}
+
+// Settles the flagged pairs of a unit: the residual proof in line, division for the rest.
+template <int F>
+__device__ __forceinline__ uint2 quant8_bf16_fix(uint4 v, uint2 codes, uint32_t bad, float s, float r) {
+  const uint32_t left = quant8_bf16_settle<F>(v, codes, bad, s, r);
+  return left ? quant8_bf16_divide<F>(v, codes, left, s) : codes;
+}
+
+// Eight bf16 -> eight FP8 bytes, two values at a time (quant2: bracket, division if refused).
+template <int F>
+__device__ __forceinline__ uint2 quant8_bf16_pairwise(uint4 v, const Quantizer& q) {
+  uint2 r;
+  r.x = quant4<F>(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y), q);
+  r.y = quant4<F>(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w), q);
+  return r;
 }
 
 // Eight bf16 (packed in a uint4) -> eight FP8 bytes (uint2).
 template <int F>
 __device__ __forceinline__ uint2 quant8_bf16(uint4 v, const Quantizer& q) {
-  bool ok;
-  const uint2 r = quant8_bf16_try<F>(v, q, ok);
-  return ok ? r : quant8_bf16_exact<F>(v, q.s, q.r);
+  uint32_t bad;
+  const uint2 r = quant8_bf16_try<F>(v, q, bad);
+  return bad == 0 ? r : quant8_bf16_fix<F>(v, r, bad, q.s, q.r);
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }

@@ -319,14 +319,14 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
                              : make_uint4(0, 0, 0, 0);
           }
           uint2 q[kQuantUnroll];
-          bool ok[kQuantUnroll];
+          uint32_t bad[kQuantUnroll];
 #pragma unroll
-          for (int j = 0; j < kQuantUnroll; ++j) q[j] = quant8_bf16_try<FA>(x[j], qz, ok[j]);
+          for (int j = 0; j < kQuantUnroll; ++j) q[j] = quant8_bf16_try<FA>(x[j], qz, bad[j]);
 #pragma unroll
           for (int j = 0; j < kQuantUnroll; ++j) {
             if (!inside[j]) {
               q[j] = make_uint2(0, 0);
-            } else if (!ok[j]) {
+            } else if (bad[j]) {
               // a value next to a rounding boundary: queue the unit for the division pass below
               // (one divergent division per warp round would stall all of its lanes)
               const int slot = atomicAdd(&n_exact, 1);
@@ -334,7 +334,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
                 exact_units[slot] = i0 + j * kConsumerThreads;
                 continue;
               }
-              q[j] = quant8_bf16_exact<FA>(x[j], qz.s, qz.r);
+              q[j] = quant8_bf16_fix<FA>(x[j], q[j], bad[j], qz.s, qz.r);
             }
             if (i0 + j * kConsumerThreads < total)
               asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(dst[j]), "r"(q[j].x), "r"(q[j].y) : "memory");
@@ -345,8 +345,10 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
         for (int e = threadIdx.x; e < n_queued; e += kConsumerThreads) {
           const int i = exact_units[e];
           const int m = int((float(i) + 0.5f) * inv_upt), kk = (i - m * upt) << 3;
-          const uint2 qe = quant8_bf16_exact<FA>(
-              lds_v4(scratch + uint32_t(m * rowlen + (full ? k0 : 0) + kk) * 2u), qz.s, qz.r);
+          const uint4 xe = lds_v4(scratch + uint32_t(m * rowlen + (full ? k0 : 0) + kk) * 2u);
+          uint32_t bad_e;
+          const uint2 qf = quant8_bf16_try<FA>(xe, qz, bad_e);
+          const uint2 qe = quant8_bf16_fix<FA>(xe, qf, bad_e, qz.s, qz.r);
           asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(act + m * p.act_stride + kk), "r"(qe.x), "r"(qe.y)
                        : "memory");
         }
