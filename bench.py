@@ -139,6 +139,21 @@ def flops(M, layers):
     return sum(2.0 * M * L.N * L.K for L in layers)
 
 
+def max_over_ranks(torch, ms: float, world: int, device=None) -> float:
+    """The slowest replica's time: the job is done when its last rank is (no-op at N = 1)."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_rate(work_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job throughput of N independent replicas (weak scaling): all ranks' work over the
+    slowest rank's time, per second."""
+    return world * work_per_rank / (ms_max * 1e-3)
+
+
 def time_loop(torch, fn, steps: int, warmup: int):
     """Median-free timing: W warm-up calls, then K calls between two events (both synced)."""
     for _ in range(warmup):
@@ -285,13 +300,9 @@ def run_ours(args, rank: int, world: int):
         if world > 1:
             torch.distributed.barrier()
         ms = t0.elapsed_time(t1) / args.steps
-        ms_max = ms
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms_max = float(t.item())
+        ms_max = max_over_ranks(torch, ms, world, dev)
         total_flops = flops(M, layers)
-        value = world * total_flops / (ms_max * 1e-3) / 1e12
+        value = replica_rate(total_flops, world, ms_max) / 1e12
         launches = args.steps * len(layers) * 3  # amax, cast, gemm per layer
 
         # ---- GEMM kernel alone (fp8_scaled_mm on the quantized activations), per layer
@@ -344,9 +355,9 @@ def run_ours(args, rank: int, world: int):
                     for i in range(len(layers)):
                         F.fp8_linear(ad[i], dq[c][i][0], dq[c][i][1], out=ydm[i])
 
-            t_eager = time_loop(torch, dstep, max(5, args.steps), 3)
-            t = time_loop(torch, graph_of(torch, dstep).replay, max(5, args.steps), 3)
-            per_m[str(Md)] = {"weight_gbs": round(wbytes_step / (t * 1e-3) / 1e9, 1),
+            t_eager = max_over_ranks(torch, time_loop(torch, dstep, max(5, args.steps), 3), world, dev)
+            t = max_over_ranks(torch, time_loop(torch, graph_of(torch, dstep).replay, max(5, args.steps), 3), world, dev)
+            per_m[str(Md)] = {"weight_gbs": round(replica_rate(wbytes_step, world, t) / 1e9, 1),
                               "us_per_layer": round(t * 1e3 / (copies * len(layers)), 2),
                               "eager_us_per_layer": round(t_eager * 1e3 / (copies * len(layers)), 2)}
         gbs = [v["weight_gbs"] for v in per_m.values()]
@@ -377,8 +388,8 @@ def run_ours(args, rank: int, world: int):
                 F.fp8_linear_channelwise(A_d[i], Wq[i][0], Wq[i][1], out=Y[i], ws=ws)
                 Y_h[i].copy_(Y[i], non_blocking=True)
 
-        te = time_loop(torch, estep, max(3, args.steps // 4), 2)
-        e2e = {"value": round(world * total_flops / (te * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        te = max_over_ranks(torch, time_loop(torch, estep, max(3, args.steps // 4), 2), world, dev)
+        e2e = {"value": round(replica_rate(total_flops, world, te) / 1e12, 2), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(sum(a.numel() * 2 for a in A_h)),
                "d2h_bytes_per_step": int(sum(y.numel() * 2 for y in Y_h)), "ms_per_step": round(te, 3)}
 

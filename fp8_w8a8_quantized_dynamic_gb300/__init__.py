@@ -65,6 +65,7 @@ _SIGNATURES = {
     "fp8_linear_weight_only": (_int, [_vp, _i64, _i64, _i64, _vp, _int, _i64, _i64, _vp, _int, _vp, _vp, _i64,
                                       _vp, _sz, _vp]),
     "fp8_last_device_status": (_int, [_vp]),
+    "fp8_selftest_timeout": (_int, [_i64, _vp]),
     "fp8_status_string": (ctypes.c_char_p, [_int]),
 }
 
@@ -341,6 +342,13 @@ def fp8_linear_noalloc(a, qw, s_w, per_channel: bool = False, bias=None, out=Non
                                     s_w.data_ptr(), int(per_channel), _ptr(bias), y.data_ptr(), y.stride(0),
                                     _stream_ptr(a)), "fp8_linear_noalloc")
     return y
+
+
+def fp8_selftest_timeout(limit_ns: int = 20_000_000, stream=None) -> int:
+    """Enqueue the failure-path self-test (a bounded device wait made to run out); returns the status."""
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    return int(lib().fp8_selftest_timeout(int(limit_ns), s))
 
 
 def fp8_last_device_status(stream=None) -> int:

@@ -691,6 +691,14 @@ FP8_API fp8_status fp8_last_device_status(fp8_stream_t stream) {
   return (e & kErrTimeout) ? FP8_ERR_TIMEOUT : FP8_OK;
 }
 
+FP8_API fp8_status fp8_selftest_timeout(int64_t limit_ns, fp8_stream_t stream) {
+  if (limit_ns < 1000 || limit_ns > 10000000000ll) return FP8_ERR_INVALID_ARG;
+  int sms = 0;
+  FP8_TRY(current_device(&sms));
+  gemv::selftest_timeout(static_cast<unsigned long long>(limit_ns), reinterpret_cast<cudaStream_t>(stream));
+  return report_cuda(cudaGetLastError(), "self-test launch") == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
 FP8_API const char* fp8_status_string(fp8_status s) {
   switch (s) {
     case FP8_OK: return "FP8_OK";

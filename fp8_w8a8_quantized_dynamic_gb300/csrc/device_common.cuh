@@ -319,17 +319,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete. Gives up (returns false) when
-// *abort_flag becomes non-zero or after kWaitLimitNs; on a timeout it raises the abort
-// flag and ORs kErrTimeout into *err so the host can report it. Never spins unbounded.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  volatile int* abort_flag, unsigned int* err) {
+// *abort_flag becomes non-zero or after limit_ns (kWaitLimitNs by default); on a timeout it
+// raises the abort flag and ORs kErrTimeout into *err so the host can report it. Never spins
+// unbounded.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                  unsigned int* err,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 15u) == 0) {
       if (abort_flag != nullptr && *abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         if (abort_flag != nullptr) *abort_flag = 1;
         atomicOr(err, kErrTimeout);
         return false;

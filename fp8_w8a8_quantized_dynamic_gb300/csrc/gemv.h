@@ -83,6 +83,9 @@ __host__ __device__ inline Layout layout(int stages, int act_stride, int act_row
 using KernelFn = void (*)(CUtensorMap, Params);
 KernelFn kernel_for(int NT, int mode, int fa, int fw);
 
+// Enqueues the failure-path self-test kernel (a bounded wait made to run out after limit_ns).
+void selftest_timeout(unsigned long long limit_ns, cudaStream_t st);
+
 // Device-side error bits of the GEMV on the current device (read, then cleared).
 unsigned int read_and_clear_error();
 

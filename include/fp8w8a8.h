@@ -286,6 +286,17 @@ fp8_status fp8_linear_weight_only(const void* a_bf16, int64_t M, int64_t K, int6
  */
 fp8_status fp8_last_device_status(fp8_stream_t stream);
 
+/*
+ * Failure-path self-test: enqueues a small kernel whose bounded device wait is
+ * made to run out (its producer withholds one item), using the same wait
+ * primitive and error word as the library's GEMV. The wait gives up after
+ * limit_ns (1e3 .. 1e10 nanoseconds, else FP8_ERR_INVALID_ARG), the kernel
+ * returns normally and the context stays usable; the next
+ * fp8_last_device_status reports FP8_ERR_TIMEOUT once. Nothing faults or hangs.
+ * The pages have no counterpart; it exists so the error path can be tested.
+ */
+fp8_status fp8_selftest_timeout(int64_t limit_ns, fp8_stream_t stream);
+
 /* Static, human-readable name of a status code. Never NULL. */
 const char* fp8_status_string(fp8_status status);
 

@@ -178,3 +178,8 @@ def test_static_quantize_needs_no_workspace(L):
     # static scale: validation passes without a workspace; only the device query fails here
     assert L.fp8_quantize_act_ex(P, 8, 64, 64, 0, P, P, 64, P, None, 0, None) in (
         F.FP8_ERR_CUDA, F.FP8_ERR_UNSUPPORTED_DEVICE)
+
+
+def test_selftest_rejects_bad_limits(L):
+    for limit in (-1, 0, 999, 10_000_000_001):
+        assert L.fp8_selftest_timeout(limit, None) == F.FP8_ERR_INVALID_ARG
