@@ -275,24 +275,24 @@ fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uin
     const int kslice = slice_tiles * kTileK;
     if (kslice > max_slice) continue;
     const int act_stride = gemv_act_stride(mode, kslice);
-    // deepest ring that fits with room for the most row blocks a cluster may own
-    int stages = kMaxStages;
-    while (stages > kMinStages && smem_for(stages, act_stride, kMaxRowBlocks) > size_t(smem_limit)) --stages;
-    if (smem_for(stages, act_stride, kMaxRowBlocks) > size_t(smem_limit)) continue;
-    const int cmax = gemv_max_clusters(kfn, S, smem_for(stages, act_stride, kMaxRowBlocks));
+    if (smem_for(kMinStages, act_stride, 1) > size_t(smem_limit)) continue;
+    // co-resident clusters at the largest shared memory any configuration may take (a lower
+    // bound for every configuration, so the grid never runs in waves)
+    const int cmax = gemv_max_clusters(kfn, S, size_t(smem_limit));
     if (cmax <= 0) continue;
     int C = std::min(cmax, R);
     const int nrb = (R + C - 1) / C;
     if (nrb > kMaxRowBlocks) continue;
     C = (R + nrb - 1) / nrb;
+    if (smem_for(kMinStages, act_stride, nrb) > size_t(smem_limit)) continue;
     // streamed tiles of the busiest CTA, plus (dynamic mode) its activation prologue: each
     // batch of kRegUnits A loads per consumer thread costs about as much as two weight tiles
     const int units = p.M * (kslice / 8);
     const int batches = dyn ? (units + kRegUnits * kConsumerThreads - 1) / (kRegUnits * kConsumerThreads) : 0;
     const int cost = nrb * slice_tiles + 2 * (batches > 1 ? batches : 0);
     if (best_cost < 0 || cost < best_cost) {
-      // with the row blocks known, deepen the ring into the smem they leave free
-      int stg = stages;
+      // with the row blocks known, the deepest ring that fits
+      int stg = kMinStages;
       while (stg < kMaxStages && smem_for(stg + 1, act_stride, nrb) <= size_t(smem_limit)) ++stg;
       best_cost = cost;
       bS = S;

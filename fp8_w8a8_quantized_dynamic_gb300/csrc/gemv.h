@@ -28,7 +28,7 @@ constexpr int kSmemLimit = 227 * 1024;
 constexpr int kRegUnits = 8;  // 8-element units of A a consumer thread keeps in registers
 constexpr int kQuantUnroll = 4;  // units a consumer thread quantizes per round (independent chains)
 constexpr int kExactSlots = 512;  // units next to a rounding boundary queued for the division pass
-constexpr int kMaxSliceBf16 = 2048;                   // bytes of K per rank with bf16 activations
+constexpr int kMaxSliceBf16 = 4096;  // K elements per rank with bf16 activations (smem permitting)
 
 // Activation modes of the kernel.
 constexpr int kModePrequant = 0;  // qA and s_a given (fp8_scaled_mm)

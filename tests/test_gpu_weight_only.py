@@ -60,7 +60,7 @@ def test_weight_only_decode(fmt, M):
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
-@pytest.mark.parametrize("K", [4096, 14336, 16384])
+@pytest.mark.parametrize("K", [4096, 14336, 16384, 32768])
 def test_weight_only_decode_layer_k(fmt, K):
     for M in (1, 16):
         N = 1500
@@ -72,7 +72,7 @@ def test_weight_only_decode_layer_k(fmt, K):
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
 @pytest.mark.parametrize("M,K,N,pad", [(17, 1000, 1027, 0), (300, 2048, 640, 0), (129, 1001, 700, 0),
-                                       (200, 1024, 513, 3), (5, 16400, 300, 0)])
+                                       (200, 1024, 513, 3), (5, 32800, 300, 0)])
 def test_weight_only_gemm(fmt, M, K, N, pad):
     """GEMM path: ragged M, N and K, K not a multiple of 8 and an odd row stride (A is copied to an
     aligned buffer), and a decode-sized M whose K is beyond the GEMV's slice budget."""
