@@ -58,12 +58,13 @@ __device__ __forceinline__ uint32_t fp8x2_to_bf16x2(uint32_t codes) {
 // Quantizer for one scale s: FP8 codes of fl32(x / s), most of the time without a division.
 // y = x * fl32(1/s) carries two roundings, so |y - fl32(x/s)| < 3 ulp(y) (relative error at
 // most 3 * 2^-24 against an ulp of at least 2^-24 |y|). Rounding to FP8 is monotone and
-// symmetric in sign, so when the magnitudes |y| - 4 ulp and |y| + 4 ulp (4 steps of the fp32
-// bit pattern, at least 2 ulp(y) in either direction) round to the same FP8 magnitude, that
-// is the magnitude of the exact quotient's code and the sign comes from y. Otherwise the
-// quotient lies within a few ulps of an FP8 rounding boundary and the IEEE division decides
-// (out of line, so the common path stays short). Scales below 2^-125, where 1/s could
-// overflow, always divide.
+// symmetric in sign, so when |y| - 4 ulp and |y| + 4 ulp (4 steps of the fp32 bit pattern, at
+// least 2 ulp(y) in either direction; clamped at zero below) round to the same FP8 magnitude,
+// that is the magnitude of the exact quotient's code. The upper end is converted with y's sign
+// (a negative bit pattern grows in magnitude when incremented), so its code is the answer.
+// Otherwise the quotient lies within a few ulps of an FP8 rounding boundary and the value is
+// refused: an fma residual that proves the quotient exact, or the IEEE division, decides.
+// Scales below 2^-125, where 1/s could overflow, always divide.
 struct Quantizer {
   float s, r;
   bool fast;
@@ -82,15 +83,28 @@ static __device__ __noinline__ uint32_t quant2_divide(float x0, float x1, float 
   return cvt_fp8x2<F>(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
 }
 
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Bracket of two values: returns the codes of the upper ends (with signs) and sets `bad`
+// non-zero when a lower end rounds to another magnitude.
+template <int F>
+__device__ __forceinline__ uint32_t bracket2(float x0, float x1, float r, uint32_t& bad) {
+  const uint32_t b0 = __float_as_uint(x0 * r), b1 = __float_as_uint(x1 * r);
+  const uint32_t a0 = b0 & 0x7FFFFFFFu, a1 = b1 & 0x7FFFFFFFu;
+  const uint32_t lo = cvt_fp8x2<F>(__uint_as_float(max(a0, 4u) - 4u), __uint_as_float(max(a1, 4u) - 4u));
+  const uint32_t hi = cvt_fp8x2<F>(__uint_as_float(b0 + 4u), __uint_as_float(b1 + 4u));
+  bad = (hi & 0x7F7Fu) ^ lo;
+  return hi;
+}
+
 // Two values -> two FP8 bytes of format F (x0 in bits 0..7, x1 in bits 8..15).
 template <int F>
 __device__ __forceinline__ uint32_t quant2(float x0, float x1, const Quantizer& q) {
   if (q.fast) {
-    const uint32_t b0 = __float_as_uint(x0 * q.r), b1 = __float_as_uint(x1 * q.r);
-    const uint32_t a0 = b0 & 0x7FFFFFFFu, a1 = b1 & 0x7FFFFFFFu;
-    const uint32_t lo = cvt_fp8x2<F>(__uint_as_float(a0 > 4u ? a0 - 4u : 0u), __uint_as_float(a1 > 4u ? a1 - 4u : 0u));
-    const uint32_t hi = cvt_fp8x2<F>(__uint_as_float(a0 + 4u), __uint_as_float(a1 + 4u));
-    if (lo == hi) return lo | ((b0 >> 31) << 7) | ((b1 >> 31) << 15);
+    uint32_t bad;
+    const uint32_t c = bracket2<F>(x0, x1, q.r, bad);
+    if (bad == 0) return c;
   }
   return quant2_divide<F>(x0, x1, q.s);
 }
@@ -99,21 +113,6 @@ __device__ __forceinline__ uint32_t quant2(float x0, float x1, const Quantizer& 
 template <int F>
 __device__ __forceinline__ uint32_t quant4(float x0, float x1, float x2, float x3, const Quantizer& q) {
   return quant2<F>(x0, x1, q) | (quant2<F>(x2, x3, q) << 16);
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Bracketed fast codes of two values: the codes of |x*r| with sign bits attached; `bad` is
-// non-zero when |y| - 4 ulp and |y| + 4 ulp round differently.
-template <int F>
-__device__ __forceinline__ uint32_t bracket2(float x0, float x1, float r, uint32_t& bad) {
-  const uint32_t b0 = __float_as_uint(x0 * r), b1 = __float_as_uint(x1 * r);
-  const uint32_t a0 = b0 & 0x7FFFFFFFu, a1 = b1 & 0x7FFFFFFFu;
-  const uint32_t lo = cvt_fp8x2<F>(__uint_as_float(max(a0, 4u) - 4u), __uint_as_float(max(a1, 4u) - 4u));
-  const uint32_t hi = cvt_fp8x2<F>(__uint_as_float(a0 + 4u), __uint_as_float(a1 + 4u));
-  bad = lo ^ hi;
-  return lo | ((b0 >> 31) << 7) | ((b1 >> 31) << 15);
 }
 
 // Eight bf16 (packed in a uint4) -> eight FP8 bytes with no branch. `bad` gets bit p set for
