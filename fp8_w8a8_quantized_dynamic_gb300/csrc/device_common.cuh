@@ -56,17 +56,18 @@ __device__ __forceinline__ uint32_t fp8x2_to_bf16x2(uint32_t codes) {
 }
 
 // Quantizer for one scale s: FP8 codes of fl32(x / s), most of the time without a division.
-// y = x * fl32(1/s) carries two roundings, so |y - fl32(x/s)| < 3 ulp(y) (relative error at
-// most 3 * 2^-24 against an ulp of at least 2^-24 |y|). Rounding to FP8 is monotone and
-// symmetric in sign, so when |y| - 4 ulp and |y| + 4 ulp (4 steps of the fp32 bit pattern, at
-// least 2 ulp(y) in either direction; clamped at zero below) round to the same FP8 magnitude,
-// that is the magnitude of the exact quotient's code. The upper end is converted with y's sign
-// (a negative bit pattern grows in magnitude when incremented), so its code is the answer.
-// Otherwise the quotient lies within a few ulps of an FP8 rounding boundary and the value is
-// refused: an fma residual that proves the quotient exact, or the IEEE division, decides.
-// Scales below 2^-125, where 1/s could overflow, always divide.
+// With r = fl32(1/s), the products L = fl32(|x| * fl32(r * (1 - 2^-20))) and
+// H = fl32(x * fl32(r * (1 + 2^-20))) bracket the quotient strictly: each carries at most
+// four roundings of 2^-24 (relative) against a 2^-20 margin, so L < |fl32(x/s)| < |H|, and
+// the bracket is at most ~2^-19 |x/s| wide. Rounding to FP8 is monotone and symmetric in sign,
+// so when L and |H| round to the same FP8 magnitude, that is the magnitude of the quotient's
+// code, and H (converted with x's sign) gives the code itself. Zero, overflow to infinity
+// (saturation) and fp32 subnormal quotients (FP8 zero) all fall out of the same test.
+// Otherwise the quotient lies next to an FP8 rounding boundary and the value is refused: an
+// fma residual that proves the quotient exact, or the IEEE division, decides. Scales below
+// 2^-125, where 1/s could overflow, always divide.
 struct Quantizer {
-  float s, r;
+  float s, r, r_lo, r_hi;
   bool fast;
 };
 
@@ -74,6 +75,8 @@ __device__ __forceinline__ Quantizer make_quantizer(float s) {
   Quantizer q;
   q.s = s;
   q.r = __frcp_rn(s);
+  q.r_lo = q.r * (1.0f - 0x1p-20f);
+  q.r_hi = q.r * (1.0f + 0x1p-20f);
   q.fast = s >= 0x1p-125f && q.r < 0x1p126f;
   return q;
 }
@@ -86,14 +89,12 @@ static __device__ __noinline__ uint32_t quant2_divide(float x0, float x1, float 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Bracket of two values: returns the codes of the upper ends (with signs) and sets `bad`
-// non-zero when a lower end rounds to another magnitude.
+// Bracket of two values (see Quantizer): returns the codes of the upper ends (with signs) and
+// sets `bad` non-zero when a lower end rounds to another magnitude.
 template <int F>
-__device__ __forceinline__ uint32_t bracket2(float x0, float x1, float r, uint32_t& bad) {
-  const uint32_t b0 = __float_as_uint(x0 * r), b1 = __float_as_uint(x1 * r);
-  const uint32_t a0 = b0 & 0x7FFFFFFFu, a1 = b1 & 0x7FFFFFFFu;
-  const uint32_t lo = cvt_fp8x2<F>(__uint_as_float(max(a0, 4u) - 4u), __uint_as_float(max(a1, 4u) - 4u));
-  const uint32_t hi = cvt_fp8x2<F>(__uint_as_float(b0 + 4u), __uint_as_float(b1 + 4u));
+__device__ __forceinline__ uint32_t bracket2(float x0, float x1, const Quantizer& q, uint32_t& bad) {
+  const uint32_t lo = cvt_fp8x2<F>(fabsf(x0) * q.r_lo, fabsf(x1) * q.r_lo);
+  const uint32_t hi = cvt_fp8x2<F>(x0 * q.r_hi, x1 * q.r_hi);
   bad = (hi & 0x7F7Fu) ^ lo;
   return hi;
 }
@@ -103,7 +104,7 @@ template <int F>
 __device__ __forceinline__ uint32_t quant2(float x0, float x1, const Quantizer& q) {
   if (q.fast) {
     uint32_t bad;
-    const uint32_t c = bracket2<F>(x0, x1, q.r, bad);
+    const uint32_t c = bracket2<F>(x0, x1, q, bad);
     if (bad == 0) return c;
   }
   return quant2_divide<F>(x0, x1, q.s);
@@ -122,10 +123,10 @@ __device__ __forceinline__ uint32_t quant4(float x0, float x1, float x2, float x
 template <int F>
 __device__ __forceinline__ uint2 quant8_bf16_try(uint4 v, const Quantizer& q, uint32_t& bad) {
   uint32_t b0, b1, b2, b3;
-  const uint32_t w0 = bracket2<F>(bf16_lo(v.x), bf16_hi(v.x), q.r, b0);
-  const uint32_t w1 = bracket2<F>(bf16_lo(v.y), bf16_hi(v.y), q.r, b1);
-  const uint32_t w2 = bracket2<F>(bf16_lo(v.z), bf16_hi(v.z), q.r, b2);
-  const uint32_t w3 = bracket2<F>(bf16_lo(v.w), bf16_hi(v.w), q.r, b3);
+  const uint32_t w0 = bracket2<F>(bf16_lo(v.x), bf16_hi(v.x), q, b0);
+  const uint32_t w1 = bracket2<F>(bf16_lo(v.y), bf16_hi(v.y), q, b1);
+  const uint32_t w2 = bracket2<F>(bf16_lo(v.z), bf16_hi(v.z), q, b2);
+  const uint32_t w3 = bracket2<F>(bf16_lo(v.w), bf16_hi(v.w), q, b3);
   bad = q.fast ? (uint32_t(b0 != 0) | (uint32_t(b1 != 0) << 1) | (uint32_t(b2 != 0) << 2) | (uint32_t(b3 != 0) << 3))
                : 0xFu;
   return make_uint2(w0 | (w1 << 16), w2 | (w3 << 16));
