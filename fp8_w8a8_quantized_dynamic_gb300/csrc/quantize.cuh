@@ -125,11 +125,27 @@ cast_kernel(const uint16_t* __restrict__ a, int64_t rows, int64_t cols, int64_t 
   const Idx upr = static_cast<Idx>(ldq >> 4);  // 16-byte output units per row
   const Idx units = static_cast<Idx>(rows) * upr;
   const Idx stride = static_cast<Idx>(gridDim.x) * blockDim.x;
-  for (Idx u = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x; u < units; u += stride) {
-    const Idx r = u / upr;
-    const int64_t c = static_cast<int64_t>(u - r * upr) << 4;
-    const uint4 out = quant16_row<F>(a + (int64_t)r * ld + c, c, cols, vec != 0, s);
-    *reinterpret_cast<uint4*>(q + (int64_t)r * ldq + c) = out;
+  // two units per thread per round, all four 16-byte loads issued before any arithmetic: the
+  // loop is bound by loads in flight and instruction issue, not by HBM
+  for (Idx u0 = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x; u0 < units; u0 += 2 * stride) {
+    const Idx u1 = u0 + stride < units ? u0 + stride : u0;
+    const Idx r0 = u0 / upr, r1 = u1 / upr;
+    const int64_t c0 = static_cast<int64_t>(u0 - r0 * upr) << 4, c1 = static_cast<int64_t>(u1 - r1 * upr) << 4;
+    const uint16_t* s0 = a + (int64_t)r0 * ld + c0;
+    const uint16_t* s1 = a + (int64_t)r1 * ld + c1;
+    uint4 o0, o1;
+    if (vec && c0 + 16 <= cols && c1 + 16 <= cols) {
+      const uint4 v0 = ld_v4(s0), v1 = ld_v4(s0 + 8), v2 = ld_v4(s1), v3 = ld_v4(s1 + 8);
+      const uint2 q0 = quant8_bf16_pairwise<F>(v0, s), q1 = quant8_bf16_pairwise<F>(v1, s);
+      const uint2 q2 = quant8_bf16_pairwise<F>(v2, s), q3 = quant8_bf16_pairwise<F>(v3, s);
+      o0 = make_uint4(q0.x, q0.y, q1.x, q1.y);
+      o1 = make_uint4(q2.x, q2.y, q3.x, q3.y);
+    } else {
+      o0 = quant16_row<F>(s0, c0, cols, vec != 0, s);
+      o1 = quant16_row<F>(s1, c1, cols, vec != 0, s);
+    }
+    *reinterpret_cast<uint4*>(q + (int64_t)r0 * ldq + c0) = o0;
+    if (u1 != u0) *reinterpret_cast<uint4*>(q + (int64_t)r1 * ldq + c1) = o1;
   }
 }
 
