@@ -381,12 +381,35 @@ def run_ours(args, rank: int, world: int):
         A_h = [a.pin_memory() for _, a, _ in host]
         Y_h = [torch.empty((M, L.N), dtype=torch.bfloat16).pin_memory() for L in layers]
         A_d = A
+        # A user's pipeline: host->device copies on one stream, the linears on the compute
+        # stream, device->host copies on a third, ordered per layer by events, so the two
+        # copy directions overlap each other and the compute of neighbouring layers.
+        compute = torch.cuda.current_stream(dev)
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        n = len(layers)
+        ev_in = [torch.cuda.Event() for _ in range(n)]
+        ev_done = [torch.cuda.Event() for _ in range(n)]
+        ev_out = [torch.cuda.Event() for _ in range(n)]
+        for e in ev_done + ev_out:
+            e.record(compute)
 
         def estep():
-            for i in range(len(layers)):
-                A_d[i].copy_(A_h[i], non_blocking=True)
+            for i in range(n):
+                s_in.wait_event(ev_done[i])          # A_d[i] is free once the last step's linear read it
+                with torch.cuda.stream(s_in):
+                    A_d[i].copy_(A_h[i], non_blocking=True)
+                ev_in[i].record(s_in)
+            for i in range(n):
+                compute.wait_event(ev_in[i])
+                compute.wait_event(ev_out[i])        # Y[i] is free once the last step's copy read it
                 F.fp8_linear_channelwise(A_d[i], Wq[i][0], Wq[i][1], out=Y[i], ws=ws)
-                Y_h[i].copy_(Y[i], non_blocking=True)
+                ev_done[i].record(compute)
+                s_out.wait_event(ev_done[i])
+                with torch.cuda.stream(s_out):
+                    Y_h[i].copy_(Y[i], non_blocking=True)
+                ev_out[i].record(s_out)
+            for i in range(n):
+                compute.wait_event(ev_out[i])        # the step ends when its results are on the host
 
         te = max_over_ranks(torch, time_loop(torch, estep, max(3, args.steps // 4), 2), world, dev)
         e2e = {"value": round(replica_rate(total_flops, world, te) / 1e12, 2), "unit": "TFLOP/s",
