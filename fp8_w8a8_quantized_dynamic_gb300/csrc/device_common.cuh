@@ -209,6 +209,101 @@ __device__ __forceinline__ uint2 quant8_bf16(uint4 v, const Quantizer& q) {
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
 
+// ---------------------------------------------------------------------------
+// Exact quotient without division: fl32(x / s) for every x, no refusals, no branches.
+//
+// With r = fl32(1/s) (correctly rounded reciprocal) and its tail r_lo = fl32(fl32(1 - s*r) * r)
+// (1 - s*r is exact in one fma), q0 = fl32(x*r + fl32(x*r_lo)) approximates x/s to about
+// 2^-46 relative, so q0 is faithful (within one ulp of x/s). The residual x - s*q0 of a
+// faithful quotient is exactly representable (one fma computes it exactly), and by
+// Markstein's theorem (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990) q = fl32(q0 + (x - s*q0) * r) is the
+// correctly rounded quotient fl32(x / s). Conditions: no underflow in the residual and no
+// overflow, which hold for s in [2^-80, 2^100] and quotients of magnitude >= 2^-20; smaller
+// quotients may be off in their last bits but stay far below the smallest FP8 rounding
+// boundary (2^-17), so the FP8 code is still exact. Checked on a GB300 against IEEE division
+// over all finite bf16 x for 27264 scales in that range: equal quotients for |x/s| >= 2^-20,
+// equal e4m3 and e5m2 codes everywhere.
+//
+// Two values travel as one 64-bit register pair through the packed f32x2 multiply and fma
+// (sm_100 family): four codes take four unpacks, eight packed arithmetic ops, two
+// conversions, one byte permute and one select. Signs come from the inputs (x = -0 gives
+// q = +0 in the fma chain; the code must still be 0x80). Non-finite x, or |x/s| beyond
+// fp32, give a NaN code (0x7F in magnitude for e4m3, >= 0x7C for e5m2), which no finite
+// in-range quotient produces: callers that may see such inputs check for it.
+struct ExactScale {
+  uint64_t r2, r_lo2, neg_s2;  // (r, r), (r_lo, r_lo), (-s, -s)
+  bool fast;                   // s in [2^-80, 2^100]
+};
+
+__device__ __forceinline__ uint64_t pack_f32x2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ ExactScale make_exact_scale(float s) {
+  ExactScale k;
+  const float r = __frcp_rn(s);
+  const float r_lo = fmaf(-s, r, 1.0f) * r;
+  k.r2 = pack_f32x2(r, r);
+  k.r_lo2 = pack_f32x2(r_lo, r_lo);
+  k.neg_s2 = pack_f32x2(-s, -s);
+  k.fast = s >= 0x1p-80f && s <= 0x1p100f;
+  return k;
+}
+
+// fl32(x / s) for the two bf16 values of a word, as a packed pair (low half first).
+__device__ __forceinline__ uint64_t exact_quotient2(uint32_t w, const ExactScale& k) {
+  const uint64_t x = pack_f32x2(bf16_lo(w), bf16_hi(w));
+  const uint64_t q0 = fma_f32x2(x, k.r2, mul_f32x2(x, k.r_lo2));
+  return fma_f32x2(fma_f32x2(k.neg_s2, q0, x), k.r2, q0);
+}
+
+// Two packed quotient pairs -> four FP8 codes of format F, the first value in the lowest byte.
+template <int F>
+__device__ __forceinline__ uint32_t cvt_fp8x4(uint64_t p01, uint64_t p23) {
+  uint32_t d;
+  if constexpr (F == kFmtE5M2)
+    asm("{\n .reg .b16 l, h;\n .reg .f32 a, b, c, e;\n mov.b64 {a, b}, %1;\n mov.b64 {c, e}, %2;\n"
+        " cvt.rn.satfinite.e5m2x2.f32 l, b, a;\n cvt.rn.satfinite.e5m2x2.f32 h, e, c;\n mov.b32 %0, {l, h};\n}"
+        : "=r"(d) : "l"(p01), "l"(p23));
+  else
+    asm("{\n .reg .b16 l, h;\n .reg .f32 a, b, c, e;\n mov.b64 {a, b}, %1;\n mov.b64 {c, e}, %2;\n"
+        " cvt.rn.satfinite.e4m3x2.f32 l, b, a;\n cvt.rn.satfinite.e4m3x2.f32 h, e, c;\n mov.b32 %0, {l, h};\n}"
+        : "=r"(d) : "l"(p01), "l"(p23));
+  return d;
+}
+
+// Four bf16 (two words) -> four FP8 codes; magnitudes from the exact quotients, signs from x.
+template <int F>
+__device__ __forceinline__ uint32_t exact_codes4(uint32_t w0, uint32_t w1, const ExactScale& k) {
+  const uint32_t c = cvt_fp8x4<F>(exact_quotient2(w0, k), exact_quotient2(w1, k));
+  return (c & 0x7F7F7F7Fu) | (__byte_perm(w0, w1, 0x7531) & 0x80808080u);
+}
+
+// Eight bf16 (a uint4) -> eight FP8 codes.
+template <int F>
+__device__ __forceinline__ uint2 exact_codes8(uint4 v, const ExactScale& k) {
+  return make_uint2(exact_codes4<F>(v.x, v.y, k), exact_codes4<F>(v.z, v.w, k));
+}
+
+// Non-zero when a code word holds a NaN code (from a non-finite x or an fp32 overflow of x/s).
+template <int F>
+__device__ __forceinline__ uint32_t nan_code_bits(uint32_t c) {
+  return ((c & 0x7F7F7F7Fu) + (F == kFmtE5M2 ? 0x04040404u : 0x01010101u)) & 0x80808080u;
+}
+
 // scale = amax / 448 (57344 for e5m2) by IEEE fp32 division; 1 when amax is 0 (or the
 // quotient underflows).
 template <int F>

@@ -108,9 +108,49 @@ __device__ __forceinline__ uint4 quant16_row(const uint16_t* __restrict__ src, i
   return out;
 }
 
+// Sixteen values of one row starting at column c (c + 16 <= cols, 16-byte aligned source) by
+// the exact quotient. kCheck: the scale does not bound the inputs (a caller-supplied scale),
+// so a NaN code (non-finite x, or x / s beyond fp32) sends the unit to quant16_row, which
+// saturates or keeps the NaN as the definition says.
+template <int F, bool kCheck>
+__device__ __forceinline__ uint4 quant16_exact(const uint16_t* __restrict__ src, const ExactScale& k, float s) {
+  const uint4 v0 = ld_v4(src), v1 = ld_v4(src + 8);
+  uint4 o = make_uint4(exact_codes4<F>(v0.x, v0.y, k), exact_codes4<F>(v0.z, v0.w, k),
+                       exact_codes4<F>(v1.x, v1.y, k), exact_codes4<F>(v1.z, v1.w, k));
+  if (kCheck && (nan_code_bits<F>(o.x) | nan_code_bits<F>(o.y) | nan_code_bits<F>(o.z) | nan_code_bits<F>(o.w)))
+    o = quant16_row<F>(src, 0, 16, true, make_quantizer(s));
+  return o;
+}
+
 // q[r, 0:ldq) = fp8(A[r, 0:cols) / s) with zero bytes for columns >= cols. Dynamic scale
 // (partials != null): s = scale_from_amax(max of the n_partials partials). Static scale
 // (partials == null): s = *s_static. CTA 0 stores s to *s_out unless s_out is null.
+// For s in the exact quotient's range every 16-byte unit is quantized branch-free, the flat
+// loop when both matrices are gap-free (ld == ldq == cols); ragged row ends, unaligned rows
+// and scales outside that range take quant16_row (bracket, then division).
+template <typename Idx, int F, bool kCheck>
+__device__ __forceinline__ void cast_rows(const uint16_t* __restrict__ a, int64_t rows, int64_t cols, int64_t ld,
+                                          int vec, float sc, uint8_t* __restrict__ q, int64_t ldq) {
+  const ExactScale k = make_exact_scale(sc);
+  const Idx upr = static_cast<Idx>(ldq >> 4);  // 16-byte output units per row
+  const Idx units = static_cast<Idx>(rows) * upr;
+  const Idx stride = static_cast<Idx>(gridDim.x) * blockDim.x;
+  const Idx first = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (k.fast && vec && ld == cols && ldq == cols) {
+    uint4* dst = reinterpret_cast<uint4*>(q);
+    for (Idx u = first; u < units; u += stride) dst[u] = quant16_exact<F, kCheck>(a + (int64_t(u) << 4), k, sc);
+    return;
+  }
+  for (Idx u = first; u < units; u += stride) {
+    const Idx r = u / upr;
+    const int64_t c = static_cast<int64_t>(u - r * upr) << 4;
+    const uint16_t* src = a + (int64_t)r * ld + c;
+    *reinterpret_cast<uint4*>(q + (int64_t)r * ldq + c) =
+        k.fast && vec && c + 16 <= cols ? quant16_exact<F, kCheck>(src, k, sc)
+                                        : quant16_row<F>(src, c, cols, vec != 0, make_quantizer(sc));
+  }
+}
+
 template <typename Idx, int F>
 __global__ void __launch_bounds__(kQuantThreads)
 cast_kernel(const uint16_t* __restrict__ a, int64_t rows, int64_t cols, int64_t ld, int vec,
@@ -121,32 +161,12 @@ cast_kernel(const uint16_t* __restrict__ a, int64_t rows, int64_t cols, int64_t 
   pdl_wait();
   const float sc = partials ? scale_from_amax<F>(block_max_partials(partials, n_partials, red)) : *s_static;
   if (s_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *s_out = sc;
-  const Quantizer s = make_quantizer(sc);
-  const Idx upr = static_cast<Idx>(ldq >> 4);  // 16-byte output units per row
-  const Idx units = static_cast<Idx>(rows) * upr;
-  const Idx stride = static_cast<Idx>(gridDim.x) * blockDim.x;
-  // two units per thread per round, all four 16-byte loads issued before any arithmetic: the
-  // loop is bound by loads in flight and instruction issue, not by HBM
-  for (Idx u0 = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x; u0 < units; u0 += 2 * stride) {
-    const Idx u1 = u0 + stride < units ? u0 + stride : u0;
-    const Idx r0 = u0 / upr, r1 = u1 / upr;
-    const int64_t c0 = static_cast<int64_t>(u0 - r0 * upr) << 4, c1 = static_cast<int64_t>(u1 - r1 * upr) << 4;
-    const uint16_t* s0 = a + (int64_t)r0 * ld + c0;
-    const uint16_t* s1 = a + (int64_t)r1 * ld + c1;
-    uint4 o0, o1;
-    if (vec && c0 + 16 <= cols && c1 + 16 <= cols) {
-      const uint4 v0 = ld_v4(s0), v1 = ld_v4(s0 + 8), v2 = ld_v4(s1), v3 = ld_v4(s1 + 8);
-      const uint2 q0 = quant8_bf16_pairwise<F>(v0, s), q1 = quant8_bf16_pairwise<F>(v1, s);
-      const uint2 q2 = quant8_bf16_pairwise<F>(v2, s), q3 = quant8_bf16_pairwise<F>(v3, s);
-      o0 = make_uint4(q0.x, q0.y, q1.x, q1.y);
-      o1 = make_uint4(q2.x, q2.y, q3.x, q3.y);
-    } else {
-      o0 = quant16_row<F>(s0, c0, cols, vec != 0, s);
-      o1 = quant16_row<F>(s1, c1, cols, vec != 0, s);
-    }
-    *reinterpret_cast<uint4*>(q + (int64_t)r0 * ldq + c0) = o0;
-    if (u1 != u0) *reinterpret_cast<uint4*>(q + (int64_t)r1 * ldq + c1) = o1;
-  }
+  // a dynamic scale bounds every |x| by amax, so x / s <= ~448 and no input is non-finite
+  // (a non-finite amax gives a scale outside the exact range)
+  if (partials)
+    cast_rows<Idx, F, false>(a, rows, cols, ld, vec, sc, q, ldq);
+  else
+    cast_rows<Idx, F, true>(a, rows, cols, ld, vec, sc, q, ldq);
 }
 
 // Per-row (output channel) weight quantization: CTA per row, s_w[r] = amax(W[r,:]) / 448
@@ -174,9 +194,12 @@ quantize_rows_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t K, int64
       s_w[r] = s_sh;
     }
     __syncthreads();
-    const Quantizer s = make_quantizer(s_sh);
+    const float sr = s_sh;
+    const ExactScale k = make_exact_scale(sr);  // |W[r, :]| <= amax: no input check needed
     for (int64_t c = (int64_t)threadIdx.x << 4; c < ldq; c += (int64_t)blockDim.x << 4)
-      *reinterpret_cast<uint4*>(q + r * ldq + c) = quant16_row<F>(row + c, c, K, vec != 0, s);
+      *reinterpret_cast<uint4*>(q + r * ldq + c) = k.fast && vec && c + 16 <= K
+                                                       ? quant16_exact<F, false>(row + c, k, sr)
+                                                       : quant16_row<F>(row + c, c, K, vec != 0, make_quantizer(sr));
     __syncthreads();  // s_sh and red are reused by the next row
   }
 }

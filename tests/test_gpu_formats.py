@@ -97,6 +97,49 @@ def test_static_scale_all_bf16_values():
             assert_codes_equal(qa, q_ref, 255, f"static {fmt} s={s:g} over all bf16")
 
 
+def flat_rows(v: torch.Tensor, width: int = 256) -> torch.Tensor:
+    """v padded with zeros into rows of `width` (a multiple of 16: ld == ldq == K, the
+    gap-free layout the cast kernel streams without row arithmetic)."""
+    return torch.cat([v, torch.zeros((-v.numel()) % width, dtype=torch.bfloat16)]).view(-1, width)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_static_scale_all_bf16_values_flat_rows(fmt):
+    """Every finite bf16 value and +-inf in gap-free 256-wide rows, at scales inside, on the
+    edges of and just outside the range where the cast computes x / s without division
+    ([2^-80, 2^100]): codes bit-exact. The infinities and quotients beyond fp32 leave the
+    branch-free path through its NaN-code check and saturate."""
+    x = torch.cat([all_finite_bf16(), torch.tensor([float("inf"), float("-inf")], dtype=torch.bfloat16)])
+    a = flat_rows(x)
+    for s in (1.0, 2.0 ** -80, 2.0 ** -81, 2.0 ** 100, 2.0 ** 101, 3.7e-3, 1.1e17, 1e-30, 3.375 / 448, 0.5 / 448):
+        s = float(np.float32(s))
+        qa, _ = F.fp8_quantize_act_ex(a.to(DEV), fmt, s_static=dev_scalar(s))
+        torch.cuda.synchronize()
+        q_ref, _ = oracle_act(a, fmt=fmt, s_static=s)
+        assert_codes_equal(qa, q_ref, 256, f"static {fmt} s={s:g} over all bf16, flat rows")
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_dynamic_all_bf16_values_flat_rows(fmt):
+    """Every finite bf16 value up to an amax, in gap-free rows, for amax values whose scale
+    amax / max has few significant bits (mantissa a multiple of 7, or of 27, or a power of
+    two: many quotients sit exactly on FP8 rounding midpoints) and random ones: dynamic codes
+    and scale bit-exact."""
+    x = all_finite_bf16()
+    g = np.random.default_rng(122)
+    targets = [float(v) for v in np.abs(g.standard_normal(8)) * np.exp2(g.integers(-30, 30, 8))]
+    targets += [3.5, 3.375, 4.0, 7.0 * 2.0 ** -12, 27.0 * 2.0 ** 9, 1.0, O.fp8_max(fmt), 2.0 ** 70]
+    for T in targets:
+        T = abs(float(torch.tensor(T).bfloat16().float()))
+        v = x[x.float().abs() <= T]
+        a = flat_rows(torch.cat([v, torch.tensor([T, -T], dtype=torch.bfloat16)]))
+        qa, s_a = F.fp8_quantize_act_ex(a.to(DEV), fmt)
+        torch.cuda.synchronize()
+        q_ref, s_ref = oracle_act(a, fmt=fmt)
+        assert_scale_equal(s_a, s_ref, f"dynamic {fmt} amax {T:g}")
+        assert_codes_equal(qa, q_ref, 256, f"dynamic {fmt} amax {T:g}, flat rows")
+
+
 # --------------------------------------------------------------------------- linear
 
 def run_ex(a_cpu, w_cpu, fmt_a, fmt_w, per_channel, bias_cpu=None, s_static=None, check_w=True):
