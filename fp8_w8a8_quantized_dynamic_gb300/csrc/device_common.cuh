@@ -304,6 +304,24 @@ __device__ __forceinline__ uint32_t nan_code_bits(uint32_t c) {
   return ((c & 0x7F7F7F7Fu) + (F == kFmtE5M2 ? 0x04040404u : 0x01010101u)) & 0x80808080u;
 }
 
+// Eight values through the bracket-and-division path, out of line (rare callers).
+template <int F>
+__device__ __noinline__ uint2 quant8_bf16_slow(uint4 v, float s) {
+  return quant8_bf16<F>(v, make_quantizer(s));
+}
+
+// Eight bf16 -> eight FP8 codes of fl32(x / s) for any s: the exact quotient when s is in its
+// range, else (or when `check` and a NaN code shows a non-finite x or an overflowing quotient)
+// the division path.
+template <int F>
+__device__ __forceinline__ uint2 quant8_exact(uint4 v, const ExactScale& k, float s, bool check) {
+  if (k.fast) {
+    const uint2 q = exact_codes8<F>(v, k);
+    if (!check || (nan_code_bits<F>(q.x) | nan_code_bits<F>(q.y)) == 0) return q;
+  }
+  return quant8_bf16_slow<F>(v, s);
+}
+
 // scale = amax / 448 (57344 for e5m2) by IEEE fp32 division; 1 when amax is 0 (or the
 // quotient underflows).
 template <int F>

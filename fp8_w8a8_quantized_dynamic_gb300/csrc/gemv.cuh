@@ -197,13 +197,10 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
   __shared__ float s_a_out;
   __shared__ float slice_amax;
   __shared__ float red[kConsumerWarps];
-  __shared__ int n_exact;                 // units queued for exact division
-  __shared__ int exact_units[kExactSlots];
   if (warp == kConsumerWarps && lane == 0)  // fetch the descriptor while the barriers are set up
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    n_exact = 0;
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, kConsumerWarps);
@@ -299,9 +296,9 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
           }
           s_a = scale_from_amax<FA>(amax);
         }
-        const Quantizer qz = make_quantizer(s_a);
-        // quantize the slice: kQuantUnroll units per thread per round, fast codes of all of
-        // them first (independent, branch-free), exact division only for flagged units
+        const ExactScale kq = make_exact_scale(s_a);
+        const bool check = p.s_static != nullptr;  // a given scale does not bound the inputs
+        // quantize the slice: kQuantUnroll units per thread per round, all loads first
         const int upt = span >> 3;  // 8-element units per token of this rank's slice
         const int total = p.M * upt;
         const float inv_upt = 1.0f / float(upt);  // unit -> token by float: exact for these sizes
@@ -318,39 +315,12 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
             x[j] = inside[j] ? lds_v4(scratch + uint32_t(m * rowlen + (full ? k0 : 0) + kk) * 2u)
                              : make_uint4(0, 0, 0, 0);
           }
-          uint2 q[kQuantUnroll];
-          uint32_t bad[kQuantUnroll];
-#pragma unroll
-          for (int j = 0; j < kQuantUnroll; ++j) q[j] = quant8_bf16_try<FA>(x[j], qz, bad[j]);
 #pragma unroll
           for (int j = 0; j < kQuantUnroll; ++j) {
-            if (!inside[j]) {
-              q[j] = make_uint2(0, 0);
-            } else if (bad[j]) {
-              // a value next to a rounding boundary: queue the unit for the division pass below
-              // (one divergent division per warp round would stall all of its lanes)
-              const int slot = atomicAdd(&n_exact, 1);
-              if (slot < kExactSlots) {
-                exact_units[slot] = i0 + j * kConsumerThreads;
-                continue;
-              }
-              q[j] = quant8_bf16_fix<FA>(x[j], q[j], bad[j], qz.s, qz.r);
-            }
+            const uint2 q = inside[j] ? quant8_exact<FA>(x[j], kq, s_a, check) : make_uint2(0, 0);
             if (i0 + j * kConsumerThreads < total)
-              asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(dst[j]), "r"(q[j].x), "r"(q[j].y) : "memory");
+              asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(dst[j]), "r"(q.x), "r"(q.y) : "memory");
           }
-        }
-        consumer_bar_sync();  // the queue is complete
-        const int n_queued = min(n_exact, kExactSlots);
-        for (int e = threadIdx.x; e < n_queued; e += kConsumerThreads) {
-          const int i = exact_units[e];
-          const int m = int((float(i) + 0.5f) * inv_upt), kk = (i - m * upt) << 3;
-          const uint4 xe = lds_v4(scratch + uint32_t(m * rowlen + (full ? k0 : 0) + kk) * 2u);
-          uint32_t bad_e;
-          const uint2 qf = quant8_bf16_try<FA>(xe, qz, bad_e);
-          const uint2 qe = quant8_bf16_fix<FA>(xe, qf, bad_e, qz.s, qz.r);
-          asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(act + m * p.act_stride + kk), "r"(qe.x), "r"(qe.y)
-                       : "memory");
         }
       } else {
         const int upt = span >> 3;  // 8-element units per token of this rank's slice
@@ -398,12 +368,13 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
           }
           s_a = scale_from_amax<FA>(amax);
         }
-        const Quantizer qz = make_quantizer(s_a);
+        const ExactScale kq = make_exact_scale(s_a);
+        const bool check = p.s_static != nullptr;
         // quantize into act[token][k - k0]; units past K and tokens past M are plain zeros
         auto put = [&](int i, const uint4& x) {
           const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
           uint2 q = make_uint2(0, 0);
-          if (k0 + kk < p.K) q = quant8_bf16<FA>(x, qz);
+          if (k0 + kk < p.K) q = quant8_exact<FA>(x, kq, s_a, check);
           asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(act + m * p.act_stride + kk), "r"(q.x), "r"(q.y)
                        : "memory");
         };

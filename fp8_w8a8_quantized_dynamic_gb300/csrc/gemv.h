@@ -27,7 +27,6 @@ constexpr int kMaxSlice = 4096;                       // bytes of K per rank
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kRegUnits = 8;  // 8-element units of A a consumer thread keeps in registers
 constexpr int kQuantUnroll = 4;  // units a consumer thread quantizes per round (independent chains)
-constexpr int kExactSlots = 512;  // units next to a rounding boundary queued for the division pass
 constexpr int kMaxSliceBf16 = 4096;  // K elements per rank with bf16 activations (smem permitting)
 
 // Activation modes of the kernel.
