@@ -25,6 +25,14 @@
 // Ragged M, N and K need no padding: TMA fills out-of-range rows/columns with zeros and
 // the epilogue predicates its stores.
 //
+// Paired mode (kPair, a cluster of two CTAs on row blocks 2i and 2i+1 of the same column
+// tile): the 256-row weight tile is shared. Each CTA loads its own qA tile and one half of
+// the weight tile, the half multicast into both CTAs' shared memory, so the L2 -> SM traffic
+// per tile drops from 48 KB to 32 KB per stage (the single-CTA kernel reads ~19 TB/s from
+// L2 at 73 % of its request peak). Each stage's empty barrier then counts the MMA commits of
+// both CTAs (a CTA's multicast half overwrites the peer's stage too), and the two CTAs run
+// the same tile sequence with the same number of k-blocks.
+//
 // Every wait is bounded (2 s); on expiry the kernel records an error for the host, drains
 // its own outstanding copies and MMAs (again bounded), frees its TMEM and returns.
 
@@ -33,6 +41,10 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <map>
+#include <mutex>
 
 #include "device_common.cuh"
 #include "gemm_tcgen05.h"
@@ -120,6 +132,34 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
 }
 
+// Multicast forms for the paired mode: the copy lands at the same shared-memory offset in
+// every CTA of `mask` and completes bytes on the mbarrier at the same offset in each; the
+// commit arrives once on that mbarrier in each CTA of `mask`.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%3, %4}], [%2], %5;"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask) : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+               :: "r"(bar), "h"(mask) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pair_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of both CTAs: barrier inits visible before the first multicast, and no CTA
+// leaves while its peer may still write into its shared memory or arrive on its barriers.
+__device__ __forceinline__ void pair_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tmem_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -155,8 +195,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // Tile order: groups of `group_n` column tiles; inside a group the column index runs fastest,
 // so the CTAs resident at one time share a few qA row blocks and a W slice that stays in L2
 // while the group sweeps all rows: W is read from HBM once, qA once per group.
-__device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& m_idx, int& n_idx) {
-  const int per_group = p.group_n * p.m_tiles;
+__device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int m_units, int& m_idx, int& n_idx) {
+  const int per_group = p.group_n * m_units;
   const int gidx = tile / per_group;
   const int r = tile - gidx * per_group;
   const int n_first = gidx * p.group_n;
@@ -165,8 +205,9 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& 
   n_idx = n_first + (r - m_idx * gn);
 }
 
-// kBf16: operands are bf16 (weight-only product) instead of FP8.
-template <bool kBf16>
+// kBf16: operands are bf16 (weight-only product) instead of FP8. kPair: clusters of two CTAs
+// sharing the weight tile (see the paired mode above).
+template <bool kBf16, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
             const __grid_constant__ GemmParams p) {
@@ -180,7 +221,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   auto b_stage = [&](int s) { return smem_base + s * kStageBytes + kABytes; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_tiles = p.m_tiles * p.n_tiles;
+  // work units: tiles, or (paired) vertical tile pairs; rank r of a pair takes row block 2i + r
+  const uint32_t rank = kPair ? pair_rank() : 0u;
+  const int m_units = kPair ? (p.m_tiles + 1) / 2 : p.m_tiles;
+  const int num_tiles = m_units * p.n_tiles;
+  const int first_unit = kPair ? int(blockIdx.x >> 1) : int(blockIdx.x);
+  const int unit_stride = kPair ? int(gridDim.x >> 1) : int(gridDim.x);
+  auto coords = [&](int unit, int& m_idx, int& n_idx) {
+    tile_coords(unit, p, m_units, m_idx, n_idx);
+    if (kPair) m_idx = 2 * m_idx + int(rank);
+  };
   const int num_kb = (p.K + kElemsPerStage - 1) / kElemsPerStage;
   volatile int* abort_flag = &ctl->abort_flag;
 
@@ -189,7 +239,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
-      mbar_init(smem_u32(&ctl->empty[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), kPair ? 2 : 1);  // paired: both CTAs' MMAs read the stage
     }
     for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(smem_u32(&ctl->tfull[b]), 1);
@@ -207,6 +257,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   }
   tmem_fence_before();
   __syncthreads();
+  if (kPair) pair_sync();  // the peer's barriers exist before the first multicast lands there
   tmem_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
 
@@ -218,9 +269,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       // ---------------- TMA producer ----------------
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int tile = first_unit; tile < num_tiles && ok; tile += unit_stride) {
         int m_idx, n_idx;
-        tile_coords(tile, p, m_idx, n_idx);
+        coords(tile, m_idx, n_idx);
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
@@ -228,7 +279,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
           const uint32_t fb = smem_u32(&ctl->full[s]);
           mbar_arrive_expect_tx(fb, kStageBytes);
           tma_load_2d(a_stage(s), &tmap_a, fb, kb * kElemsPerStage, m_idx * BM);
-          tma_load_2d(b_stage(s), &tmap_b, fb, kb * kElemsPerStage, n_idx * BN);
+          if (kPair)  // this CTA's half of the weight tile, into both CTAs
+            tma_load_2d_mc(b_stage(s) + rank * (kBBytes / 2), &tmap_b, fb, kb * kElemsPerStage,
+                           n_idx * BN + int(rank) * (BN / 2), uint16_t(0x3));
+          else
+            tma_load_2d(b_stage(s), &tmap_b, fb, kb * kElemsPerStage, n_idx * BN);
         }
       }
       if (!ok) {
@@ -243,7 +298,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       // ---------------- MMA issuer ----------------
       uint32_t it = 0, acc_it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++acc_it) {
+      for (int tile = first_unit; tile < num_tiles && ok; tile += unit_stride, ++acc_it) {
         const int ab = acc_it % kAccBufs;
         const uint32_t aph = (acc_it / kAccBufs) & 1u;
         if (!mbar_wait_bounded(smem_u32(&ctl->tempty[ab]), aph ^ 1u, abort_flag, &g_gemm_error)) { ok = false; break; }
@@ -262,7 +317,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             mma_issue<kBf16>(d_tmem, adesc + uint64_t(kk * kMmaK >> 4), bdesc + uint64_t(kk * kMmaK >> 4),
                              p.idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          mma_commit(smem_u32(&ctl->empty[s]));  // frees the stage once these MMAs have read it
+          // frees the stage once these MMAs have read it (in both CTAs' counts when paired)
+          if (kPair)
+            mma_commit_mc(smem_u32(&ctl->empty[s]), uint16_t(0x3));
+          else
+            mma_commit(smem_u32(&ctl->empty[s]));
         }
         if (!ok) break;
         mma_commit(smem_u32(&ctl->tfull[ab]));   // accumulator ready for the epilogue
@@ -278,9 +337,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     const int et = threadIdx.x - 64;           // 0..127
     const float s_a = p.s_a ? *p.s_a : 1.0f;
     uint32_t acc_it = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++acc_it) {
+    for (int tile = first_unit; tile < num_tiles; tile += unit_stride, ++acc_it) {
       int m_idx, n_idx;
-      tile_coords(tile, p, m_idx, n_idx);
+      coords(tile, m_idx, n_idx);
       const int ab = acc_it % kAccBufs;
       const uint32_t aph = (acc_it / kAccBufs) & 1u;
       // column scales/bias of this tile, double-buffered by accumulator: a warp can only
@@ -346,6 +405,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   __syncwarp();
   tmem_fence_before();
   __syncthreads();
+  if (kPair) pair_sync();  // the peer's last multicast copies and commit arrivals are done
   tmem_fence_after();
   if (warp == 1) {
     __syncwarp();
@@ -404,21 +464,57 @@ bool make_fp8_tensor_map(CUtensorMap* map, const uint8_t* base, int64_t rows, in
 
 namespace {
 
-// Shared launch: operands are FP8 (ld in bytes) or bf16 (ld in bytes as well).
-int launch_gemm(bool bf16, const void* a, int64_t lda_bytes, const float* s_a, const void* w, int64_t ldw_bytes,
+// Resident clusters of two for the paired kernel (cached per kernel): clusters must fit in
+// one GPC, so GPCs with an odd number of free SMs leave one SM out.
+int pair_clusters(const void* kernel, cudaLaunchConfig_t cfg) {
+  static std::mutex mu;
+  static std::map<const void*, int> cache;
+  std::lock_guard<std::mutex> g(mu);
+  auto it = cache.find(kernel);
+  if (it != cache.end()) return it->second;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(2 * 64);  // any multiple of the cluster size
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  if (std::getenv("FP8W8A8_DEBUG")) std::fprintf(stderr, "fp8w8a8: gemm pairs resident: %d clusters of 2\n", n);
+  cache[kernel] = n;
+  return n;
+}
+
+// Paired (cluster) mode unless FP8W8A8_GEMM_PAIR=0, there is only one row block, or fewer
+// than 3/4 of the SMs could run pairs.
+bool pair_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("FP8W8A8_GEMM_PAIR");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
+template <bool kBf16>
+int launch_kind(const void* a, int64_t lda_bytes, const float* s_a, const void* w, int64_t ldw_bytes,
                 const float* s_w, int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy, int M, int N,
                 int K, uint32_t idesc, int num_sms, cudaStream_t stream) {
   using namespace gemm;
-  auto kernel = bf16 ? gemm_kernel<true> : gemm_kernel<false>;
-  static bool attr_done[2] = {false, false};  // the attribute is per function, set once per process
-  if (!attr_done[bf16]) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes)) != cudaSuccess)
+  auto single = gemm_kernel<kBf16, false>;
+  auto paired = gemm_kernel<kBf16, true>;
+  static bool attr_done = false;  // the attribute is per function, set once per process
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(single, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(paired, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(paired, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess)
       return 1;
-    attr_done[bf16] = true;
+    attr_done = true;
   }
-  CUtensorMap ma, mb;
-  if (!make_tensor_map(&ma, a, bf16, M, K, lda_bytes, BM) || !make_tensor_map(&mb, w, bf16, N, K, ldw_bytes, BN))
-    return 2;
 
   GemmParams p;
   p.M = M;
@@ -432,27 +528,59 @@ int launch_gemm(bool bf16, const void* a, int64_t lda_bytes, const float* s_a, c
   p.ldy = ldy;
   p.m_tiles = (M + BM - 1) / BM;
   p.n_tiles = (N + BN - 1) / BN;
+  p.y_vec = (ldy % 8 == 0) && (reinterpret_cast<uintptr_t>(y) % 16 == 0);
+  p.idesc = idesc;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  int clusters = 0;
+  if (pair_enabled() && p.m_tiles >= 2) {
+    clusters = pair_clusters(reinterpret_cast<const void*>(paired), cfg);
+    if (2 * clusters < (3 * num_sms) / 4) clusters = 0;
+  }
+  const bool pair = clusters > 0;
+  const int m_units = pair ? (p.m_tiles + 1) / 2 : p.m_tiles;
   // raster: a group of column tiles whose W slice (~26 MB) stays hot in L2 while the group
   // sweeps all rows; qA is then read once per group. Larger hot sets were measured to be
   // evicted by the streaming qA and Y traffic.
   const int64_t slice_budget = int64_t(26) << 20;
   const int64_t w_tile_bytes = int64_t(BN) * ldw_bytes;
   p.group_n = int(std::max<int64_t>(1, std::min<int64_t>(p.n_tiles, slice_budget / w_tile_bytes)));
-  p.y_vec = (ldy % 8 == 0) && (reinterpret_cast<uintptr_t>(y) % 16 == 0);
-  p.idesc = idesc;
 
-  const int tiles = p.m_tiles * p.n_tiles;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(tiles < num_sms ? tiles : num_sms);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  CUtensorMap ma, mb;
+  if (!make_tensor_map(&ma, a, kBf16, M, K, lda_bytes, BM) ||
+      !make_tensor_map(&mb, w, kBf16, N, K, ldw_bytes, pair ? BN / 2 : BN))
+    return 2;
+
+  const int units = m_units * p.n_tiles;
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
+  if (pair) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+    cfg.gridDim = dim3(2 * unsigned(std::min(units, clusters)));
+    return cudaLaunchKernelEx(&cfg, paired, ma, mb, p) == cudaSuccess ? 0 : 3;
+  }
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, ma, mb, p) == cudaSuccess ? 0 : 3;
+  cfg.gridDim = dim3(units < num_sms ? units : num_sms);
+  return cudaLaunchKernelEx(&cfg, single, ma, mb, p) == cudaSuccess ? 0 : 3;
+}
+
+// Shared launch: operands are FP8 (ld in bytes) or bf16 (ld in bytes as well).
+int launch_gemm(bool bf16, const void* a, int64_t lda_bytes, const float* s_a, const void* w, int64_t ldw_bytes,
+                const float* s_w, int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy, int M, int N,
+                int K, uint32_t idesc, int num_sms, cudaStream_t stream) {
+  return bf16 ? launch_kind<true>(a, lda_bytes, s_a, w, ldw_bytes, s_w, per_channel, bias, y, ldy, M, N, K, idesc,
+                                  num_sms, stream)
+              : launch_kind<false>(a, lda_bytes, s_a, w, ldw_bytes, s_w, per_channel, bias, y, ldy, M, N, K, idesc,
+                                   num_sms, stream);
 }
 
 }  // namespace

@@ -19,6 +19,8 @@
 namespace fp8k {
 
 constexpr int kQuantThreads = 256;
+// Resident cast CTAs per SM the register budget must allow (loads in flight keep HBM busy).
+constexpr int kCastBlocksPerSM = 8;
 
 // Cached 16-byte load (the row is read again shortly after).
 __device__ __forceinline__ uint4 ld_v4(const void* p) {
@@ -152,7 +154,7 @@ __device__ __forceinline__ void cast_rows(const uint16_t* __restrict__ a, int64_
 }
 
 template <typename Idx, int F>
-__global__ void __launch_bounds__(kQuantThreads)
+__global__ void __launch_bounds__(kQuantThreads, kCastBlocksPerSM)
 cast_kernel(const uint16_t* __restrict__ a, int64_t rows, int64_t cols, int64_t ld, int vec,
             const float* __restrict__ partials, int n_partials, const float* __restrict__ s_static,
             float* __restrict__ s_out, uint8_t* __restrict__ q, int64_t ldq, int pdl) {
