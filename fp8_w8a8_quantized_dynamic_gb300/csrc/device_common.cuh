@@ -56,6 +56,9 @@ __device__ __forceinline__ uint32_t fp8x2_to_bf16x2(uint32_t codes) {
 }
 
 // Quantizer for one scale s: FP8 codes of fl32(x / s), most of the time without a division.
+// The kernels' main paths use the exact quotient further below; this bracket serves what
+// that form does not cover: scales outside [2^-80, 2^100], ragged row ends, and units whose
+// codes show a non-finite input under a caller-supplied scale.
 // With r = fl32(1/s), the products L = fl32(|x| * fl32(r * (1 - 2^-20))) and
 // H = fl32(x * fl32(r * (1 + 2^-20))) bracket the quotient strictly: each carries at most
 // four roundings of 2^-24 (relative) against a 2^-20 margin, so L < |fl32(x/s)| < |H|, and
