@@ -328,7 +328,7 @@ def run_ours(args, rank: int, world: int):
                     "traffic_note": "mean dram__bytes_read.sum + dram__bytes_write.sum per GEMM launch "
                                     "(ncu, profiles/gemm_tcgen05_dram_llama8b_m16384.json)",
                     "traffic_per_launch": traffic_per,
-                    "kernel": "gemm_kernel (tcgen05 kind::f8f6f4)",
+                    "kernel": "gemm_kernel (tcgen05 kind::f8f6f4; clusters of two CTAs sharing the weight tile by TMA multicast)",
                     "peak_source": f"{peak_src} bf16 burst x {NOMINAL_FP8_OVER_BF16} nominal fp8/bf16 ratio",
                     "per_layer_ms": {L.name: round(t, 4) for L, t in zip(layers, gemm_ms)}}
 
