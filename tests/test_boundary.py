@@ -183,3 +183,38 @@ def test_static_quantize_needs_no_workspace(L):
 def test_selftest_rejects_bad_limits(L):
     for limit in (-1, 0, 999, 10_000_000_001):
         assert L.fp8_selftest_timeout(limit, None) == F.FP8_ERR_INVALID_ARG
+
+
+def wo(L, a=P, M=4, K=64, lda=64, qw=P, fmt_w=0, N=32, ldqw=64, s_w=P, per_channel=0, bias=None, y=P, ldy=32,
+       ws=WS, ws_bytes=1 << 20):
+    return L.fp8_linear_weight_only(a, M, K, lda, qw, fmt_w, N, ldqw, s_w, per_channel, bias, y, ldy, ws, ws_bytes,
+                                    None)
+
+
+def test_weight_only_rejects_bad_arguments(L):
+    """fp8_linear_weight_only validates before any device work: formats, flags, pointers,
+    strides, alignment, and the workspace its GEMM path needs; empty shapes are no-ops."""
+    assert wo(L, fmt_w=2) == F.FP8_ERR_INVALID_ARG
+    assert wo(L, fmt_w=-1) == F.FP8_ERR_INVALID_ARG
+    assert wo(L, per_channel=2) == F.FP8_ERR_INVALID_ARG
+    assert wo(L, a=None) == F.FP8_ERR_INVALID_ARG
+    assert wo(L, qw=None) == F.FP8_ERR_INVALID_ARG
+    assert wo(L, y=None) == F.FP8_ERR_INVALID_ARG
+    assert wo(L, s_w=None) == F.FP8_ERR_INVALID_ARG
+    assert wo(L, lda=63) == F.FP8_ERR_INVALID_ARG                # lda < K
+    assert wo(L, ldy=31) == F.FP8_ERR_INVALID_ARG                # ldy < N
+    assert wo(L, ldqw=48) == F.FP8_ERR_INVALID_ARG               # ldqw < K
+    assert wo(L, K=60, lda=60, ldqw=72) == F.FP8_ERR_MISALIGNED  # FP8 ld not a multiple of 16
+    assert wo(L, qw=P + 8) == F.FP8_ERR_MISALIGNED
+    assert wo(L, a=P + 1) == F.FP8_ERR_MISALIGNED
+    assert wo(L, bias=P + 1) == F.FP8_ERR_MISALIGNED
+    # GEMM-path shapes hold the up-converted weights in the workspace
+    need = F.fp8_weight_only_workspace_bytes(64, 64, 32)
+    assert need > 0
+    assert wo(L, M=64, ws=None, ws_bytes=0) == F.FP8_ERR_WORKSPACE
+    assert wo(L, M=64, ws_bytes=need - 1) == F.FP8_ERR_WORKSPACE
+    assert wo(L, M=64, ws=WS + 16) == F.FP8_ERR_WORKSPACE        # not 256-byte aligned
+    # decode shapes need none, and empty shapes return before any CUDA call
+    assert F.fp8_weight_only_workspace_bytes(4, 4096, 4096) == 0
+    assert wo(L, M=0, a=None, y=None) == F.FP8_OK
+    assert wo(L, N=0, qw=None, s_w=None, ldy=1) == F.FP8_OK
