@@ -124,7 +124,7 @@ def test_gemm_strided_activations_and_output():
     linear_parity(ybig[:, :N], a, w, True, what="gemm odd ldy")
 
 
-@pytest.mark.parametrize("layer", [0, 3])
+@pytest.mark.parametrize("layer", [0, 1, 2, 3])
 def test_prefill_config_full_size_sampled(layer):
     """Llama-3-8B prefill layer at M = 16384, channelwise, as the benchmark runs it.
     qW/s_w bit-exact on sampled rows; Y on 40 sampled rows x 768 sampled columns."""
