@@ -15,10 +15,16 @@ Also reported on the same line:
             copy of A, fp8_linear_channelwise, device->host copy of Y, per layer;
   cpu_baseline  the CPU oracle on a bounded sample of the workload.
 
+  sweep     the TinyLlama-1.1B decoder-stack sweep (22 layers x 4 linears, both weight
+            modes, M from 1 to 16384): per-M time, TFLOP/s, weight-GB/s, roofline fraction;
+  crossover GEMV against GEMM at M around 16 on the Mistral-7B and TinyLlama linears;
+  unaligned weight-GB/s of the four shapes whose dimensions are not multiples of 16;
+  tiny      latency of the 16 x 256 x 256 linear.
+
 `--impl reference` times the CPU oracle alone on that bounded sample (rank 0 only).
-Multi-GPU (torchrun): every rank runs the same workload independently (replicas only;
-the layer does not shard across GPUs here) and value sums over ranks with the slowest
-rank's time.
+One GPU only: the library's pair GEMM uses cluster-scoped operations meant for a single
+device, and the path is not sharded, so a launch with more than one process (torchrun,
+WORLD_SIZE > 1) or --gpus > 1 prints an "unavailable" line and does no GPU work.
 """
 
 from __future__ import annotations
@@ -139,21 +145,6 @@ def flops(M, layers):
     return sum(2.0 * M * L.N * L.K for L in layers)
 
 
-def max_over_ranks(torch, ms: float, world: int, device=None) -> float:
-    """The slowest replica's time: the job is done when its last rank is (no-op at N = 1)."""
-    if world <= 1:
-        return ms
-    t = torch.tensor([ms], dtype=torch.float64, device=device)
-    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    return float(t.item())
-
-
-def replica_rate(work_per_rank: float, world: int, ms_max: float) -> float:
-    """Whole-job throughput of N independent replicas (weak scaling): all ranks' work over the
-    slowest rank's time, per second."""
-    return world * work_per_rank / (ms_max * 1e-3)
-
-
 def time_loop(torch, fn, steps: int, warmup: int):
     """Median-free timing: W warm-up calls, then K calls between two events (both synced)."""
     for _ in range(warmup):
@@ -248,27 +239,174 @@ def measure_variants(torch, F, I, args, dev, layers, names, host, A, Y, ws, M):
     return out
 
 
-def run_ours(args, rank: int, world: int):
+def roofline_time_s(M, K, N, per_channel, fp8_tflops, hbm_gbs):
+    """Roofline time of one linear: the slower of its FP8 flops at the compute peak and its
+    algorithmic bytes (A read, qW, scales, Y write) at the HBM rate."""
+    flop = 2.0 * M * N * K
+    byts = 2.0 * M * K + float(N) * K + (4.0 * N if per_channel else 4.0) + 2.0 * M * N
+    return max(flop / (fp8_tflops * 1e12), byts / (hbm_gbs * 1e9))
+
+
+def measure_sweep(torch, F, I, dev, args, fp8_tflops, hbm_gbs):
+    """TinyLlama-1.1B decoder stack: 22 layers x (qkv, o_proj, gate_up, down), 22 distinct
+    weight sets (969 MB of FP8 per mode, far above L2), both weight-scale modes, every M of the
+    workload; activations quantized per layer. One step = all 88 linears, CUDA graph replay."""
+    layers, depth = I.TINYLLAMA_LAYERS, I.TINYLLAMA_DEPTH
+    Ms = [m for m in I.TINYLLAMA_MS if m <= args.sweep_max_m]
+    W = {}
+    for mode in (False, True):
+        W[mode] = []
+        for d in range(depth):
+            row = []
+            for j in range(len(layers)):
+                w = I.tinyllama_weight_device(d, j, dev)
+                row.append(F.fp8_quantize_weight(w, per_channel=mode))
+                del w
+            W[mode].append(row)
+    copies = 2  # consecutive layers read different activation buffers
+    Mmax = max(Ms)
+    A = [[I.tinyllama_activations_device(Mmax, c, j, dev) for j in range(len(layers))] for c in range(copies)]
+    Y = [torch.empty((Mmax, L.N), dtype=torch.bfloat16, device=dev) for L in layers]
+    ws = torch.empty(max(1, max(F.fp8_workspace_bytes(Mmax, L.K, L.N) for L in layers)), dtype=torch.uint8,
+                     device=dev)
+    torch.cuda.synchronize()
+    wbytes = depth * sum(L.N * L.K for L in layers)
+    out = {}
+    for mode in (False, True):
+        fn = F.fp8_linear_channelwise if mode else F.fp8_linear
+        rows = []
+        for M in Ms:
+            def step(M=M):
+                for d in range(depth):
+                    for j in range(len(layers)):
+                        fn(A[d % copies][j][:M], W[mode][d][j][0], W[mode][d][j][1], out=Y[j][:M], ws=ws)
+
+            t = time_loop(torch, graph_of(torch, step).replay, max(3, min(args.steps, 10)), 2)
+            fl = depth * sum(2.0 * M * L.N * L.K for L in layers)
+            t_roof = depth * sum(roofline_time_s(M, L.K, L.N, mode, fp8_tflops, hbm_gbs) for L in layers)
+            rows.append({"M": M, "ms_per_stack": round(t, 4), "tflops": round(fl / (t * 1e-3) / 1e12, 1),
+                         "weight_gbs": round(wbytes / (t * 1e-3) / 1e9, 1),
+                         "roofline_frac": round(t_roof / (t * 1e-3), 4),
+                         "path": "gemv" if F.fp8_uses_gemv(M, layers[0].K, layers[0].N) else "gemm"})
+        out["channelwise" if mode else "per_tensor"] = rows
+    del W, A, Y, ws
+    torch.cuda.synchronize()
+    return {"workload": "TinyLlama-1.1B linears (qkv 2048->2560, o_proj 2048->2048, gate_up 2048->11264, "
+                        "down 5632->2048) x 22 distinct layers per step, activations ~N(0,1) quantized per layer "
+                        "(dynamic e4m3), weights ~N(0,0.02) drawn on the device (timing only)",
+            "timing": "CUDA graph replay of the 88 linears; roofline_frac = sum of per-linear roofline times "
+                      "(max of 2MNK / FP8 peak and algorithmic bytes / HBM) over the measured time",
+            "weight_mb_per_mode": round(wbytes / 1e6, 1), "by_mode": out}
+
+
+def measure_crossover(torch, F, I, dev, args):
+    """GEMV against GEMM for the same calls at M around the threshold: Mistral-7B decode
+    linears (three weight copies rotated past L2) and the TinyLlama linears (22 layers)."""
+    res = {}
+    prev = F.fp8_set_gemv_max_m(-1)
+    fams = {"mistral7b": (I.LLAMA8B_LAYERS, [[F.fp8_quantize_weight(I.decode_weight(i, c).to(dev))
+                                               for i in range(4)] for c in range(3)]),
+            "tinyllama": (I.TINYLLAMA_LAYERS, [[F.fp8_quantize_weight(I.tinyllama_weight_device(d, j, dev))
+                                                for j in range(4)] for d in range(I.TINYLLAMA_DEPTH)])}
+    Ms = (8, 12, 15, 16, 17, 24, 32)
+    try:
+        for fam, (layers, Wq) in fams.items():
+            Kmax = max(L.K for L in layers)
+            A = [torch.randn((32, L.K), device=dev).to(torch.bfloat16) for L in layers]
+            Y = [torch.empty((32, L.N), dtype=torch.bfloat16, device=dev) for L in layers]
+            ws = torch.empty(F.fp8_workspace_bytes(32, Kmax, 1) + 256, dtype=torch.uint8, device=dev)
+            rows = []
+            for M in Ms:
+                row = {"M": M}
+                for path, thr in (("gemv", 16), ("gemm", 0)):
+                    if path == "gemv" and M > 16:
+                        continue
+                    F.fp8_set_gemv_max_m(thr)
+
+                    def step(M=M):
+                        for Wc in Wq:
+                            for j in range(len(layers)):
+                                F.fp8_linear(A[j][:M], Wc[j][0], Wc[j][1], out=Y[j][:M], ws=ws)
+
+                    t = time_loop(torch, graph_of(torch, step).replay, 10, 3)
+                    row[path + "_us_per_linear"] = round(t * 1e3 / (len(Wq) * len(layers)), 2)
+                rows.append(row)
+            both = [r for r in rows if "gemv_us_per_linear" in r]
+            wins = [r["M"] for r in both if r["gemv_us_per_linear"] <= r["gemm_us_per_linear"]]
+            res[fam] = {"rows": rows, "gemv_faster_at": wins}
+            del A, Y, ws
+    finally:
+        F.fp8_set_gemv_max_m(prev)
+    del fams
+    torch.cuda.synchronize()
+    return res
+
+
+def measure_unaligned(torch, F, I, dev, hbm_gbs):
+    """The four shapes whose dimensions are not multiples of 16 (per-tensor, outlier channels),
+    decode GEMV path; enough weight copies per shape to exceed twice the L2."""
+    out = []
+    for c in I.unaligned_cases():
+        M, K, N = c.M, c.K, c.N
+        copies = max(3, -(-256_000_000 // (N * K)))
+        w = c.w.to(dev)
+        Wq = [F.fp8_quantize_weight(w) for _ in range(copies)]
+        a = c.a.to(dev)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+        def step():
+            for qw, s_w in Wq:
+                F.fp8_linear(a, qw, s_w, out=y)
+
+        t = time_loop(torch, graph_of(torch, step).replay, 10, 3)
+        per = t * 1e-3 / copies
+        gbs = N * K / per / 1e9
+        out.append({"M": M, "K": K, "N": N, "us_per_call": round(per * 1e6, 2), "weight_gbs": round(gbs, 1),
+                    "hbm_frac": round(gbs / hbm_gbs, 4), "weight_copies": copies,
+                    "path": "gemv" if F.fp8_uses_gemv(M, K, N) else "gemm"})
+        del Wq
+    torch.cuda.synchronize()
+    return out
+
+
+def measure_tiny(torch, F, I, dev):
+    """Latency of the 16 x 256 x 256 per-tensor linear (one call, decode GEMV)."""
+    c = I.tiny_case()
+    a, (qw, s_w) = c.a.to(dev), F.fp8_quantize_weight(c.w.to(dev))
+    y = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=dev)
+    reps = 100
+
+    def step():
+        for _ in range(reps):
+            F.fp8_linear(a, qw, s_w, out=y)
+
+    t_graph = time_loop(torch, graph_of(torch, step).replay, 5, 2) / reps
+    t_eager = time_loop(torch, lambda: F.fp8_linear(a, qw, s_w, out=y), 200, 20)
+    return {"M": c.M, "K": c.K, "N": c.N, "us_per_call_graph": round(t_graph * 1e3, 2),
+            "us_per_call_eager": round(t_eager * 1e3, 2)}
+
+
+def run_ours(args):
     import torch
     import fp8_w8a8_quantized_dynamic_gb300 as F
     from fp8_w8a8_quantized_dynamic_gb300 import _build
     from fp8_w8a8_quantized_dynamic_gb300 import inputs as I
 
-    if rank == 0 or not os.path.exists(_build.LIB_PATH):
-        _build.build()
-    if world > 1:
-        torch.distributed.barrier()
+    _build.build()
     F.lib()
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * NOMINAL_FP8_OVER_BF16
+    hbm = peaks["hbm_gbs"]
     M = args.m
     names = args.layers.split(",") if args.layers else None
     layers = [L for _, L in selected_layers(names)]
 
     clocks = ClockSampler(dev.index)
     clocks.start()
-    host, value, ms_max, launches, roofline, quant_ms, gemm_ms = [], None, None, 0, None, [], []
+    host, value, ms, launches, roofline, quant_ms, gemm_ms = [], None, None, 0, None, [], []
+    total_flops = flops(M, layers)
     if not args.no_prefill:
         # ---- inputs: bf16 A per layer, FP8 weights quantized once on the device (load time)
         host = prefill_inputs(M, names)
@@ -288,49 +426,47 @@ def run_ours(args, rank: int, world: int):
         for _ in range(args.warmup):
             step()
         torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record()
         for _ in range(args.steps):
             step()
         t1.record()
         torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
         ms = t0.elapsed_time(t1) / args.steps
-        ms_max = max_over_ranks(torch, ms, world, dev)
-        total_flops = flops(M, layers)
-        value = replica_rate(total_flops, world, ms_max) / 1e12
+        value = total_flops / (ms * 1e-3) / 1e12
         launches = args.steps * len(layers) * 3  # amax, cast, gemm per layer
 
         # ---- GEMM kernel alone (fp8_scaled_mm on the quantized activations), per layer
         Q = [F.fp8_quantize_act(a) for a in A]
         torch.cuda.synchronize()
-        gemm_ms = []
+        plans = {}
         for i, L in enumerate(layers):
             qa, s_a = Q[i]
             f = lambda i=i, qa=qa, s_a=s_a, L=L: F.fp8_scaled_mm(qa, L.K, s_a, Wq[i][0], Wq[i][1], True, out=Y[i])
             gemm_ms.append(time_loop(torch, f, max(3, args.steps // 2), 2))
-        quant_ms = []
+            plans[L.name] = F.fp8_gemm_config(qa, Wq[i][0])
         for i, L in enumerate(layers):
             f = lambda i=i: F.fp8_quantize_act(A[i], ws=ws)
             quant_ms.append(time_loop(torch, f, max(3, args.steps // 2), 2))
         del Q
         gemm_flops = [2.0 * M * L.N * L.K for L in layers]
         gemm_tflops = sum(gemm_flops) / (sum(gemm_ms) * 1e-3) / 1e12
-        fp8_peak = peaks["bf16_tflops"] * NOMINAL_FP8_OVER_BF16
         traffic, traffic_per = gemm_traffic(layers)
+        two = all(p["two_sm"] for p in plans.values())
         roofline = {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
                     "traffic": None if traffic is None else int(traffic),
                     "traffic_note": "mean dram__bytes_read.sum + dram__bytes_write.sum per GEMM launch "
-                                    "(ncu, profiles/gemm_tcgen05_dram_llama8b_m16384.json)",
+                                    "(ncu, profiles/gemm_tcgen05_dram_llama8b_m16384.json); null when that "
+                                    "capture predates the current GEMM source",
                     "traffic_per_launch": traffic_per,
-                    "kernel": "gemm_kernel (tcgen05 kind::f8f6f4; clusters of two CTAs sharing the weight tile by TMA multicast)",
+                    "kernel": "gemm_kernel (tcgen05 kind::f8f6f4, " +
+                              ("CTA pairs on the two-SM MMA, cta_group::2)" if two else "one CTA per tile)"),
+                    "launch_plans": plans,
                     "peak_source": f"{peak_src} bf16 burst x {NOMINAL_FP8_OVER_BF16} nominal fp8/bf16 ratio",
-                    "per_layer_ms": {L.name: round(t, 4) for L, t in zip(layers, gemm_ms)}}
+                    "per_layer_ms": {L.name: round(t, 4) for L, t in zip(layers, gemm_ms)},
+                    "per_layer_frac": {L.name: round(f / (t * 1e-3) / 1e12 / fp8_peak, 4)
+                                       for L, f, t in zip(layers, gemm_flops, gemm_ms)}}
 
     # ---- wider rows on the same workloads: e5m2 operands, static activation scale
     variants = None
@@ -345,7 +481,7 @@ def run_ours(args, rank: int, world: int):
         dq = [[F.fp8_quantize_weight(I.decode_weight(i, c).to(dev)) for i in li] for c in range(copies)]
         wbytes_step = copies * sum(L.N * L.K for L in layers)
         yd = [torch.empty((16, L.N), dtype=torch.bfloat16, device=dev) for L in layers]
-        per_m = {}
+        per_m, per_layer = {}, {}
         for Md in I.DECODE_MS:
             ad = [I.decode_activations(Md, i).to(dev) for i in li]
             ydm = [y[:Md] for y in yd]
@@ -355,16 +491,28 @@ def run_ours(args, rank: int, world: int):
                     for i in range(len(layers)):
                         F.fp8_linear(ad[i], dq[c][i][0], dq[c][i][1], out=ydm[i])
 
-            t_eager = max_over_ranks(torch, time_loop(torch, dstep, max(5, args.steps), 3), world, dev)
-            t = max_over_ranks(torch, time_loop(torch, graph_of(torch, dstep).replay, max(5, args.steps), 3), world, dev)
-            per_m[str(Md)] = {"weight_gbs": round(replica_rate(wbytes_step, world, t) / 1e9, 1),
+            t_eager = time_loop(torch, dstep, max(5, args.steps), 3)
+            t = time_loop(torch, graph_of(torch, dstep).replay, max(5, args.steps), 3)
+            per_m[str(Md)] = {"weight_gbs": round(wbytes_step / (t * 1e-3) / 1e9, 1),
                               "us_per_layer": round(t * 1e3 / (copies * len(layers)), 2),
                               "eager_us_per_layer": round(t_eager * 1e3 / (copies * len(layers)), 2)}
+            if Md in (1, 15):
+                rows = {}
+                for i, L in enumerate(layers):
+                    def lstep(i=i, ad=ad):
+                        for c in range(copies):
+                            F.fp8_linear(ad[i], dq[c][i][0], dq[c][i][1], out=ydm[i])
+
+                    tl = time_loop(torch, graph_of(torch, lstep).replay, max(10, args.steps), 3) / copies
+                    gbs = L.N * L.K / (tl * 1e-3) / 1e9
+                    rows[L.name] = {"us": round(tl * 1e3, 2), "weight_gbs": round(gbs, 1),
+                                    "hbm_frac": round(gbs / hbm, 4),
+                                    "ideal_us": round(L.N * L.K / (hbm * 1e9) * 1e6, 2)}
+                per_layer[f"M{Md}"] = rows
         gbs = [v["weight_gbs"] for v in per_m.values()]
-        hbm = peaks["hbm_gbs"]
         decode = {"metric": "decode weight GB/s (one fused quantize + split-K GEMV kernel per layer, "
                             "CUDA graph replay of the 4 layers x weight copies)", "unit": "GB/s",
-                  "value": round(statistics.median(gbs), 1), "per_M": per_m,
+                  "value": round(statistics.median(gbs), 1), "per_M": per_m, "per_layer": per_layer,
                   "workload": "Mistral-7B linears qkv/o_proj/gate_up/down, M in 1,2,4,8,15, per-tensor scales",
                   "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
                                "frac_median": round(statistics.median(gbs) / hbm, 4),
@@ -372,6 +520,13 @@ def run_ours(args, rank: int, world: int):
                   "l2": f"{copies} weight copies of {sum(L.N * L.K for L in layers) / 1e6:.0f} MB rotated",
                   "gpu_launches_per_replay": copies * len(layers)}
         del dq
+
+    sweep = crossover = unaligned = tiny = None
+    if not args.no_sweep:
+        sweep = measure_sweep(torch, F, I, dev, args, fp8_peak, hbm)
+        crossover = measure_crossover(torch, F, I, dev, args)
+        unaligned = measure_unaligned(torch, F, I, dev, hbm)
+        tiny = measure_tiny(torch, F, I, dev)
 
     clk = clocks.stop()
 
@@ -393,7 +548,7 @@ def run_ours(args, rank: int, world: int):
         for e in ev_done + ev_out:
             e.record(compute)
 
-        def estep():
+        def estep(with_linear=True):
             for i in range(n):
                 s_in.wait_event(ev_done[i])          # A_d[i] is free once the last step's linear read it
                 with torch.cuda.stream(s_in):
@@ -402,7 +557,8 @@ def run_ours(args, rank: int, world: int):
             for i in range(n):
                 compute.wait_event(ev_in[i])
                 compute.wait_event(ev_out[i])        # Y[i] is free once the last step's copy read it
-                F.fp8_linear_channelwise(A_d[i], Wq[i][0], Wq[i][1], out=Y[i], ws=ws)
+                if with_linear:
+                    F.fp8_linear_channelwise(A_d[i], Wq[i][0], Wq[i][1], out=Y[i], ws=ws)
                 ev_done[i].record(compute)
                 s_out.wait_event(ev_done[i])
                 with torch.cuda.stream(s_out):
@@ -411,30 +567,49 @@ def run_ours(args, rank: int, world: int):
             for i in range(n):
                 compute.wait_event(ev_out[i])        # the step ends when its results are on the host
 
-        te = max_over_ranks(torch, time_loop(torch, estep, max(3, args.steps // 4), 2), world, dev)
-        e2e = {"value": round(replica_rate(total_flops, world, te) / 1e12, 2), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(sum(a.numel() * 2 for a in A_h)),
-               "d2h_bytes_per_step": int(sum(y.numel() * 2 for y in Y_h)), "ms_per_step": round(te, 3)}
+        def copies_only():
+            # the link alone: every input copy on one stream, every output copy on the other
+            with torch.cuda.stream(s_in):
+                for i in range(n):
+                    A_d[i].copy_(A_h[i], non_blocking=True)
+            with torch.cuda.stream(s_out):
+                for i in range(n):
+                    Y_h[i].copy_(Y[i], non_blocking=True)
+            compute.wait_stream(s_in)
+            compute.wait_stream(s_out)
+
+        te = time_loop(torch, estep, max(3, args.steps // 4), 2)
+        t_chain = time_loop(torch, lambda: estep(False), max(3, args.steps // 4), 2)
+        t_link = time_loop(torch, copies_only, max(3, args.steps // 4), 2)
+        h2d = int(sum(a.numel() * 2 for a in A_h))
+        d2h = int(sum(y.numel() * 2 for y in Y_h))
+        e2e = {"value": round(total_flops / (te * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(te, 3),
+               "copy_bound_ms": round(t_link, 3), "link_gbs": round((h2d + d2h) / (t_link * 1e-3) / 1e9, 1),
+               "frac_of_copy_bound": round(t_link / te, 4),
+               "copies_in_step_order_ms": round(t_chain, 3),
+               "note": "copy_bound_ms: the same host copies alone, inputs on one stream and outputs on "
+                       "another; copies_in_step_order_ms: the step's copy and event chain without the linears"}
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline and not args.no_prefill:
+    if not args.no_cpu_baseline and not args.no_prefill:
         cpu = oracle_sample(host, M, args.cpu_rows, args.cpu_cols)
 
-    if rank != 0:
-        return None
     return {
-        "metric": METRIC, "value": None if value is None else round(value, 1), "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None if ms_max is None else round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": None if value is None else round(value, 1), "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None if ms is None else round(ms, 4),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 x e4m3 -> fp32 accumulate, bf16 out", "data": "synthetic",
         "config": {"workload": "prefill: Llama-3-8B linears qkv/o_proj/gate_up/down at M=16384, channelwise "
                                "weight scales, dynamic per-tensor activation scale",
                    "M": M, "layers": [[L.name, L.K, L.N] for L in layers], "global_batch": M,
-                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "parallelism": "single GPU",
                    "l2": "inputs larger than L2: each step streams 0.87 GB of bf16 activations and writes "
                          "1.4 GB of outputs across four layers"},
         "roofline": roofline, "kernels_ms": {"quantize_act(amax+cast)": [round(t, 4) for t in quant_ms],
                                              "gemm": [round(t, 4) for t in gemm_ms]},
-        "decode": decode, "variants": variants, "e2e": e2e, "gpu_launches": launches,
+        "decode": decode, "sweep": sweep, "crossover": crossover, "unaligned": unaligned, "tiny": tiny,
+        "variants": variants, "e2e": e2e, "gpu_launches": launches,
         "gpu_launches_note": "timed prefill region: 3 kernels per layer per step (amax, cast, GEMM)",
         "clocks": clk, "cpu_baseline": cpu,
     }
@@ -511,11 +686,13 @@ def main():
     ap.add_argument("--decode-copies", type=int, default=3)
     ap.add_argument("--cpu-rows", type=int, default=16)
     ap.add_argument("--cpu-cols", type=int, default=512)
+    ap.add_argument("--sweep-max-m", type=int, default=16384, help="largest M of the TinyLlama sweep")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="decode leg only (profiling)")
     ap.add_argument("--layers", default="", help="comma list of qkv,o_proj,gate_up,down (default all)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-variants", action="store_true", help="skip the e5m2 / static-scale legs")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the sweep, crossover, unaligned and tiny legs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
 
@@ -525,16 +702,14 @@ def main():
         if rank == 0:
             print(json.dumps(run_reference(args)))
         return
-    if world > 1:
-        import torch
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
-        torch.distributed.init_process_group("nccl")
-    out = run_ours(args, rank, world)
-    if rank == 0:
-        print(json.dumps(out))
-    if world > 1:
-        import torch
-        torch.distributed.destroy_process_group()
+    if world > 1 or args.gpus > 1:
+        # the path runs on one GPU; no rank touches a device here
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "n_gpus": max(world, args.gpus),
+                              "unavailable": "single-GPU path only: the linear is not sharded across GPUs and its "
+                                             "pair GEMM is built for one device; run with --gpus 1"}))
+        return
+    print(json.dumps(run_ours(args)))
 
 
 if __name__ == "__main__":

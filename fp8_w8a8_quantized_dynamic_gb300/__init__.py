@@ -47,6 +47,7 @@ _SIGNATURES = {
     "fp8_min_ld": (_i64, [_i64]),
     "fp8_workspace_bytes": (_sz, [_i64, _i64, _i64]),
     "fp8_uses_gemv": (_int, [_i64, _i64, _i64]),
+    "fp8_set_gemv_max_m": (_int, [_int]),
     "fp8_quantize_weight": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _i64, _vp, _vp, _sz, _vp]),
     "fp8_quantize_act": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _sz, _vp]),
     "fp8_scaled_mm": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _i64, _vp, _int, _vp, _vp, _i64, _vp]),
@@ -64,6 +65,7 @@ _SIGNATURES = {
     "fp8_weight_only_workspace_bytes": (_sz, [_i64, _i64, _i64]),
     "fp8_linear_weight_only": (_int, [_vp, _i64, _i64, _i64, _vp, _int, _i64, _i64, _vp, _int, _vp, _vp, _i64,
                                       _vp, _sz, _vp]),
+    "fp8_gemm_config": (_int, [_vp, _i64, _i64, _vp, _i64, _i64, _vp, _vp, _vp]),
     "fp8_last_device_status": (_int, [_vp]),
     "fp8_selftest_timeout": (_int, [_i64, _vp]),
     "fp8_status_string": (ctypes.c_char_p, [_int]),
@@ -143,6 +145,11 @@ def fp8_workspace_bytes(M: int, K: int, N: int) -> int:
 
 def fp8_uses_gemv(M: int, K: int, N: int) -> bool:
     return bool(lib().fp8_uses_gemv(M, K, N))
+
+
+def fp8_set_gemv_max_m(m: int) -> int:
+    """Largest M that runs the decode GEMV (clamped to 0..16; m < 0 only queries); returns the previous value."""
+    return int(lib().fp8_set_gemv_max_m(int(m)))
 
 
 def fp8_min_ld(K: int) -> int:
@@ -356,3 +363,14 @@ def fp8_last_device_status(stream=None) -> int:
     torch = _torch()
     s = stream if stream is not None else torch.cuda.current_stream().cuda_stream
     return int(lib().fp8_last_device_status(s))
+
+
+def fp8_gemm_config(qa, qw) -> dict:
+    """The GEMM launch the library would use for FP8 operands qa [M, ld] and qw [N, ld] on the
+    current device: {"two_sm": bool, "grid": int, "group_n": int}. Enqueues nothing."""
+    two, grid, gn = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    st = lib().fp8_gemm_config(qa.data_ptr(), qa.shape[0], qa.stride(0), qw.data_ptr(), qw.shape[0], qw.stride(0),
+                               ctypes.byref(two), ctypes.byref(grid), ctypes.byref(gn))
+    if st != FP8_OK:
+        raise FP8Error(st, "fp8_gemm_config")
+    return {"two_sm": bool(two.value), "grid": grid.value, "group_n": gn.value}

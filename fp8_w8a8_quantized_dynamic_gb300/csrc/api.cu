@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -60,14 +61,18 @@ fp8_status current_device(int* sms) {
   return FP8_OK;
 }
 
-int gemv_max_m() {
-  static const int v = [] {
+// Largest M that runs the decode GEMV: FP8W8A8_GEMV_MAX_M at start-up (default 16), then
+// fp8_set_gemv_max_m.
+std::atomic<int>& gemv_max_m_value() {
+  static std::atomic<int> v{[] {
     const char* e = std::getenv("FP8W8A8_GEMV_MAX_M");
-    int x = e ? std::atoi(e) : gemv::kMaxTokens;
+    const int x = e ? std::atoi(e) : gemv::kMaxTokens;
     return std::max(0, std::min(x, gemv::kMaxTokens));
-  }();
+  }()};
   return v;
 }
+
+int gemv_max_m() { return gemv_max_m_value().load(std::memory_order_relaxed); }
 
 bool use_gemv(int64_t M, int64_t K) { return M <= gemv_max_m() && K <= kGemvMaxK; }
 
@@ -597,6 +602,11 @@ FP8_API size_t fp8_workspace_bytes(int64_t M, int64_t K, int64_t N) {
   return linear_ws_bytes(std::max<int64_t>(M, 0), std::max<int64_t>(K, 0));
 }
 
+FP8_API int fp8_set_gemv_max_m(int m) {
+  if (m < 0) return gemv_max_m();
+  return gemv_max_m_value().exchange(std::min(m, gemv::kMaxTokens));
+}
+
 FP8_API int fp8_uses_gemv(int64_t M, int64_t K, int64_t N) {
   (void)N;
   return use_gemv(M, K) ? 1 : 0;
@@ -682,6 +692,19 @@ FP8_API fp8_status fp8_linear_weight_only(const void* a_bf16, int64_t M, int64_t
                                           void* ws, size_t ws_bytes, fp8_stream_t stream) {
   return weight_only_impl(a_bf16, M, K, lda, qw, int(fmt_w), N, ldqw, s_w, per_channel, bias_bf16, y_bf16, ldy, ws,
                           ws_bytes, stream);
+}
+
+FP8_API fp8_status fp8_gemm_config(const uint8_t* qa, int64_t M, int64_t ldqa, const uint8_t* qw, int64_t N,
+                                   int64_t ldqw, int* two_sm, int* grid, int* group_n) {
+  if (M <= 0 || N <= 0 || M > kMaxDim || N > kMaxDim || ldqa <= 0 || ldqw <= 0) return FP8_ERR_INVALID_ARG;
+  int sms = 0;
+  FP8_TRY(current_device(&sms));
+  const fp8k::GemmPlan pl = fp8k::gemm_plan(qa, ldqa, qw, ldqw, int(M), int(N), sms);
+  if (pl.grid <= 0) return FP8_ERR_CUDA;
+  if (two_sm) *two_sm = pl.two_sm;
+  if (grid) *grid = pl.grid;
+  if (group_n) *group_n = pl.group_n;
+  return FP8_OK;
 }
 
 FP8_API fp8_status fp8_last_device_status(fp8_stream_t stream) {

@@ -15,26 +15,32 @@
 // one MMA still consumes 32 bytes of K (16 elements), so tiles, descriptors and the ring
 // are unchanged.
 //
-// Structure (one CTA per SM, persistent over output tiles of 128 x 256):
-//   warp 0      TMA producer: qA tile [128 x 128B] and qW tile [256 x 128B] per stage into a
-//               4-stage ring of 128B-swizzled shared memory, completion on an mbarrier.
-//   warp 1      TMEM allocator + MMA issuer: tcgen05.mma.cta_group::1.kind::f8f6f4,
-//               M=128 N=256 K=32, fp32 accumulators in TMEM, two accumulator buffers of 256
+// Structure (persistent, one CTA per SM, output tiles of 128 x 256 per CTA):
+//   warp 0      TMA producer: this CTA's qA tile [128 x 128B] and its part of the qW tile
+//               per stage into a ring of 128B-swizzled shared memory, completion on an
+//               mbarrier.
+//   warp 1      TMEM allocator + MMA issuer: tcgen05.mma kind::f8f6f4, K = 32 per
+//               instruction, fp32 accumulators in TMEM, two accumulator buffers of 256
 //               columns so the epilogue of tile i overlaps the main loop of tile i+1.
 //   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, scale (+bias), bf16, store.
 // Ragged M, N and K need no padding: TMA fills out-of-range rows/columns with zeros and
 // the epilogue predicates its stores.
 //
-// Paired mode (kPair, a cluster of two CTAs on row blocks 2i and 2i+1 of the same column
-// tile): the 256-row weight tile is shared. Each CTA loads its own qA tile and one half of
-// the weight tile, the half multicast into both CTAs' shared memory, so the L2 -> SM traffic
-// per tile drops from 48 KB to 32 KB per stage (the single-CTA kernel reads ~19 TB/s from
-// L2 at 73 % of its request peak). Each stage's empty barrier then counts the MMA commits of
-// both CTAs (a CTA's multicast half overwrites the peer's stage too), and the two CTAs run
-// the same tile sequence with the same number of k-blocks.
+// Two modes:
+//   single   one CTA per 128 x 256 tile, tcgen05.mma.cta_group::1 (M = 128, N = 256),
+//            4 stages of 48 KB (A 16 KB + W 32 KB).
+//   two-SM   a cluster of two CTAs (a CTA pair) computes a 256 x 256 tile with
+//            tcgen05.mma.cta_group::2 (M = 256, N = 256): each CTA holds its own 128 rows
+//            of qA and one half (128 rows) of the weight tile, so a stage is 32 KB and the
+//            ring is 6 deep. Both CTAs' copies complete on the leader's (rank 0) full
+//            barrier; the leader's one elected thread issues the MMAs for the pair, and
+//            its commits arrive on both CTAs' barriers. Each CTA's epilogue reads its own
+//            tensor memory (the accumulator rows of its A tile). The weight tile crosses
+//            from L2 to the SMs once per pair, not once per CTA.
 //
-// Every wait is bounded (2 s); on expiry the kernel records an error for the host, drains
-// its own outstanding copies and MMAs (again bounded), frees its TMEM and returns.
+// Every wait is bounded (2 s); on expiry the kernel records an error for the host (with a
+// bit naming the wait), stops its peer, drains every copy either CTA issued, frees its
+// TMEM and returns.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -43,9 +49,8 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
-#include <map>
-#include <mutex>
 
+#include "device_cache.h"
 #include "device_common.cuh"
 #include "gemm_tcgen05.h"
 
@@ -54,32 +59,50 @@ namespace gemm {
 
 __device__ unsigned int g_gemm_error;
 
+// Error bits beyond kErrTimeout: which wait gave up (diagnostics for the host).
+constexpr unsigned int kSiteEmpty = 0x100u;   // producer waiting for a free stage
+constexpr unsigned int kSiteFull = 0x200u;    // MMA issuer waiting for a filled stage
+constexpr unsigned int kSiteTempty = 0x400u;  // MMA issuer waiting for a drained accumulator
+constexpr unsigned int kSiteTfull = 0x800u;   // epilogue waiting for a finished accumulator
+constexpr unsigned int kSiteDrain = 0x1000u;  // exit path: outstanding copies or MMAs
+
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 128;  // bytes of K per stage: one 128-byte swizzle row (128 FP8 / 64 bf16 elements)
-constexpr int kStages = 4;
 constexpr int kAccBufs = 2;
 constexpr int kTmemCols = kAccBufs * BN;  // 512: the whole tensor memory of the SM
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kABytes = BM * BK;
 constexpr uint32_t kBBytes = BN * BK;
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr int kMmaK = 32;  // bytes of K of one MMA (32 FP8 elements, kind::f8f6f4; 16 bf16, kind::f16)
 
+// Shared-memory ring of each mode: the two-SM CTA holds half of the weight tile per stage.
+template <bool kTwo>
+struct Ring {
+  static constexpr uint32_t stage_bytes = kTwo ? kABytes + kBBytes / 2 : kABytes + kBBytes;
+  static constexpr int stages = kTwo ? 6 : 4;
+};
+constexpr int kMaxStages = 6;
+constexpr size_t kRingBytes =
+    std::max(size_t(Ring<true>::stages) * Ring<true>::stage_bytes, size_t(Ring<false>::stages) * Ring<false>::stage_bytes);
+
 struct SharedCtl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tfull[kAccBufs];
   uint64_t tempty[kAccBufs];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  uint32_t issued[2];  // two-SM: stages each CTA's producer filled (in the leader's block)
   float colscale[kAccBufs][BN];
   float colbias[kAccBufs][BN];
 };
 
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + sizeof(SharedCtl);
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kRingBytes + sizeof(SharedCtl);
+static_assert(kSmemBytes <= 232448, "ring and control block must fit the 227 KB per-block limit");
+static_assert(2 * kSmemBytes > 233472, "two GEMM CTAs must never share an SM (each holds all of TMEM)");
 
 // Instruction descriptor, kind::f8f6f4: D fp32 (bits 4-5 = 1), A and B format at bits 7-9 and
 // 10-12 (e4m3 = 0, e5m2 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at
@@ -92,6 +115,11 @@ constexpr uint32_t make_idesc(int fmt_a, int fmt_w) {
 
 // kind::f16 with bf16 A and B: the format fields hold BF16 = 1.
 constexpr uint32_t kIdescBf16 = kIdescBase | (1u << 7) | (1u << 10);
+
+// The two-SM MMA covers both CTAs' rows: M = 256 in the descriptor.
+__host__ __device__ constexpr uint32_t idesc_two_sm(uint32_t idesc) {
+  return (idesc & ~(0x1Fu << 24)) | (uint32_t((2 * BM) >> 4) << 24);
+}
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA with 128-byte
 // swizzle: rows of 128 bytes, 8-row swizzle atoms of 1024 bytes (stride byte offset), start
@@ -107,16 +135,54 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr) {
   return d;
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
-      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y) : "memory");
+// L2 eviction priorities for the TMA loads and the output stores (createpolicy): the operand
+// the raster keeps hot in L2 is loaded evict_last, the one streamed once evict_first.
+enum : int { kHintNormal = 0, kHintFirst = 1, kHintLast = 2 };
+
+__device__ __forceinline__ uint64_t l2_policy(int hint) {
+  uint64_t p;
+  if (hint == kHintLast)
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  else if (hint == kHintFirst)
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  else
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
-template <bool kBf16>
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy) : "memory");
+}
+
+// Two-SM form: the copy lands in this CTA's shared memory and completes its bytes on an
+// mbarrier that may be the peer's (here always the leader's).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t cluster_bar, int x,
+                                                 int y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+template <bool kBf16, bool kTwo>
 __device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                           uint32_t accumulate) {
-  if constexpr (kBf16)
+  if constexpr (kTwo && kBf16)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+  else if constexpr (kTwo)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+  else if constexpr (kBf16)
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
@@ -128,33 +194,45 @@ __device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint64_t adesc, uint6
         :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
+// Arrives once on `bar` when every MMA this thread issued before has completed; in two-SM
+// mode it arrives on the barrier at that offset in both CTAs of the pair.
+template <bool kTwo>
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
+  if constexpr (kTwo)
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 :: "r"(bar), "h"(uint16_t(0x3)) : "memory");
+  else
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar)
+                 : "memory");
 }
 
-// Multicast forms for the paired mode: the copy lands at the same shared-memory offset in
-// every CTA of `mask` and completes bytes on the mbarrier at the same offset in each; the
-// commit arrives once on that mbarrier in each CTA of `mask`.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;"
-      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask) : "memory");
-}
-
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-               :: "r"(bar), "h"(mask) : "memory");
-}
-
-__device__ __forceinline__ uint32_t pair_rank() {
+__device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
 
-// Every thread of both CTAs: barrier inits visible before the first multicast, and no CTA
+// A shared-memory address of this CTA, as seen in CTA `rank` of the cluster (shared::cluster).
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t a, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(rank));
+  return d;
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(cluster_addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(cluster_bar) : "memory");
+}
+
+// Accounts for `bytes` that will never arrive on this CTA's barrier (abort path only).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+
+// Every thread of both CTAs: barrier inits visible before the first remote signal, and no CTA
 // leaves while its peer may still write into its shared memory or arrive on its barriers.
 __device__ __forceinline__ void pair_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -192,9 +270,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
          (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
 }
 
-// Tile order: groups of `group_n` column tiles; inside a group the column index runs fastest,
-// so the CTAs resident at one time share a few qA row blocks and a W slice that stays in L2
-// while the group sweeps all rows: W is read from HBM once, qA once per group.
+__device__ __forceinline__ void st_global_v4(uint4* p, uint4 v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;"
+               :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy) : "memory");
+}
+
+// Tile order: groups of `group_n` column tiles; inside a group the column index runs fastest.
+// group_n = n_tiles keeps all of W hot in L2 while the row blocks stream past (qA read from
+// HBM once); group_n = 1 sweeps all row blocks for one column tile before the next, keeping
+// qA hot while W streams once; between the two, a W slice stays hot per group.
 __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int m_units, int& m_idx, int& n_idx) {
   const int per_group = p.group_n * m_units;
   const int gidx = tile / per_group;
@@ -205,59 +289,75 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int m
   n_idx = n_first + (r - m_idx * gn);
 }
 
-// kBf16: operands are bf16 (weight-only product) instead of FP8. kPair: clusters of two CTAs
-// sharing the weight tile (see the paired mode above).
-template <bool kBf16, bool kPair>
+// kBf16: operands are bf16 (weight-only product) instead of FP8. kTwo: clusters of two CTAs
+// on the two-SM MMA (see the modes above).
+template <bool kBf16, bool kTwo>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
             const __grid_constant__ GemmParams p) {
   constexpr int kElemsPerStage = kBf16 ? BK / 2 : BK;  // K elements per stage
+  constexpr int kStages = Ring<kTwo>::stages;
+  constexpr uint32_t kStageBytes = Ring<kTwo>::stage_bytes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-aligned for the 128B swizzle
-  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + kStages * kStageBytes);
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + kRingBytes);
   const uint32_t smem_base = smem_u32(smem);
   auto a_stage = [&](int s) { return smem_base + s * kStageBytes; };
   auto b_stage = [&](int s) { return smem_base + s * kStageBytes + kABytes; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // work units: tiles, or (paired) vertical tile pairs; rank r of a pair takes row block 2i + r
-  const uint32_t rank = kPair ? pair_rank() : 0u;
-  const int m_units = kPair ? (p.m_tiles + 1) / 2 : p.m_tiles;
+  // work units: tiles, or (two-SM) vertical tile pairs; rank r of a pair takes row block 2i + r
+  const uint32_t rank = kTwo ? cluster_rank() : 0u;
+  const bool leader = rank == 0;
+  const int m_units = kTwo ? (p.m_tiles + 1) / 2 : p.m_tiles;
   const int num_tiles = m_units * p.n_tiles;
-  const int first_unit = kPair ? int(blockIdx.x >> 1) : int(blockIdx.x);
-  const int unit_stride = kPair ? int(gridDim.x >> 1) : int(gridDim.x);
+  const int first_unit = kTwo ? int(blockIdx.x >> 1) : int(blockIdx.x);
+  const int unit_stride = kTwo ? int(gridDim.x >> 1) : int(gridDim.x);
   auto coords = [&](int unit, int& m_idx, int& n_idx) {
     tile_coords(unit, p, m_units, m_idx, n_idx);
-    if (kPair) m_idx = 2 * m_idx + int(rank);
+    if (kTwo) m_idx = 2 * m_idx + int(rank);
   };
   const int num_kb = (p.K + kElemsPerStage - 1) / kElemsPerStage;
   volatile int* abort_flag = &ctl->abort_flag;
+  // after a wait gives up: stop the peer CTA as well, so the pair leaves together
+  auto fail = [&](unsigned int site) {
+    atomicOr(&g_gemm_error, site);
+    if (kTwo) st_cluster_u32(map_to_rank(smem_u32(&ctl->abort_flag), rank ^ 1u), 1u);
+  };
 
   if (threadIdx.x == 0) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
-      mbar_init(smem_u32(&ctl->empty[s]), kPair ? 2 : 1);  // paired: both CTAs' MMAs read the stage
+      mbar_init(smem_u32(&ctl->empty[s]), 1);  // one commit per stage (two-SM: the leader's, in both CTAs)
     }
     for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(smem_u32(&ctl->tfull[b]), 1);
-      mbar_init(smem_u32(&ctl->tempty[b]), kEpiThreads);
+      // two-SM: the leader's MMA waits until both CTAs' epilogues have drained the buffer
+      mbar_init(smem_u32(&ctl->tempty[b]), kTwo ? 2 * kEpiThreads : kEpiThreads);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort_flag = 0;
+    ctl->issued[0] = ctl->issued[1] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                 :: "r"(smem_u32(&ctl->tmem_base)), "n"(kTmemCols) : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if (kTwo) {  // one warp of each CTA allocates the pair's tensor memory together
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                   :: "r"(smem_u32(&ctl->tmem_base)), "n"(kTmemCols) : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                   :: "r"(smem_u32(&ctl->tmem_base)), "n"(kTmemCols) : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tmem_fence_before();
   __syncthreads();
-  if (kPair) pair_sync();  // the peer's barriers exist before the first multicast lands there
+  if (kTwo) pair_sync();  // the peer's barriers exist before the first copy or commit signals them
   tmem_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
 
@@ -267,6 +367,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
+      const uint64_t pol_a = l2_policy(p.hint_a), pol_b = l2_policy(p.hint_b);
       uint32_t it = 0;
       bool ok = true;
       for (int tile = first_unit; tile < num_tiles && ok; tile += unit_stride) {
@@ -275,60 +376,80 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
-          if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, &g_gemm_error)) { ok = false; break; }
+          if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, &g_gemm_error)) {
+            fail(kSiteEmpty);
+            ok = false;
+            break;
+          }
           const uint32_t fb = smem_u32(&ctl->full[s]);
-          mbar_arrive_expect_tx(fb, kStageBytes);
-          tma_load_2d(a_stage(s), &tmap_a, fb, kb * kElemsPerStage, m_idx * BM);
-          if (kPair)  // this CTA's half of the weight tile, into both CTAs
-            tma_load_2d_mc(b_stage(s) + rank * (kBBytes / 2), &tmap_b, fb, kb * kElemsPerStage,
-                           n_idx * BN + int(rank) * (BN / 2), uint16_t(0x3));
-          else
-            tma_load_2d(b_stage(s), &tmap_b, fb, kb * kElemsPerStage, n_idx * BN);
+          if (kTwo) {
+            // both CTAs' copies complete on the leader's barrier, which expects all of them
+            const uint32_t lb = map_to_rank(fb, 0);
+            if (leader) mbar_arrive_expect_tx(fb, 2 * kStageBytes);
+            tma_load_2d_pair(a_stage(s), &tmap_a, lb, kb * kElemsPerStage, m_idx * BM, pol_a);
+            tma_load_2d_pair(b_stage(s), &tmap_b, lb, kb * kElemsPerStage, n_idx * BN + int(rank) * (BN / 2),
+                             pol_b);
+          } else {
+            mbar_arrive_expect_tx(fb, kStageBytes);
+            tma_load_2d(a_stage(s), &tmap_a, fb, kb * kElemsPerStage, m_idx * BM, pol_a);
+            tma_load_2d(b_stage(s), &tmap_b, fb, kb * kElemsPerStage, n_idx * BN, pol_b);
+          }
         }
       }
-      if (!ok) {
+      if (kTwo) {
+        // the leader drains the pair's copies after both have stopped (exit path below)
+        st_cluster_u32(map_to_rank(smem_u32(&ctl->issued[rank]), 0), it);
+      } else if (!ok) {
         // drain: the last fill of every stage must land before the CTA's memory is released
         const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0u;
         for (uint32_t j = first; j < it; ++j)
-          mbar_wait_bounded(smem_u32(&ctl->full[j % kStages]), (j / kStages) & 1u, nullptr, &g_gemm_error);
+          if (!mbar_wait_bounded(smem_u32(&ctl->full[j % kStages]), (j / kStages) & 1u, nullptr, &g_gemm_error))
+            atomicOr(&g_gemm_error, kSiteDrain);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (two-SM: the leader, for both CTAs) ----------------
+      const uint32_t idesc = kTwo ? idesc_two_sm(p.idesc) : p.idesc;
       uint32_t it = 0, acc_it = 0;
       bool ok = true;
       for (int tile = first_unit; tile < num_tiles && ok; tile += unit_stride, ++acc_it) {
         const int ab = acc_it % kAccBufs;
         const uint32_t aph = (acc_it / kAccBufs) & 1u;
-        if (!mbar_wait_bounded(smem_u32(&ctl->tempty[ab]), aph ^ 1u, abort_flag, &g_gemm_error)) { ok = false; break; }
+        if (!mbar_wait_bounded(smem_u32(&ctl->tempty[ab]), aph ^ 1u, abort_flag, &g_gemm_error)) {
+          fail(kSiteTempty);
+          break;
+        }
         tmem_fence_after();
         const uint32_t d_tmem = tmem_base + ab * BN;
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
-          if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, &g_gemm_error)) { ok = false; break; }
+          if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, &g_gemm_error)) {
+            fail(kSiteFull);
+            ok = false;
+            break;
+          }
           tmem_fence_after();
           const uint64_t adesc = make_sdesc(a_stage(s));
           const uint64_t bdesc = make_sdesc(b_stage(s));
 #pragma unroll
           for (int kk = 0; kk < BK / kMmaK; ++kk) {
             // advance the start address by 32 bytes of K inside the swizzled 128-byte row
-            mma_issue<kBf16>(d_tmem, adesc + uint64_t(kk * kMmaK >> 4), bdesc + uint64_t(kk * kMmaK >> 4),
-                             p.idesc, (kb | kk) != 0 ? 1u : 0u);
+            mma_issue<kBf16, kTwo>(d_tmem, adesc + uint64_t(kk * kMmaK >> 4), bdesc + uint64_t(kk * kMmaK >> 4),
+                                   idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          // frees the stage once these MMAs have read it (in both CTAs' counts when paired)
-          if (kPair)
-            mma_commit_mc(smem_u32(&ctl->empty[s]), uint16_t(0x3));
-          else
-            mma_commit(smem_u32(&ctl->empty[s]));
+          mma_commit<kTwo>(smem_u32(&ctl->empty[s]));  // frees the stage once these MMAs have read it
         }
         if (!ok) break;
-        mma_commit(smem_u32(&ctl->tfull[ab]));   // accumulator ready for the epilogue
+        mma_commit<kTwo>(smem_u32(&ctl->tfull[ab]));  // accumulator ready for the epilogue(s)
       }
       // all MMAs issued by this thread must finish before TMEM is released
-      mma_commit(smem_u32(&ctl->drain));
-      mbar_wait_bounded(smem_u32(&ctl->drain), 0, nullptr, &g_gemm_error);
+      mma_commit<kTwo>(smem_u32(&ctl->drain));
+      if (!mbar_wait_bounded(smem_u32(&ctl->drain), 0, nullptr, &g_gemm_error)) atomicOr(&g_gemm_error, kSiteDrain);
+    } else if (lane == 0 && kTwo) {
+      // the follower: its tensor memory is written by the leader's MMAs until the drain commit
+      if (!mbar_wait_bounded(smem_u32(&ctl->drain), 0, nullptr, &g_gemm_error)) atomicOr(&g_gemm_error, kSiteDrain);
     }
   } else {
     // ---------------- epilogue: warps 2..5 ----------------
@@ -336,6 +457,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     const int row_in_tile = q * 32 + lane;
     const int et = threadIdx.x - 64;           // 0..127
     const float s_a = p.s_a ? *p.s_a : 1.0f;
+    const uint64_t pol_y = l2_policy(p.hint_y);
+    const uint32_t tempty_bar = kTwo ? map_to_rank(smem_u32(&ctl->tempty[0]), 0) : smem_u32(&ctl->tempty[0]);
     uint32_t acc_it = 0;
     for (int tile = first_unit; tile < num_tiles; tile += unit_stride, ++acc_it) {
       int m_idx, n_idx;
@@ -358,7 +481,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       if (epi_bar_any(*abort_flag != 0)) break;
       // after a timeout, skip to the next barrier above, which ends the loop uniformly
       // one lane waits and the warp follows its verdict: tcgen05.ld needs a converged warp
-      bool ok = lane == 0 ? mbar_wait_bounded(smem_u32(&ctl->tfull[ab]), aph, abort_flag, &g_gemm_error) : true;
+      bool ok = true;
+      if (lane == 0 && !mbar_wait_bounded(smem_u32(&ctl->tfull[ab]), aph, abort_flag, &g_gemm_error)) {
+        fail(kSiteTfull);
+        ok = false;
+      }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) continue;
       tmem_fence_after();
@@ -385,7 +512,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 w[h] = pack_bf16x2(fmaf(__uint_as_float(r[j]), cs[j], cb[j]),
                                    fmaf(__uint_as_float(r[j + 1]), cs[j + 1], cb[j + 1]));
               }
-              dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+              st_global_v4(dst + v, make_uint4(w[0], w[1], w[2], w[3]), pol_y);
             }
           } else {
 #pragma unroll
@@ -398,18 +525,44 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         }
       }
       tmem_fence_before();
-      mbar_arrive(smem_u32(&ctl->tempty[ab]));
+      if (kTwo)
+        arrive_cluster(tempty_bar + ab * uint32_t(sizeof(uint64_t)));
+      else
+        mbar_arrive(tempty_bar + ab * uint32_t(sizeof(uint64_t)));
     }
   }
 
   __syncwarp();
+  if constexpr (kTwo) {
+    // Every copy either producer issued must have landed before either CTA's shared memory
+    // is released. Both copies of a stage complete on the leader's barrier; once both
+    // producers have stopped (their counts are in the leader's block), the leader accounts
+    // for the halves that were never issued and waits for the rest.
+    __syncthreads();
+    pair_sync();
+    if (leader && threadIdx.x == 0) {
+      const uint32_t n0 = ctl->issued[0], n1 = ctl->issued[1];
+      const uint32_t hi = n0 > n1 ? n0 : n1;
+      // a producer fills stage j only after the MMAs of stage j - kStages finished, so
+      // everything below hi - kStages is complete; each j above it is its stage's open phase
+      for (uint32_t j = hi > uint32_t(kStages) ? hi - kStages : 0u; j < hi; ++j) {
+        const uint32_t fb = smem_u32(&ctl->full[j % kStages]);
+        if (j >= n0) mbar_arrive_expect_tx(fb, kStageBytes);  // only the follower filled it
+        else if (j >= n1) mbar_complete_tx(fb, kStageBytes);  // the follower's half never came
+        if (!mbar_wait_bounded(fb, (j / kStages) & 1u, nullptr, &g_gemm_error)) atomicOr(&g_gemm_error, kSiteDrain);
+      }
+    }
+  }
   tmem_fence_before();
   __syncthreads();
-  if (kPair) pair_sync();  // the peer's last multicast copies and commit arrivals are done
+  if (kTwo) pair_sync();  // the peer's copies, commits and arrivals are done
   tmem_fence_after();
   if (warp == 1) {
     __syncwarp();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem_base), "n"(kTmemCols) : "memory");
+    if (kTwo)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(tmem_base), "n"(kTmemCols) : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem_base), "n"(kTmemCols) : "memory");
   }
 }
 
@@ -464,41 +617,126 @@ bool make_fp8_tensor_map(CUtensorMap* map, const uint8_t* base, int64_t rows, in
 
 namespace {
 
-// Resident clusters of two for the paired kernel (cached per kernel): clusters must fit in
-// one GPC, so GPCs with an odd number of free SMs leave one SM out.
-int pair_clusters(const void* kernel, cudaLaunchConfig_t cfg) {
-  static std::mutex mu;
-  static std::map<const void*, int> cache;
-  std::lock_guard<std::mutex> g(mu);
-  auto it = cache.find(kernel);
-  if (it != cache.end()) return it->second;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cfg.gridDim = dim3(2 * 64);  // any multiple of the cluster size
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+int env_int(const char* name, int dflt) {
+  const char* e = std::getenv(name);
+  return (e && e[0]) ? std::atoi(e) : dflt;
+}
+
+// Run-time switches (read once per process): FP8W8A8_GEMM_PAIR=0 selects one CTA per tile;
+// FP8W8A8_GEMM_GROUP_N fixes the raster group; FP8W8A8_GEMM_L2_MB sets the L2 bytes the
+// raster may keep hot for one operand; FP8W8A8_GEMM_L2HINT=0 drops the eviction hints.
+struct GemmSwitches {
+  bool pair;
+  int group_n;
+  int64_t l2_budget;
+  bool hints;
+};
+
+const GemmSwitches& switches() {
+  static const GemmSwitches s = [] {
+    GemmSwitches v;
+    v.pair = env_int("FP8W8A8_GEMM_PAIR", 2) != 0;
+    v.group_n = env_int("FP8W8A8_GEMM_GROUP_N", 0);
+    v.l2_budget = int64_t(std::max(1, env_int("FP8W8A8_GEMM_L2_MB", 72))) << 20;
+    v.hints = env_int("FP8W8A8_GEMM_L2HINT", 1) != 0;
+    return v;
+  }();
+  return s;
+}
+
+// True when p is memory of device `dev` itself. The pair mode's tensor maps may only cover
+// this GPU's own memory: pinned or managed host memory, and memory of another GPU, take the
+// single-CTA kernel.
+bool local_device_memory(const void* p, int dev) {
+  cudaPointerAttributes at = {};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
     cudaGetLastError();
-    n = 0;
+    return false;
   }
-  if (std::getenv("FP8W8A8_DEBUG")) std::fprintf(stderr, "fp8w8a8: gemm pairs resident: %d clusters of 2\n", n);
-  cache[kernel] = n;
+  return at.type == cudaMemoryTypeDevice && at.device == dev;
+}
+
+PerDeviceCache<const void*, int> g_attr_cache;   // kernel -> attributes set on this device
+PerDeviceCache<const void*, int> g_pair_cache;   // kernel -> co-resident clusters of two
+
+// Kernel attributes (dynamic shared memory) are per device: set once on each.
+bool ensure_attributes(int dev, const void* kernel) {
+  int done = 0;
+  return g_attr_cache.get(dev, kernel, &done, [&](int* v) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(gemm::kSmemBytes)) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    *v = 1;
+    return true;
+  });
+}
+
+// Resident clusters of two for the pair kernel on device `dev`: clusters must fit in one
+// GPC, so GPCs with an odd number of free SMs leave one SM out.
+int pair_clusters(int dev, const void* kernel) {
+  int n = 0;
+  g_pair_cache.get(dev, kernel, &n, [&](int* v) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(gemm::kThreads);
+    cfg.dynamicSmemBytes = gemm::kSmemBytes;
+    cfg.gridDim = dim3(2 * 64);  // any multiple of the cluster size
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(v, kernel, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    if (std::getenv("FP8W8A8_DEBUG")) std::fprintf(stderr, "fp8w8a8: gemm pairs resident on device %d: %d\n", dev, *v);
+    return true;
+  });
   return n;
 }
 
-// Paired (cluster) mode unless FP8W8A8_GEMM_PAIR=0, there is only one row block, or fewer
-// than 3/4 of the SMs could run pairs.
-bool pair_enabled() {
-  static const bool on = [] {
-    const char* e = std::getenv("FP8W8A8_GEMM_PAIR");
-    return !(e && e[0] == '0');
-  }();
-  return on;
+}  // namespace
+
+// The launch configuration (host logic only; see GemmPlan).
+GemmPlan plan_gemm(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_bytes, int M, int N, int dev,
+                   int num_sms, int pair_clusters_available) {
+  using namespace gemm;
+  const GemmSwitches& sw = switches();
+  GemmPlan pl;
+  pl.m_tiles = (M + BM - 1) / BM;
+  pl.n_tiles = (N + BN - 1) / BN;
+  pl.two_sm = sw.pair && pl.m_tiles >= 2 && 2 * pair_clusters_available >= (3 * num_sms) / 4 &&
+              local_device_memory(a, dev) && local_device_memory(w, dev);
+  const int m_units = pl.two_sm ? (pl.m_tiles + 1) / 2 : pl.m_tiles;
+  const int units = m_units * pl.n_tiles;
+  pl.grid = pl.two_sm ? 2 * std::min(units, pair_clusters_available) : std::min(units, num_sms);
+  // raster: keep the smaller operand hot in L2 when it fits the budget, stream the other once
+  const int64_t a_bytes = int64_t(M) * lda_bytes, w_bytes = int64_t(N) * ldw_bytes;
+  const int64_t w_tile_bytes = int64_t(BN) * ldw_bytes;
+  pl.hint_a = pl.hint_b = kHintNormal;
+  if (w_bytes <= sw.l2_budget && (w_bytes <= a_bytes || a_bytes > sw.l2_budget)) {
+    pl.group_n = pl.n_tiles;  // W resident, qA streamed once
+    pl.hint_a = kHintFirst;
+    pl.hint_b = kHintLast;
+  } else if (a_bytes <= sw.l2_budget) {
+    pl.group_n = 1;  // qA resident, W streamed once
+    pl.hint_a = kHintLast;
+    pl.hint_b = kHintFirst;
+  } else {
+    // neither fits: a W slice of about a third of the budget stays hot per group
+    pl.group_n = int(std::max<int64_t>(1, std::min<int64_t>(pl.n_tiles, (sw.l2_budget / 3) / w_tile_bytes)));
+  }
+  if (sw.group_n > 0) pl.group_n = std::min(sw.group_n, pl.n_tiles);
+  pl.hint_y = kHintFirst;  // Y is written once
+  if (!sw.hints) pl.hint_a = pl.hint_b = pl.hint_y = kHintNormal;
+  return pl;
 }
+
+namespace {
 
 template <bool kBf16>
 int launch_kind(const void* a, int64_t lda_bytes, const float* s_a, const void* w, int64_t ldw_bytes,
@@ -506,15 +744,14 @@ int launch_kind(const void* a, int64_t lda_bytes, const float* s_a, const void* 
                 int K, uint32_t idesc, int num_sms, cudaStream_t stream) {
   using namespace gemm;
   auto single = gemm_kernel<kBf16, false>;
-  auto paired = gemm_kernel<kBf16, true>;
-  static bool attr_done = false;  // the attribute is per function, set once per process
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(single, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes)) != cudaSuccess ||
-        cudaFuncSetAttribute(paired, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes)) != cudaSuccess ||
-        cudaFuncSetAttribute(paired, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess)
-      return 1;
-    attr_done = true;
-  }
+  auto two_sm = gemm_kernel<kBf16, true>;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (!ensure_attributes(dev, reinterpret_cast<const void*>(single)) ||
+      !ensure_attributes(dev, reinterpret_cast<const void*>(two_sm)))
+    return 1;
+  const int clusters = switches().pair ? pair_clusters(dev, reinterpret_cast<const void*>(two_sm)) : 0;
+  const GemmPlan pl = plan_gemm(a, lda_bytes, w, ldw_bytes, M, N, dev, num_sms, clusters);
 
   GemmParams p;
   p.M = M;
@@ -526,50 +763,41 @@ int launch_kind(const void* a, int64_t lda_bytes, const float* s_a, const void* 
   p.bias = bias;
   p.y = y;
   p.ldy = ldy;
-  p.m_tiles = (M + BM - 1) / BM;
-  p.n_tiles = (N + BN - 1) / BN;
+  p.m_tiles = pl.m_tiles;
+  p.n_tiles = pl.n_tiles;
+  p.group_n = pl.group_n;
   p.y_vec = (ldy % 8 == 0) && (reinterpret_cast<uintptr_t>(y) % 16 == 0);
   p.idesc = idesc;
+  p.hint_a = pl.hint_a;
+  p.hint_b = pl.hint_b;
+  p.hint_y = pl.hint_y;
+
+  CUtensorMap ma, mb;
+  if (!make_tensor_map(&ma, a, kBf16, M, K, lda_bytes, BM) ||
+      !make_tensor_map(&mb, w, kBf16, N, K, ldw_bytes, pl.two_sm ? BN / 2 : BN))
+    return 2;
 
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  int clusters = 0;
-  if (pair_enabled() && p.m_tiles >= 2) {
-    clusters = pair_clusters(reinterpret_cast<const void*>(paired), cfg);
-    if (2 * clusters < (3 * num_sms) / 4) clusters = 0;
+  cfg.gridDim = dim3(unsigned(pl.grid));
+  cudaLaunchAttribute attr[1];
+  cfg.attrs = attr;
+  if (pl.two_sm) {
+    // Launched without programmatic stream serialization: the pair's grid starts only after
+    // the kernel before it has finished, so no CTA pair becomes resident while CTAs of an
+    // earlier GEMM grid still run (its own trigger still lets the next kernel start early).
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, two_sm, ma, mb, p) == cudaSuccess ? 0 : 3;
   }
-  const bool pair = clusters > 0;
-  const int m_units = pair ? (p.m_tiles + 1) / 2 : p.m_tiles;
-  // raster: a group of column tiles whose W slice (~26 MB) stays hot in L2 while the group
-  // sweeps all rows; qA is then read once per group. Larger hot sets were measured to be
-  // evicted by the streaming qA and Y traffic.
-  const int64_t slice_budget = int64_t(26) << 20;
-  const int64_t w_tile_bytes = int64_t(BN) * ldw_bytes;
-  p.group_n = int(std::max<int64_t>(1, std::min<int64_t>(p.n_tiles, slice_budget / w_tile_bytes)));
-
-  CUtensorMap ma, mb;
-  if (!make_tensor_map(&ma, a, kBf16, M, K, lda_bytes, BM) ||
-      !make_tensor_map(&mb, w, kBf16, N, K, ldw_bytes, pair ? BN / 2 : BN))
-    return 2;
-
-  const int units = m_units * p.n_tiles;
-  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  if (pair) {
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 2;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.numAttrs = 2;
-    cfg.gridDim = dim3(2 * unsigned(std::min(units, clusters)));
-    return cudaLaunchKernelEx(&cfg, paired, ma, mb, p) == cudaSuccess ? 0 : 3;
-  }
   cfg.numAttrs = 1;
-  cfg.gridDim = dim3(units < num_sms ? units : num_sms);
   return cudaLaunchKernelEx(&cfg, single, ma, mb, p) == cudaSuccess ? 0 : 3;
 }
 
@@ -597,6 +825,19 @@ int gemm_bf16_launch(const uint16_t* a, int64_t lda, const uint16_t* w, int64_t 
                      int num_sms, cudaStream_t stream) {
   return launch_gemm(true, a, lda * 2, nullptr, w, ldw * 2, s_w, per_channel, bias, y, ldy, M, N, K,
                      gemm::kIdescBf16, num_sms, stream);
+}
+
+GemmPlan gemm_plan(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_bytes, int M, int N, int num_sms) {
+  int dev = 0;
+  GemmPlan none{};
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return none;
+  }
+  const void* k = reinterpret_cast<const void*>(gemm::gemm_kernel<false, true>);
+  if (!ensure_attributes(dev, k)) return none;
+  const int clusters = switches().pair ? pair_clusters(dev, k) : 0;
+  return plan_gemm(a, lda_bytes, w, ldw_bytes, M, N, dev, num_sms, clusters);
 }
 
 unsigned int gemm_read_and_clear_error() {

@@ -19,7 +19,26 @@ struct GemmParams {
   int m_tiles, n_tiles, group_n;
   int y_vec;
   uint32_t idesc;  // tcgen05 instruction descriptor (carries the two operand formats)
+  int hint_a, hint_b, hint_y;  // L2 eviction priority of qA / qW loads and Y stores (0 normal, 1 first, 2 last)
 };
+
+// Launch configuration of one GEMM call (host logic only).
+struct GemmPlan {
+  int two_sm;    // 1: CTA pairs on the two-SM MMA; 0: one CTA per tile
+  int grid;      // CTAs launched (persistent)
+  int m_tiles, n_tiles;
+  int group_n;   // raster group (column tiles per group)
+  int hint_a, hint_b, hint_y;
+};
+
+// The plan for operands a [M, lda_bytes] and w [N, ldw_bytes] on device `dev` with
+// `pair_clusters_available` co-resident CTA pairs: the two-SM mode needs at least two row
+// blocks, pairs on 3/4 of the SMs, and both operands in this device's own memory.
+GemmPlan plan_gemm(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_bytes, int M, int N, int dev,
+                   int num_sms, int pair_clusters_available);
+
+// The plan gemm_launch would use on the current device (queries pointer attributes and occupancy).
+GemmPlan gemm_plan(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_bytes, int M, int N, int num_sms);
 
 // Enqueues the persistent GEMM. Returns 0 on success, non-zero when the tensor maps could
 // not be encoded or the launch failed. qa/qw: 16-byte aligned, ld multiples of 16.

@@ -188,3 +188,32 @@ def tinyllama_weight(depth: int, layer_idx: int) -> torch.Tensor:
 def tinyllama_activations(M: int, depth: int, layer_idx: int) -> torch.Tensor:
     L = TINYLLAMA_LAYERS[layer_idx]
     return activations_normal(M, L.K, (TINYLLAMA, depth, layer_idx, M))
+
+
+# ---------------------------------------------------------------------------
+# Device-drawn tensors for timing-only workloads (never compared with the oracle)
+# ---------------------------------------------------------------------------
+
+def _device_seed(key: Sequence[int]) -> int:
+    return int(np.random.SeedSequence(list(key)).generate_state(1, dtype=np.uint64)[0] >> 1)
+
+
+def normal_device(rows: int, cols: int, key: Sequence[int], std: float, device) -> torch.Tensor:
+    """bf16 [rows, cols] ~ N(0, std^2) drawn on `device` by torch's generator seeded from `key`.
+    Used where only timing matters and host generation of gigabytes would dominate the run
+    (the TinyLlama sweep's 22 weight sets); parity tests use the host draws above."""
+    g = torch.Generator(device=device)
+    g.manual_seed(_device_seed(key))
+    x = torch.empty((rows, cols), dtype=torch.float32, device=device)
+    x.normal_(0.0, std, generator=g)
+    return x.to(torch.bfloat16)
+
+
+def tinyllama_weight_device(depth: int, layer_idx: int, device) -> torch.Tensor:
+    L = TINYLLAMA_LAYERS[layer_idx]
+    return normal_device(L.N, L.K, (TINYLLAMA, depth, layer_idx, 7), 0.02, device)
+
+
+def tinyllama_activations_device(M: int, copy: int, layer_idx: int, device) -> torch.Tensor:
+    L = TINYLLAMA_LAYERS[layer_idx]
+    return normal_device(M, L.K, (TINYLLAMA, copy, layer_idx, 8), 1.0, device)

@@ -94,6 +94,16 @@ size_t fp8_workspace_bytes(int64_t M, int64_t K, int64_t N);
 /* 1 when fp8_linear takes the decode GEMV path for this shape, 0 for the GEMM path. Host-only. */
 int fp8_uses_gemv(int64_t M, int64_t K, int64_t N);
 
+/* Sets the decode crossover: calls with M <= m (and K <= 32768) run the GEMV,
+ * larger M the GEMM. m is clamped to [0, 16] (16 is the GEMV's largest M; 0
+ * sends every shape to the GEMM); m < 0 only queries. Returns the previous
+ * value. The start-up value is 16, or FP8W8A8_GEMV_MAX_M from the environment.
+ * Process-wide; it changes which kernels later calls enqueue (and so
+ * fp8_workspace_bytes), never their results beyond the stated tolerance.
+ * ("[WIP] FP8 support": decode runs at sequence length < 16 and wants its own
+ * GEMV; where exactly to switch is a tuning choice.) Host-only. */
+int fp8_set_gemv_max_m(int m);
+
 /*
  * Quantize bf16 weights W [N, K] (stride ldw) to qW u8 [N, ldq] and scales s_w.
  * per_channel == 0: one scale, s_w[0] = amax(W)/448 ("Fp8 Quantization
@@ -277,6 +287,21 @@ fp8_status fp8_linear_weight_only(const void* a_bf16, int64_t M, int64_t K, int6
                                   const float* s_w, int per_channel, const void* bias_bf16,
                                   void* y_bf16, int64_t ldy, void* ws, size_t ws_bytes,
                                   fp8_stream_t stream);
+
+/*
+ * Diagnostics (no counterpart on the source pages): the launch the GEMM path of
+ * fp8_scaled_mm / fp8_linear would use for FP8 operands qa [M, ldqa] and
+ * qw [N, ldqw] (ld in bytes) on the current device. *two_sm = 1 when CTA pairs
+ * run the two-SM MMA (tcgen05 cta_group::2), which needs at least two 128-row
+ * blocks and both operands in the current device's own memory (cudaMalloc'd on
+ * it); any other memory (pinned or managed host memory, another GPU's memory)
+ * takes one CTA per tile, *two_sm = 0. *grid = CTAs launched; *group_n =
+ * column tiles per raster group. Output pointers may be NULL. Enqueues
+ * nothing; FP8_ERR_INVALID_ARG for non-positive sizes, FP8_ERR_CUDA or
+ * FP8_ERR_UNSUPPORTED_DEVICE when the device cannot be queried.
+ */
+fp8_status fp8_gemm_config(const uint8_t* qa, int64_t M, int64_t ldqa, const uint8_t* qw, int64_t N,
+                           int64_t ldqw, int* two_sm, int* grid, int* group_n);
 
 /*
  * Synchronizes `stream`, then reports and clears device-side errors recorded

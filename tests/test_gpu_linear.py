@@ -5,6 +5,8 @@ Y must lie within one bf16 ulp of the exact value plus K * 2^-23 * sum_k |a_k w_
 them. Output buffers carry canary guard bands to catch stray writes.
 """
 
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -86,7 +88,7 @@ def test_unaligned_config(idx):
 
 
 @pytest.mark.parametrize("layer", range(4))
-@pytest.mark.parametrize("M", [1, 15])
+@pytest.mark.parametrize("M", list(I.DECODE_MS))
 def test_decode_config_layers(layer, M):
     """Mistral-7B decode layers at full size; Y checked on all rows and 1536 sampled columns."""
     L = I.LLAMA8B_LAYERS[layer]
@@ -142,15 +144,37 @@ def test_prefill_config_full_size_sampled(layer):
     linear_parity(y, a, w, True, None, rows, cols, f"prefill {L.name}")
 
 
-@pytest.mark.parametrize("M", [1, 16, 64, 512, 4096])
-def test_tinyllama_sweep_sampled(M):
+@functools.lru_cache(maxsize=None)
+def _tinyllama_layer(depth, li, per_channel):
+    """Host weights of one TinyLlama linear, their oracle quantization on sampled columns, and
+    the library's quantized copy on the device (shared by every M of the sweep)."""
+    L = I.TINYLLAMA_LAYERS[li]
+    w = I.tinyllama_weight(depth, li)
+    cols = np.unique(np.r_[np.random.default_rng(7 + li).choice(L.N, 384, replace=False), 0, L.N - 1])
+    qw, s_w = F.fp8_quantize_weight(w.to(DEV), per_channel=per_channel)
+    return w, cols, oracle_weight(w, per_channel, cols), qw, s_w
+
+
+@pytest.mark.parametrize("depth", [0, I.TINYLLAMA_DEPTH - 1])
+@pytest.mark.parametrize("M", sorted(set(I.TINYLLAMA_MS) | {17}))
+def test_tinyllama_sweep_sampled(M, depth):
+    """Every M of the TinyLlama sweep (and M = 17, the first GEMM row count above the GEMV),
+    first and last layer of the stack, both weight modes: Y against the oracle on sampled rows
+    (all rows up to M = 64) and 386 sampled columns."""
+    from parity import assert_y_within_tolerance, f32, oracle_act
     for li, L in enumerate(I.TINYLLAMA_LAYERS):
-        w = I.tinyllama_weight(0, li)
-        a = I.tinyllama_activations(M, 0, li)
+        a = I.tinyllama_activations(M, depth, li)
         rows = np.arange(M) if M <= 64 else np.unique(np.r_[np.random.default_rng(M).choice(M, 30), M - 1])
+        qa, s_a = oracle_act(a, rows)
+        ad = a.to(DEV)
         for pc in (False, True):
-            y, _, _ = run_linear(a, w, pc, guard=False)
-            linear_parity(y, a, w, pc, None, rows, None, f"tinyllama {L.name} M={M} pc={pc}")
+            w, cols, (qw_o, s_w_o), qw, s_w = _tinyllama_layer(depth, li, pc)
+            fn = F.fp8_linear_channelwise if pc else F.fp8_linear
+            y = fn(ad, qw, s_w)
+            torch.cuda.synchronize()
+            assert F.fp8_last_device_status() == F.FP8_OK
+            assert_y_within_tolerance(f32(y)[np.ix_(rows, cols)], qa, s_a, qw_o, s_w_o, None,
+                                      f"tinyllama d={depth} {L.name} M={M} pc={pc}")
 
 
 # --------------------------------------------------------------------------- API behaviour
@@ -242,3 +266,34 @@ def test_gemv_in_kernel_quantization_codes(M, K):
     a = I.to_bf16(a)
     w = torch.eye(K, dtype=torch.bfloat16)
     check(a, w, False, None, f"identity M={M} K={K}")
+
+
+def test_pair_mode_needs_local_device_memory():
+    """The two-SM pair GEMM is planned only for operands in this GPU's own memory; a pinned
+    host buffer (reachable by the GPU) gets the single-CTA plan. Only the plan is queried:
+    nothing is launched on host memory."""
+    M, K, N = 512, 1024, 768
+    qa = torch.zeros((M, K), dtype=torch.uint8, device=DEV)
+    qw = torch.zeros((N, K), dtype=torch.uint8, device=DEV)
+    cfg_dev = F.fp8_gemm_config(qa, qw)
+    assert cfg_dev["two_sm"] and cfg_dev["grid"] % 2 == 0
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for qa_x, qw_x in ((qa.cpu().pin_memory(), qw), (qa, qw.cpu().pin_memory())):
+        cfg = F.fp8_gemm_config(qa_x, qw_x)
+        assert not cfg["two_sm"] and 0 < cfg["grid"] <= sms
+    # one row block: single CTA per tile as well
+    assert not F.fp8_gemm_config(qa[:100], qw)["two_sm"]
+
+
+@pytest.mark.parametrize("M,K,N", [(16384, 4096, 4096), (16384, 14336, 4096), (16384, 4096, 28672), (300, 4096, 512)])
+def test_gemm_raster_keeps_smaller_operand_hot(M, K, N):
+    """Launch plan of the prefill layers: W resident (one raster group) when it is the smaller
+    operand and fits the L2 budget, qA resident (groups of one column tile) otherwise."""
+    qa = torch.empty((M, K), dtype=torch.uint8, device=DEV)
+    qw = torch.empty((N, K), dtype=torch.uint8, device=DEV)
+    cfg = F.fp8_gemm_config(qa, qw)
+    n_tiles = (N + 255) // 256
+    if N * K <= 72 << 20 and N * K <= M * K:
+        assert cfg["group_n"] == n_tiles
+    elif M * K <= 72 << 20:
+        assert cfg["group_n"] == 1

@@ -60,12 +60,15 @@ def test_noalloc_matches_workspace_entry_point(L, M, K, N, per_channel):
         torch.cuda.synchronize()
         assert F.fp8_last_device_status() == F.FP8_OK
         # tolerance of the parity tests, from the oracle's quantization of the same inputs
+        # the same kernels on the same inputs: identical bits to the workspace entry point
+        assert torch.equal(y, y_ref), f"call {call}: differs from the workspace entry point"
+        # and within the parity tolerance of the oracle on the same seeded inputs
         qa_o, s_a_o = oracle_act(a)
         qw_o, s_w_o = oracle_weight(w, per_channel)
         y_o = O.scaled_mm(qa_o, s_a_o, qw_o, s_w_o, f32(bias))
         tol = O.tolerance(qa_o, s_a_o, qw_o, s_w_o, y_o)
-        diff = np.abs(f32(y).astype(np.float64) - f32(y_ref).astype(np.float64))
-        assert np.all(diff <= tol), f"call {call}: max diff/tol {np.nanmax(diff / tol)}"
+        diff = np.abs(f32(y).astype(np.float64) - y_o.astype(np.float64))
+        assert np.all(diff <= tol), f"call {call}: max diff/tol against the oracle {np.nanmax(diff / tol)}"
 
 
 @pytest.mark.gpu
