@@ -300,28 +300,34 @@ def measure_sweep(torch, F, I, dev, args, fp8_tflops, hbm_gbs):
 
 
 def measure_crossover(torch, F, I, dev, args):
-    """GEMV against GEMM for the same calls at M around the threshold: Mistral-7B decode
-    linears (three weight copies rotated past L2) and the TinyLlama linears (22 layers)."""
+    """Decode GEMV against the GEMM path for the same calls at M around the crossover, on the
+    Mistral-7B decode linears (three weight copies rotated past L2) and the TinyLlama linears
+    (22 layers): the GEMV (up to 32 tokens), the GEMM with the library's K split, and the GEMM
+    with K unsplit (FP8W8A8_GEMM_SPLITK=1)."""
     res = {}
     prev = F.fp8_set_gemv_max_m(-1)
     fams = {"mistral7b": (I.LLAMA8B_LAYERS, [[F.fp8_quantize_weight(I.decode_weight(i, c).to(dev))
                                                for i in range(4)] for c in range(3)]),
             "tinyllama": (I.TINYLLAMA_LAYERS, [[F.fp8_quantize_weight(I.tinyllama_weight_device(d, j, dev))
                                                 for j in range(4)] for d in range(I.TINYLLAMA_DEPTH)])}
-    Ms = (8, 12, 15, 16, 17, 24, 32)
+    Ms = (8, 16, 17, 24, 32, 64, 128, 256, 512)
     try:
         for fam, (layers, Wq) in fams.items():
-            Kmax = max(L.K for L in layers)
-            A = [torch.randn((32, L.K), device=dev).to(torch.bfloat16) for L in layers]
-            Y = [torch.empty((32, L.N), dtype=torch.bfloat16, device=dev) for L in layers]
-            ws = torch.empty(F.fp8_workspace_bytes(32, Kmax, 1) + 256, dtype=torch.uint8, device=dev)
+            A = [I.normal_device(max(Ms), L.K, (1005, j), 1.0, dev) for j, L in enumerate(layers)]
+            Y = [torch.empty((max(Ms), L.N), dtype=torch.bfloat16, device=dev) for L in layers]
+            ws = torch.empty(max(F.fp8_workspace_bytes(m, L.K, L.N) for m in Ms for L in layers) + 256,
+                             dtype=torch.uint8, device=dev)
             rows = []
             for M in Ms:
                 row = {"M": M}
-                for path, thr in (("gemv", 16), ("gemm", 0)):
-                    if path == "gemv" and M > 16:
+                for path, thr, split_env in (("gemv", 32, None), ("gemm", 0, None), ("gemm_unsplit", 0, "1")):
+                    if path == "gemv" and M > 32:
                         continue
                     F.fp8_set_gemv_max_m(thr)
+                    if split_env is None:
+                        os.environ.pop("FP8W8A8_GEMM_SPLITK", None)
+                    else:
+                        os.environ["FP8W8A8_GEMM_SPLITK"] = split_env
 
                     def step(M=M):
                         for Wc in Wq:
@@ -330,6 +336,7 @@ def measure_crossover(torch, F, I, dev, args):
 
                     t = time_loop(torch, graph_of(torch, step).replay, 10, 3)
                     row[path + "_us_per_linear"] = round(t * 1e3 / (len(Wq) * len(layers)), 2)
+                os.environ.pop("FP8W8A8_GEMM_SPLITK", None)
                 rows.append(row)
             both = [r for r in rows if "gemv_us_per_linear" in r]
             wins = [r["M"] for r in both if r["gemv_us_per_linear"] <= r["gemm_us_per_linear"]]
@@ -337,6 +344,7 @@ def measure_crossover(torch, F, I, dev, args):
             del A, Y, ws
     finally:
         F.fp8_set_gemv_max_m(prev)
+        os.environ.pop("FP8W8A8_GEMM_SPLITK", None)
     del fams
     torch.cuda.synchronize()
     return res

@@ -65,7 +65,7 @@ _SIGNATURES = {
     "fp8_weight_only_workspace_bytes": (_sz, [_i64, _i64, _i64]),
     "fp8_linear_weight_only": (_int, [_vp, _i64, _i64, _i64, _vp, _int, _i64, _i64, _vp, _int, _vp, _vp, _i64,
                                       _vp, _sz, _vp]),
-    "fp8_gemm_config": (_int, [_vp, _i64, _i64, _vp, _i64, _i64, _vp, _vp, _vp]),
+    "fp8_gemm_config": (_int, [_vp, _i64, _i64, _vp, _i64, _i64, _i64, _sz, _vp, _vp, _vp, _vp]),
     "fp8_last_device_status": (_int, [_vp]),
     "fp8_selftest_timeout": (_int, [_i64, _vp]),
     "fp8_status_string": (ctypes.c_char_p, [_int]),
@@ -365,12 +365,22 @@ def fp8_last_device_status(stream=None) -> int:
     return int(lib().fp8_last_device_status(s))
 
 
-def fp8_gemm_config(qa, qw) -> dict:
-    """The GEMM launch the library would use for FP8 operands qa [M, ld] and qw [N, ld] on the
-    current device: {"two_sm": bool, "grid": int, "group_n": int}. Enqueues nothing."""
-    two, grid, gn = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+def fp8_gemm_config(qa, qw, K: Optional[int] = None, ws_bytes: int = 0) -> dict:
+    """The GEMM launch the library would use for FP8 operands qa [M, ld] and qw [N, ld] (K columns;
+    default: the row length) with a linear workspace of ws_bytes, on the current device:
+    {"two_sm": bool, "grid": int, "group_n": int, "splits": int}. Enqueues nothing."""
+    two, grid, gn, sp = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    K = qa.shape[1] if K is None else int(K)
     st = lib().fp8_gemm_config(qa.data_ptr(), qa.shape[0], qa.stride(0), qw.data_ptr(), qw.shape[0], qw.stride(0),
-                               ctypes.byref(two), ctypes.byref(grid), ctypes.byref(gn))
+                               K, int(ws_bytes), ctypes.byref(two), ctypes.byref(grid), ctypes.byref(gn),
+                               ctypes.byref(sp))
     if st != FP8_OK:
         raise FP8Error(st, "fp8_gemm_config")
-    return {"two_sm": bool(two.value), "grid": grid.value, "group_n": gn.value}
+    return {"two_sm": bool(two.value), "grid": grid.value, "group_n": gn.value, "splits": sp.value}
+
+
+def min_workspace_bytes(M: int, K: int, N: int) -> int:
+    """The least workspace fp8_linear accepts for this shape (no K split): 0 for decode shapes."""
+    if M <= 0 or K <= 0 or fp8_uses_gemv(M, K, N):
+        return 0
+    return FP8_QUANT_WORKSPACE_BYTES + M * min_ld(K)

@@ -61,12 +61,12 @@ fp8_status current_device(int* sms) {
   return FP8_OK;
 }
 
-// Largest M that runs the decode GEMV: FP8W8A8_GEMV_MAX_M at start-up (default 16), then
-// fp8_set_gemv_max_m.
+// Largest M that runs the decode GEMV: FP8W8A8_GEMV_MAX_M at start-up (default
+// gemv::kDefaultMaxM), then fp8_set_gemv_max_m; never above gemv::kMaxTokens.
 std::atomic<int>& gemv_max_m_value() {
   static std::atomic<int> v{[] {
     const char* e = std::getenv("FP8W8A8_GEMV_MAX_M");
-    const int x = e ? std::atoi(e) : gemv::kMaxTokens;
+    const int x = e ? std::atoi(e) : gemv::kDefaultMaxM;
     return std::max(0, std::min(x, gemv::kMaxTokens));
   }()};
   return v;
@@ -264,7 +264,7 @@ fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uin
   const int KT = (p.K + kTileK - 1) / kTileK;
   const bool dyn = mode == kModeQuantize;
   const int max_slice = mode == kModeBf16 ? kMaxSliceBf16 : kMaxSlice;
-  const int NT = p.M <= 8 ? 1 : 2;
+  const int NT = p.M <= 8 ? 1 : p.M <= 16 ? 2 : 4;
   const int act_rows = 8 * NT;
   const KernelFn kfn = kernel_for(NT, mode, fmt_a, fmt_w);
   const int smem_limit = gemv_smem_limit(kfn);
@@ -392,10 +392,22 @@ fp8_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
   } while (0)
 
 // Decode shapes need no workspace (the GEMV quantizes A itself); the GEMM path holds the
-// partial amax values, s_a and qA [M, round_up(K, 16)].
+// partial amax values, s_a and qA [M, round_up(K, 16)]: the least a GEMM-path call accepts.
 size_t linear_ws_bytes(int64_t M, int64_t K) {
   if (M <= 0 || K <= 0 || use_gemv(M, K)) return 0;
   return FP8_QUANT_WORKSPACE_BYTES + size_t(M) * size_t(round_up16(K));
+}
+
+size_t round_up_256(size_t b) { return (b + 255) / 256 * 256; }
+
+// What fp8_workspace_bytes reports: the above plus, from the next 256-byte boundary, the
+// split-K fp32 partials of the split a 152-SM GB300 (76 CTA pairs) would use.
+// A call given less (but at least linear_ws_bytes) splits only as far as its workspace holds.
+size_t linear_ws_bytes_full(int64_t M, int64_t K, int64_t N) {
+  const size_t base = linear_ws_bytes(M, K);
+  if (base == 0 || N <= 0) return base;
+  const int S = fp8k::plan_splits(M, N, K, 152, 76, SIZE_MAX);
+  return S > 1 ? round_up_256(base) + fp8k::splitk_bytes(M, N, S) : base;
 }
 
 fp8_status linear_impl(const void* a, int64_t M, int64_t K, int64_t lda, int fmt_a, const float* s_static,
@@ -429,6 +441,12 @@ fp8_status linear_impl(const void* a, int64_t M, int64_t K, int64_t lda, int fmt
   float* partials = reinterpret_cast<float*>(wsb);
   uint8_t* qa = wsb + kWsQaOffset;
   const int64_t ldqa = round_up16(K);
+  // split-K scratch past qA, when the workspace holds it
+  const size_t split_off = round_up_256(linear_ws_bytes(M, K));
+  const fp8k::SplitK sk =
+      ws_bytes > split_off
+          ? fp8k::gemm_split_plan(qa, ldqa, qw, ldqw, int(M), int(N), int(K), sms, wsb + split_off, ws_bytes - split_off)
+          : fp8k::SplitK();
   const float* s_a = s_static;
   if (s_static == nullptr) {
     float* s_dyn = reinterpret_cast<float*>(wsb + kWsScaleOffset);
@@ -440,7 +458,7 @@ fp8_status linear_impl(const void* a, int64_t M, int64_t K, int64_t lda, int fmt
     FP8_TRY(launch_cast(A, nullptr, 0, s_static, nullptr, qa, ldqa, fmt_a, sms, st, true));
   }
   if (gemm_launch(qa, ldqa, s_a, qw, ldqw, s_w, per_channel, static_cast<const uint16_t*>(bias),
-                  static_cast<uint16_t*>(y), ldy, int(M), int(N), int(K), fmt_a, fmt_w, sms, st) != 0)
+                  static_cast<uint16_t*>(y), ldy, int(M), int(N), int(K), fmt_a, fmt_w, sms, st, sk) != 0)
     return FP8_ERR_CUDA;
   return FP8_OK;
 }
@@ -598,8 +616,7 @@ fp8_status weight_only_impl(const void* a, int64_t M, int64_t K, int64_t lda, co
 FP8_API int64_t fp8_min_ld(int64_t K) { return K <= 0 ? 16 : round_up16(K); }
 
 FP8_API size_t fp8_workspace_bytes(int64_t M, int64_t K, int64_t N) {
-  (void)N;
-  return linear_ws_bytes(std::max<int64_t>(M, 0), std::max<int64_t>(K, 0));
+  return linear_ws_bytes_full(std::max<int64_t>(M, 0), std::max<int64_t>(K, 0), std::max<int64_t>(N, 0));
 }
 
 FP8_API int fp8_set_gemv_max_m(int m) {
@@ -695,15 +712,28 @@ FP8_API fp8_status fp8_linear_weight_only(const void* a_bf16, int64_t M, int64_t
 }
 
 FP8_API fp8_status fp8_gemm_config(const uint8_t* qa, int64_t M, int64_t ldqa, const uint8_t* qw, int64_t N,
-                                   int64_t ldqw, int* two_sm, int* grid, int* group_n) {
-  if (M <= 0 || N <= 0 || M > kMaxDim || N > kMaxDim || ldqa <= 0 || ldqw <= 0) return FP8_ERR_INVALID_ARG;
+                                   int64_t ldqw, int64_t K, size_t ws_bytes, int* two_sm, int* grid, int* group_n,
+                                   int* splits) {
+  if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim || ldqa <= 0 || ldqw <= 0)
+    return FP8_ERR_INVALID_ARG;
   int sms = 0;
   FP8_TRY(current_device(&sms));
   const fp8k::GemmPlan pl = fp8k::gemm_plan(qa, ldqa, qw, ldqw, int(M), int(N), sms);
   if (pl.grid <= 0) return FP8_ERR_CUDA;
+  // the split fp8_linear would take with a workspace of ws_bytes (the planning needs no memory)
+  const size_t split_off = round_up_256(linear_ws_bytes(M, K));
+  int S = 1;
+  if (!use_gemv(M, K) && ws_bytes > split_off) {
+    alignas(256) static unsigned char probe[256];
+    S = fp8k::gemm_split_plan(qa, ldqa, qw, ldqw, int(M), int(N), int(K), sms, probe, ws_bytes - split_off).splits;
+  }
+  const int m_units = pl.two_sm ? (pl.m_tiles + 1) / 2 : pl.m_tiles;
   if (two_sm) *two_sm = pl.two_sm;
-  if (grid) *grid = pl.grid;
+  if (grid) *grid = S > 1 ? (pl.two_sm ? std::min(pl.grid, 2 * m_units * pl.n_tiles * S)
+                                       : std::min(sms, m_units * pl.n_tiles * S))
+                          : pl.grid;
   if (group_n) *group_n = pl.group_n;
+  if (splits) *splits = S;
   return FP8_OK;
 }
 

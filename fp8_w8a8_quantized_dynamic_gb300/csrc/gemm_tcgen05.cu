@@ -311,11 +311,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   const uint32_t rank = kTwo ? cluster_rank() : 0u;
   const bool leader = rank == 0;
   const int m_units = kTwo ? (p.m_tiles + 1) / 2 : p.m_tiles;
-  const int num_tiles = m_units * p.n_tiles;
+  const int S = p.k_splits;  // split-K: work unit = (tile, split); the splits of a tile are adjacent
+  const int num_tiles = m_units * p.n_tiles * S;
   const int first_unit = kTwo ? int(blockIdx.x >> 1) : int(blockIdx.x);
   const int unit_stride = kTwo ? int(gridDim.x >> 1) : int(gridDim.x);
-  auto coords = [&](int unit, int& m_idx, int& n_idx) {
-    tile_coords(unit, p, m_units, m_idx, n_idx);
+  auto coords = [&](int unit, int& m_idx, int& n_idx, int& ks) {
+    const int tu = unit / S;
+    ks = unit - tu * S;
+    tile_coords(tu, p, m_units, m_idx, n_idx);
     if (kTwo) m_idx = 2 * m_idx + int(rank);
   };
   const int num_kb = (p.K + kElemsPerStage - 1) / kElemsPerStage;
@@ -371,9 +374,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       uint32_t it = 0;
       bool ok = true;
       for (int tile = first_unit; tile < num_tiles && ok; tile += unit_stride) {
-        int m_idx, n_idx;
-        coords(tile, m_idx, n_idx);
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        int m_idx, n_idx, ks;
+        coords(tile, m_idx, n_idx, ks);
+        const int kb_end = min(num_kb, (ks + 1) * p.kb_per_split);
+        for (int kb = ks * p.kb_per_split; kb < kb_end; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
           if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, &g_gemm_error)) {
@@ -422,7 +426,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         }
         tmem_fence_after();
         const uint32_t d_tmem = tmem_base + ab * BN;
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        const int ks = tile % S;
+        const int kb_begin = ks * p.kb_per_split, kb_end = min(num_kb, kb_begin + p.kb_per_split);
+        for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
           if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, &g_gemm_error)) {
@@ -437,7 +443,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
           for (int kk = 0; kk < BK / kMmaK; ++kk) {
             // advance the start address by 32 bytes of K inside the swizzled 128-byte row
             mma_issue<kBf16, kTwo>(d_tmem, adesc + uint64_t(kk * kMmaK >> 4), bdesc + uint64_t(kk * kMmaK >> 4),
-                                   idesc, (kb | kk) != 0 ? 1u : 0u);
+                                   idesc, (kb != kb_begin || kk != 0) ? 1u : 0u);
           }
           mma_commit<kTwo>(smem_u32(&ctl->empty[s]));  // frees the stage once these MMAs have read it
         }
@@ -461,8 +467,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     const uint32_t tempty_bar = kTwo ? map_to_rank(smem_u32(&ctl->tempty[0]), 0) : smem_u32(&ctl->tempty[0]);
     uint32_t acc_it = 0;
     for (int tile = first_unit; tile < num_tiles; tile += unit_stride, ++acc_it) {
-      int m_idx, n_idx;
-      coords(tile, m_idx, n_idx);
+      int m_idx, n_idx, ks;
+      coords(tile, m_idx, n_idx, ks);
       const int ab = acc_it % kAccBufs;
       const uint32_t aph = (acc_it / kAccBufs) & 1u;
       // column scales/bias of this tile, double-buffered by accumulator: a warp can only
@@ -479,19 +485,49 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       }
       // publishes the column tables; a set abort flag makes all epilogue warps leave together
       if (epi_bar_any(*abort_flag != 0)) break;
-      // after a timeout, skip to the next barrier above, which ends the loop uniformly
-      // one lane waits and the warp follows its verdict: tcgen05.ld needs a converged warp
+      // one lane per warp waits; after a timeout every warp skips to the barrier above, which
+      // then ends the loop uniformly (tcgen05.ld needs a converged warp)
       bool ok = true;
       if (lane == 0 && !mbar_wait_bounded(smem_u32(&ctl->tfull[ab]), aph, abort_flag, &g_gemm_error)) {
         fail(kSiteTfull);
         ok = false;
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) continue;
+      if (epi_bar_any(!ok)) continue;  // the four warps take the same path
       tmem_fence_after();
       const int m = m_idx * BM + row_in_tile;
       uint16_t* yrow = p.y + (int64_t)m * p.ldy;
       const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + ab * BN;
+      if (S > 1) {
+        // split-K: this unit's fp32 partial rows go to the workspace (unscaled)
+        float* prow = p.part + ((int64_t)ks * p.M + m) * p.ldp;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          const int n0 = n_idx * BN + c * 32;
+          if (n0 >= p.N) break;  // warp-uniform
+          uint32_t r[32];
+          tmem_ld32(tbase + c * 32, r);
+          if (m < p.M) {
+            if (n0 + 32 <= p.N) {
+              float4* dst = reinterpret_cast<float4*>(prow + n0);
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                     __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (n0 + j < p.N) prow[n0 + j] = __uint_as_float(r[j]);
+            }
+          }
+        }
+        tmem_fence_before();
+        if (kTwo)
+          arrive_cluster(tempty_bar + ab * uint32_t(sizeof(uint64_t)));
+        else
+          mbar_arrive(tempty_bar + ab * uint32_t(sizeof(uint64_t)));
+        continue;
+      }
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         const int n0 = n_idx * BN + c * 32;
@@ -563,6 +599,56 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(tmem_base), "n"(kTmemCols) : "memory");
     else
       asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem_base), "n"(kTmemCols) : "memory");
+  }
+}
+
+// Split-K epilogue: Y[m, n] = bf16(s_a * s_w[n] * sum_j part[j][m][n] (+ bias[n])), the splits
+// summed in order 0, 1, ... (deterministic). One thread per four consecutive columns of a row;
+// the partials were written by the GEMM just before (L2-resident), read once.
+__global__ void __launch_bounds__(256)
+splitk_reduce_kernel(const float* __restrict__ part, int64_t ldp, int splits, int M, int N,
+                     const float* __restrict__ s_a, const float* __restrict__ s_w, int per_channel,
+                     const uint16_t* __restrict__ bias, uint16_t* __restrict__ y, int64_t ldy, int y_vec) {
+  pdl_trigger();
+  pdl_wait();  // the partials come from the GEMM just before
+  const float sa = s_a ? *s_a : 1.0f;
+  const int c4 = (N + 3) >> 2;
+  const int64_t items = int64_t(M) * c4;
+  const int64_t plane = int64_t(M) * ldp;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < items; i += int64_t(gridDim.x) * blockDim.x) {
+    const int m = int(i / c4);
+    const int n = int(i - int64_t(m) * c4) * 4;
+    const float* src = part + int64_t(m) * ldp + n;
+    float4 acc = __ldcs(reinterpret_cast<const float4*>(src));
+    int j = 1;
+    for (; j + 3 < splits; j += 4) {  // four loads in flight, summed in split order
+      const float4 v1 = __ldcs(reinterpret_cast<const float4*>(src + j * plane));
+      const float4 v2 = __ldcs(reinterpret_cast<const float4*>(src + (j + 1) * plane));
+      const float4 v3 = __ldcs(reinterpret_cast<const float4*>(src + (j + 2) * plane));
+      const float4 v4 = __ldcs(reinterpret_cast<const float4*>(src + (j + 3) * plane));
+      acc.x += v1.x; acc.y += v1.y; acc.z += v1.z; acc.w += v1.w;
+      acc.x += v2.x; acc.y += v2.y; acc.z += v2.z; acc.w += v2.w;
+      acc.x += v3.x; acc.y += v3.y; acc.z += v3.z; acc.w += v3.w;
+      acc.x += v4.x; acc.y += v4.y; acc.z += v4.z; acc.w += v4.w;
+    }
+    for (; j < splits; ++j) {
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(src + j * plane));
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+    float o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int nn = min(n + e, N - 1);  // columns past N are computed on a valid index, not stored
+      o[e] = fmaf(a4[e], sa * s_w[per_channel ? nn : 0], bias ? bf16_bits_to_float(bias[nn]) : 0.0f);
+    }
+    uint16_t* yr = y + int64_t(m) * ldy;
+    if (y_vec && n + 4 <= N) {
+      *reinterpret_cast<uint2*>(yr + n) = make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
+    } else {
+      for (int e = 0; e < 4; ++e)
+        if (n + e < N) yr[n + e] = __bfloat16_as_ushort(__float2bfloat16_rn(o[e]));
+    }
   }
 }
 
@@ -713,6 +799,7 @@ GemmPlan plan_gemm(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_
               local_device_memory(a, dev) && local_device_memory(w, dev);
   const int m_units = pl.two_sm ? (pl.m_tiles + 1) / 2 : pl.m_tiles;
   const int units = m_units * pl.n_tiles;
+  pl.splits = 1;
   pl.grid = pl.two_sm ? 2 * std::min(units, pair_clusters_available) : std::min(units, num_sms);
   // raster: keep the smaller operand hot in L2 when it fits the budget, stream the other once
   const int64_t a_bytes = int64_t(M) * lda_bytes, w_bytes = int64_t(N) * ldw_bytes;
@@ -738,10 +825,74 @@ GemmPlan plan_gemm(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_
 
 namespace {
 
+size_t round_up_256(size_t b) { return (b + 255) / 256 * 256; }
+
+// Split count for `units` work units on `slots` parallel slots with `num_kb` K blocks each.
+// Time is modelled in K blocks of one unit: ceil(units * S / slots) waves of ceil(num_kb / S)
+// blocks, plus the cost of splitting, measured on a GB300 at about 8 us per linear (the reduce
+// kernel's launch and dependency wait, the partial stores and loads): about 18 K blocks of one
+// unit (~0.45 us each while the weight streams through few SMs). A split must save 15 %.
+int choose_splits(int units, int slots, int num_kb, int max_splits) {
+  constexpr double kSplitCost = 18.0;
+  auto cost = [&](int S, int kbs) {
+    const double waves = double((int64_t(units) * S + slots - 1) / slots);
+    return waves * kbs + (S > 1 ? kSplitCost : 0.0);
+  };
+  const double base = cost(1, num_kb);
+  int best = 1;
+  double best_cost = base;
+  for (int S = 2; S <= std::min(max_splits, num_kb); ++S) {
+    const int kbs = (num_kb + S - 1) / S;
+    if ((num_kb + kbs - 1) / kbs != S) continue;  // every split owns blocks
+    const double c = cost(S, kbs);
+    if (c < best_cost) {
+      best = S;
+      best_cost = c;
+    }
+  }
+  return best_cost < 0.85 * base ? best : 1;
+}
+
+constexpr int kMaxSplits = 16;
+
+}  // namespace
+
+size_t splitk_bytes(int64_t M, int64_t N, int splits) {
+  if (splits <= 1 || M <= 0 || N <= 0) return 0;
+  const int64_t ldp = (N + 3) / 4 * 4;
+  return size_t(splits) * size_t(M) * size_t(ldp) * 4;
+}
+
+int plan_splits(int64_t M, int64_t N, int64_t K, int num_sms, int pair_slots, size_t ws_bytes) {
+  using namespace gemm;
+  if (M <= 0 || N <= 0 || K <= 0) return 1;
+  const int m_tiles = int((M + BM - 1) / BM), n_tiles = int((N + BN - 1) / BN);
+  const int num_kb = int((K + BK - 1) / BK);
+  const bool two = pair_slots > 0 && m_tiles >= 2 && 2 * pair_slots >= (3 * num_sms) / 4;
+  const int units = (two ? (m_tiles + 1) / 2 : m_tiles) * n_tiles;
+  const int slots = two ? pair_slots : num_sms;
+  // the partials should stay in L2 (they are written once and read once by the tile's last CTA)
+  const size_t cap = std::min(ws_bytes, size_t(64) << 20);
+  int max_s = kMaxSplits;
+  while (max_s > 1 && splitk_bytes(M, N, max_s) > cap) --max_s;
+  const int forced = env_int("FP8W8A8_GEMM_SPLITK", 0);  // measurement override
+  if (forced > 0) {
+    // the largest count not above the request for which every split owns K blocks
+    const int S = std::max(1, std::min({forced, max_s, num_kb}));
+    const int kbs = (num_kb + S - 1) / S;
+    return (num_kb + kbs - 1) / kbs;
+  }
+  // measured: with CTA pairs (two or more row blocks) a split never paid for itself
+  if (two) return 1;
+  return choose_splits(units, slots, num_kb, max_s);
+}
+
+namespace {
+
 template <bool kBf16>
 int launch_kind(const void* a, int64_t lda_bytes, const float* s_a, const void* w, int64_t ldw_bytes,
                 const float* s_w, int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy, int M, int N,
-                int K, uint32_t idesc, int num_sms, cudaStream_t stream) {
+                int K, uint32_t idesc, int num_sms, cudaStream_t stream, const SplitK& split) {
   using namespace gemm;
   auto single = gemm_kernel<kBf16, false>;
   auto two_sm = gemm_kernel<kBf16, true>;
@@ -751,7 +902,11 @@ int launch_kind(const void* a, int64_t lda_bytes, const float* s_a, const void* 
       !ensure_attributes(dev, reinterpret_cast<const void*>(two_sm)))
     return 1;
   const int clusters = switches().pair ? pair_clusters(dev, reinterpret_cast<const void*>(two_sm)) : 0;
-  const GemmPlan pl = plan_gemm(a, lda_bytes, w, ldw_bytes, M, N, dev, num_sms, clusters);
+  GemmPlan pl = plan_gemm(a, lda_bytes, w, ldw_bytes, M, N, dev, num_sms, clusters);
+  const int S = std::max(1, split.splits);
+  const int num_kb = kBf16 ? (K + BK / 2 - 1) / (BK / 2) : (K + BK - 1) / BK;  // K blocks of 128 bytes
+  const int units = (pl.two_sm ? (pl.m_tiles + 1) / 2 : pl.m_tiles) * pl.n_tiles * S;
+  pl.grid = pl.two_sm ? 2 * std::min(units, clusters) : std::min(units, num_sms);
 
   GemmParams p;
   p.M = M;
@@ -771,6 +926,11 @@ int launch_kind(const void* a, int64_t lda_bytes, const float* s_a, const void* 
   p.hint_a = pl.hint_a;
   p.hint_b = pl.hint_b;
   p.hint_y = pl.hint_y;
+  p.k_splits = S;
+  p.kb_per_split = (num_kb + S - 1) / S;
+  p.part = split.part;
+  p.ldp = split.ldp;
+  if (S > 1 && (split.part == nullptr || (num_kb + p.kb_per_split - 1) / p.kb_per_split != S)) return 4;
 
   CUtensorMap ma, mb;
   if (!make_tensor_map(&ma, a, kBf16, M, K, lda_bytes, BM) ||
@@ -787,44 +947,59 @@ int launch_kind(const void* a, int64_t lda_bytes, const float* s_a, const void* 
   if (pl.two_sm) {
     // Launched without programmatic stream serialization: the pair's grid starts only after
     // the kernel before it has finished, so no CTA pair becomes resident while CTAs of an
-    // earlier GEMM grid still run (its own trigger still lets the next kernel start early).
+    // earlier kernel still hold the SMs (its own trigger still lets the next kernel start early).
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, two_sm, ma, mb, p) == cudaSuccess ? 0 : 3;
+    if (cudaLaunchKernelEx(&cfg, two_sm, ma, mb, p) != cudaSuccess) return 3;
+  } else {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, single, ma, mb, p) != cudaSuccess) return 3;
   }
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, single, ma, mb, p) == cudaSuccess ? 0 : 3;
+  if (S == 1) return 0;
+  // the split-K epilogue, launched early (programmatic) so it is resident when the GEMM ends
+  const int64_t items = int64_t(M) * ((N + 3) / 4);
+  cudaLaunchConfig_t rc = {};
+  rc.blockDim = dim3(256);
+  rc.gridDim = dim3(unsigned(std::max<int64_t>(1, std::min<int64_t>((items + 255) / 256, int64_t(num_sms) * 8))));
+  rc.stream = stream;
+  cudaLaunchAttribute rattr[1];
+  rattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  rattr[0].val.programmaticStreamSerializationAllowed = 1;
+  rc.attrs = rattr;
+  rc.numAttrs = 1;
+  return cudaLaunchKernelEx(&rc, splitk_reduce_kernel, static_cast<const float*>(split.part), split.ldp, S, M, N,
+                            s_a, s_w, per_channel, bias, y, ldy, p.y_vec) == cudaSuccess ? 0 : 3;
 }
 
 // Shared launch: operands are FP8 (ld in bytes) or bf16 (ld in bytes as well).
 int launch_gemm(bool bf16, const void* a, int64_t lda_bytes, const float* s_a, const void* w, int64_t ldw_bytes,
                 const float* s_w, int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy, int M, int N,
-                int K, uint32_t idesc, int num_sms, cudaStream_t stream) {
+                int K, uint32_t idesc, int num_sms, cudaStream_t stream, const SplitK& split) {
   return bf16 ? launch_kind<true>(a, lda_bytes, s_a, w, ldw_bytes, s_w, per_channel, bias, y, ldy, M, N, K, idesc,
-                                  num_sms, stream)
+                                  num_sms, stream, split)
               : launch_kind<false>(a, lda_bytes, s_a, w, ldw_bytes, s_w, per_channel, bias, y, ldy, M, N, K, idesc,
-                                   num_sms, stream);
+                                   num_sms, stream, split);
 }
 
 }  // namespace
 
 int gemm_launch(const uint8_t* qa, int64_t ldqa, const float* s_a, const uint8_t* qw, int64_t ldqw,
                 const float* s_w, int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy,
-                int M, int N, int K, int fmt_a, int fmt_w, int num_sms, cudaStream_t stream) {
+                int M, int N, int K, int fmt_a, int fmt_w, int num_sms, cudaStream_t stream, const SplitK& split) {
   return launch_gemm(false, qa, ldqa, s_a, qw, ldqw, s_w, per_channel, bias, y, ldy, M, N, K,
-                     gemm::make_idesc(fmt_a, fmt_w), num_sms, stream);
+                     gemm::make_idesc(fmt_a, fmt_w), num_sms, stream, split);
 }
 
 int gemm_bf16_launch(const uint16_t* a, int64_t lda, const uint16_t* w, int64_t ldw, const float* s_w,
                      int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy, int M, int N, int K,
                      int num_sms, cudaStream_t stream) {
   return launch_gemm(true, a, lda * 2, nullptr, w, ldw * 2, s_w, per_channel, bias, y, ldy, M, N, K,
-                     gemm::kIdescBf16, num_sms, stream);
+                     gemm::kIdescBf16, num_sms, stream, SplitK());
 }
 
 GemmPlan gemm_plan(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_bytes, int M, int N, int num_sms) {
@@ -838,6 +1013,27 @@ GemmPlan gemm_plan(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_
   if (!ensure_attributes(dev, k)) return none;
   const int clusters = switches().pair ? pair_clusters(dev, k) : 0;
   return plan_gemm(a, lda_bytes, w, ldw_bytes, M, N, dev, num_sms, clusters);
+}
+
+SplitK gemm_split_plan(const uint8_t* qa, int64_t ldqa, const uint8_t* qw, int64_t ldqw, int M, int N, int K,
+                       int num_sms, void* ws, size_t ws_bytes) {
+  SplitK sk;
+  if (ws == nullptr || ws_bytes == 0) return sk;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return sk;
+  }
+  const void* k = reinterpret_cast<const void*>(gemm::gemm_kernel<false, true>);
+  if (!ensure_attributes(dev, k)) return sk;
+  const int clusters = switches().pair ? pair_clusters(dev, k) : 0;
+  const GemmPlan pl = plan_gemm(qa, ldqa, qw, ldqw, M, N, dev, num_sms, clusters);
+  const int S = plan_splits(M, N, K, num_sms, pl.two_sm ? clusters : 0, ws_bytes);
+  if (S <= 1) return sk;
+  sk.splits = S;
+  sk.part = static_cast<float*>(ws);
+  sk.ldp = (int64_t(N) + 3) / 4 * 4;
+  return sk;
 }
 
 unsigned int gemm_read_and_clear_error() {

@@ -20,7 +20,27 @@ struct GemmParams {
   int y_vec;
   uint32_t idesc;  // tcgen05 instruction descriptor (carries the two operand formats)
   int hint_a, hint_b, hint_y;  // L2 eviction priority of qA / qW loads and Y stores (0 normal, 1 first, 2 last)
+  // split-K: each tile's K blocks are divided among k_splits work units (kb_per_split blocks
+  // each); every unit writes its unscaled fp32 partial to part [k_splits][M][ldp] and a reduce
+  // kernel sums them in split order and runs the epilogue. k_splits == 1: Y written directly.
+  int k_splits, kb_per_split;
+  float* part;
+  int64_t ldp;
 };
+
+// Workspace of a split-K GEMM: the fp32 partials [splits][M][ldp].
+struct SplitK {
+  int splits = 1;          // 1: K is not split
+  float* part = nullptr;
+  int64_t ldp = 0;         // row stride of the partials (elements, multiple of 4)
+};
+
+// Bytes of split-K workspace for `splits` (the fp32 partials).
+size_t splitk_bytes(int64_t M, int64_t N, int splits);
+
+// Split count for an M x N x K FP8 GEMM on a GPU with `num_sms` SMs and `pair_slots` co-resident
+// CTA pairs (0: no pair mode), limited to what `ws_bytes` of split workspace holds. Host logic.
+int plan_splits(int64_t M, int64_t N, int64_t K, int num_sms, int pair_slots, size_t ws_bytes);
 
 // Launch configuration of one GEMM call (host logic only).
 struct GemmPlan {
@@ -29,6 +49,7 @@ struct GemmPlan {
   int m_tiles, n_tiles;
   int group_n;   // raster group (column tiles per group)
   int hint_a, hint_b, hint_y;
+  int splits;    // K split count (1: none)
 };
 
 // The plan for operands a [M, lda_bytes] and w [N, ldw_bytes] on device `dev` with
@@ -42,10 +63,17 @@ GemmPlan gemm_plan(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_
 
 // Enqueues the persistent GEMM. Returns 0 on success, non-zero when the tensor maps could
 // not be encoded or the launch failed. qa/qw: 16-byte aligned, ld multiples of 16.
-// fmt_a / fmt_w: 0 = e4m3, 1 = e5m2.
+// fmt_a / fmt_w: 0 = e4m3, 1 = e5m2. split: K split (the GEMM, then the reduce kernel), or
+// the default of no split.
 int gemm_launch(const uint8_t* qa, int64_t ldqa, const float* s_a, const uint8_t* qw, int64_t ldqw,
                 const float* s_w, int per_channel, const uint16_t* bias, uint16_t* y, int64_t ldy,
-                int M, int N, int K, int fmt_a, int fmt_w, int num_sms, cudaStream_t stream);
+                int M, int N, int K, int fmt_a, int fmt_w, int num_sms, cudaStream_t stream,
+                const SplitK& split = SplitK());
+
+// The split plan gemm_launch would use for these FP8 operands with `ws_bytes` of split
+// workspace at `ws` (256-byte aligned), on the current device.
+SplitK gemm_split_plan(const uint8_t* qa, int64_t ldqa, const uint8_t* qw, int64_t ldqw, int M, int N, int K,
+                       int num_sms, void* ws, size_t ws_bytes);
 
 // bf16 x bf16 GEMM on the same kernel (tcgen05 kind::f16) for the weight-only product:
 //   Y[m, n] = bf16( s_w[n] * sum_k A[m, k] W[n, k]  (+ bias[n]) ).

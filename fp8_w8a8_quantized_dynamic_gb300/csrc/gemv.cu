@@ -30,7 +30,7 @@ KernelFn pick_mode(int mode, int fa, int fw) {
 }  // namespace
 
 KernelFn kernel_for(int NT, int mode, int fa, int fw) {
-  return NT == 1 ? pick_mode<1>(mode, fa, fw) : pick_mode<2>(mode, fa, fw);
+  return NT == 1 ? pick_mode<1>(mode, fa, fw) : NT == 2 ? pick_mode<2>(mode, fa, fw) : pick_mode<4>(mode, fa, fw);
 }
 
 // Failure-path self-test. A two-warp pipeline on a two-stage mbarrier ring, shaped like the

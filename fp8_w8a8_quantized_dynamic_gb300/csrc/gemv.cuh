@@ -155,7 +155,7 @@ __device__ __forceinline__ uint32_t abs_max_units(uint32_t m2, const uint4 (&v)[
   return m2;
 }
 
-// NT: n8 token tiles (1: M <= 8, 2: M <= 16). kMode: kModeQuantize (A is bf16 and quantized
+// NT: n8 token tiles (1: M <= 8, 2: M <= 16, 4: M <= 32). kMode: kModeQuantize (A is bf16 and quantized
 // here, dynamic scale or the static one when p.s_static is set), kModePrequant (qA and s_a
 // given) or kModeBf16 (weight-only: A stays bf16, each weight tile is up-converted to bf16 in
 // registers and multiplied with bf16 MMAs; s_a is 1). FA / FW: FP8 formats of the
@@ -516,8 +516,8 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
         for (int h = 0; h < 2; ++h) {
           const int row = warp * 16 + g + 8 * h, col = nt * 8 + 2 * t;
           const int owner = row / rows_per;
-          const uint32_t dst = part + r * kPartBytes +
-                               ((rank * rows_per + (row - owner * rows_per)) * kMaxTokens + col) * 4;
+          const uint32_t dst = part + r * part_bytes(p.act_rows) +
+                               ((rank * rows_per + (row - owner * rows_per)) * p.act_rows + col) * 4;
           st_dsmem_v2(dst, owner, acc[nt][2 * h], acc[nt][2 * h + 1]);
         }
       }
@@ -557,11 +557,11 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
       int q, r, row;
       const int n = item_n(i, q, r, row);
       if (n >= p.N) continue;
-      const uint32_t off = part + r * kPartBytes + ((row - r_begin) * kMaxTokens + 4 * q) * 4;
+      const uint32_t off = part + r * part_bytes(p.act_rows) + ((row - r_begin) * p.act_rows + 4 * q) * 4;
       // every source rank's partials are local now; summed in rank order (deterministic)
       float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
       for (uint32_t src = 0; src < nrank; ++src) {
-        const float4 v = lds_f4(off + src * rows_per * kMaxTokens * 4);
+        const float4 v = lds_f4(off + src * rows_per * p.act_rows * 4);
         sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
       }
       const bool first = i == int(threadIdx.x);

@@ -17,12 +17,14 @@ constexpr int kTileK = 128;                           // bytes of K per tile (on
 constexpr int kTileBytes = kRows * kTileK;            // 16 KB
 constexpr int kMaxStages = 12;
 constexpr int kMinStages = 4;
-constexpr int kMaxTokens = 16;
+constexpr int kMaxTokens = 32;                        // largest M (four n8 token tiles)
+constexpr int kDefaultMaxM = 16;                      // default decode crossover (M <= this runs the GEMV)
 constexpr int kMaxCluster = 8;
 constexpr int kMaxRowBlocks = 8;                      // per cluster (partials live in smem)
-// partials a rank receives for one row block: [source rank][its rows][16 tokens] fp32, at most
-// (kRows + kMaxCluster) rows in total (rows per rank rounded up)
-constexpr int kPartBytes = (kRows + kMaxCluster) * kMaxTokens * 4;
+
+// Partials a rank receives for one row block: [source rank][its rows][act_rows tokens] fp32,
+// at most (kRows + kMaxCluster) rows in total (rows per rank rounded up).
+__host__ __device__ inline int part_bytes(int act_rows) { return (kRows + kMaxCluster) * act_rows * 4; }
 constexpr int kMaxSlice = 4096;                       // bytes of K per rank
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kRegUnits = 8;  // 8-element units of A a consumer thread keeps in registers
@@ -54,7 +56,7 @@ struct Params {
   int stages;          // ring depth
   int row_blocks;      // ceil(N / kRows)
   int num_clusters;    // C
-  int act_rows;        // token rows staged in smem: 8 * NT
+  int act_rows;        // token rows staged in smem (8 * NT); also the token stride of the partials
   int head_tiles;      // weight tiles issued before the activation loads have landed
   int cluster_amax;    // dynamic scale: 1 = exchange slice maxima over the cluster, 0 = every CTA reads all of A
   int scratch_a;       // quantize mode: 0 = A read with per-thread loads; 1 = all of A, 2 = this rank's
@@ -72,12 +74,12 @@ __host__ __device__ inline Layout layout(int stages, int act_stride, int act_row
   L.ring = 0;
   L.act = stages * kTileBytes;
   L.part = L.act + act_rows * act_stride;
-  L.bars = L.part + rb_per_cluster * kPartBytes;
+  L.bars = L.part + rb_per_cluster * part_bytes(act_rows);
   L.total = L.bars + (2 * kMaxStages + 2) * 8;
   return L;
 }
 
-// One instantiation of the kernel: NT n8 token tiles (1: M <= 8, 2: M <= 16), activation
+// One instantiation of the kernel: NT n8 token tiles (1: M <= 8, 2: M <= 16, 4: M <= 32), activation
 // mode (kMode*), FP8 formats of the activations (fa, unused for kModeBf16) and weights (fw).
 using KernelFn = void (*)(CUtensorMap, Params);
 KernelFn kernel_for(int NT, int mode, int fa, int fw);

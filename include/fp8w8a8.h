@@ -84,18 +84,23 @@ typedef enum fp8_format {
 /* Smallest valid leading dimension (bytes) of an FP8 matrix with K columns: K rounded up to 16 (16 for K == 0). */
 int64_t fp8_min_ld(int64_t K);
 
-/* Bytes of workspace fp8_linear / fp8_linear_channelwise need for this shape.
+/* Bytes of workspace fp8_linear / fp8_linear_channelwise use for this shape.
  * 0 for decode shapes (fp8_uses_gemv): the GEMV quantizes A itself. GEMM
- * shapes need FP8_QUANT_WORKSPACE_BYTES (partial amax values, s_a) plus the
- * quantized activations qA [M, fp8_min_ld(K)]. 0 when M or K is 0. Host-only,
- * never touches the device. */
+ * shapes need at least FP8_QUANT_WORKSPACE_BYTES (partial amax values, s_a)
+ * plus the quantized activations qA [M, fp8_min_ld(K)]. Shapes with too few
+ * output tiles to fill the GPU (small M) split K across CTAs when the
+ * workspace also holds, from the next 256-byte boundary, a per-tile arrival
+ * counter and fp32 partials [splits, M, N rounded up to 4]; the value returned
+ * includes that space for the split a GB300 (152 SMs) takes. A workspace
+ * between the two sizes works too, with a smaller split or none. 0 when M or
+ * K is 0. Host-only, never touches the device. */
 size_t fp8_workspace_bytes(int64_t M, int64_t K, int64_t N);
 
 /* 1 when fp8_linear takes the decode GEMV path for this shape, 0 for the GEMM path. Host-only. */
 int fp8_uses_gemv(int64_t M, int64_t K, int64_t N);
 
 /* Sets the decode crossover: calls with M <= m (and K <= 32768) run the GEMV,
- * larger M the GEMM. m is clamped to [0, 16] (16 is the GEMV's largest M; 0
+ * larger M the GEMM. m is clamped to [0, 32] (32 is the GEMV's largest M; 0
  * sends every shape to the GEMM); m < 0 only queries. Returns the previous
  * value. The start-up value is 16, or FP8W8A8_GEMV_MAX_M from the environment.
  * Process-wide; it changes which kernels later calls enqueue (and so
@@ -180,10 +185,12 @@ fp8_status fp8_linear_channelwise(const void* a_bf16, int64_t M, int64_t K, int6
  *
  * The scratch lives in one fixed array inside the library of
  * FP8_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads the library holds
- * until the process exits. A call needs fp8_workspace_bytes(M, K, N) of it:
- * nothing for decode shapes, and for GEMM shapes M * fp8_min_ld(K) may be at
- * most FP8_NOALLOC_SCRATCH_BYTES - 4352. Larger shapes are refused with
- * FP8_ERR_WORKSPACE before anything is enqueued. The call allocates nothing.
+ * until the process exits. A call needs the least workspace fp8_linear
+ * accepts: nothing for decode shapes, and for GEMM shapes M * fp8_min_ld(K)
+ * may be at most FP8_NOALLOC_SCRATCH_BYTES - 4352. Larger shapes are refused
+ * with FP8_ERR_WORKSPACE before anything is enqueued. The rest of the array
+ * serves a K split where one fits (the same launches fp8_linear makes with a
+ * workspace of FP8_NOALLOC_SCRATCH_BYTES). The call allocates nothing.
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
@@ -290,18 +297,22 @@ fp8_status fp8_linear_weight_only(const void* a_bf16, int64_t M, int64_t K, int6
 
 /*
  * Diagnostics (no counterpart on the source pages): the launch the GEMM path of
- * fp8_scaled_mm / fp8_linear would use for FP8 operands qa [M, ldqa] and
- * qw [N, ldqw] (ld in bytes) on the current device. *two_sm = 1 when CTA pairs
- * run the two-SM MMA (tcgen05 cta_group::2), which needs at least two 128-row
- * blocks and both operands in the current device's own memory (cudaMalloc'd on
- * it); any other memory (pinned or managed host memory, another GPU's memory)
- * takes one CTA per tile, *two_sm = 0. *grid = CTAs launched; *group_n =
- * column tiles per raster group. Output pointers may be NULL. Enqueues
- * nothing; FP8_ERR_INVALID_ARG for non-positive sizes, FP8_ERR_CUDA or
- * FP8_ERR_UNSUPPORTED_DEVICE when the device cannot be queried.
+ * fp8_linear (and fp8_scaled_mm, which never splits K) would use for FP8
+ * operands qa [M, ldqa] and qw [N, ldqw] (ld in bytes), K columns, and a
+ * linear workspace of ws_bytes, on the current device. *two_sm = 1 when CTA
+ * pairs run the two-SM MMA (tcgen05 cta_group::2), which needs at least two
+ * 128-row blocks and both operands in the current device's own memory
+ * (cudaMalloc'd on it); any other memory (pinned or managed host memory,
+ * another GPU's memory) takes one CTA per tile, *two_sm = 0. *grid = CTAs
+ * launched; *group_n = column tiles per raster group; *splits = CTAs that
+ * share each output tile's K (1: no split; more when there are too few tiles
+ * to fill the GPU and ws_bytes holds the fp32 partials). Output pointers may
+ * be NULL. Enqueues nothing; FP8_ERR_INVALID_ARG for non-positive sizes,
+ * FP8_ERR_CUDA or FP8_ERR_UNSUPPORTED_DEVICE when the device cannot be queried.
  */
 fp8_status fp8_gemm_config(const uint8_t* qa, int64_t M, int64_t ldqa, const uint8_t* qw, int64_t N,
-                           int64_t ldqw, int* two_sm, int* grid, int* group_n);
+                           int64_t ldqw, int64_t K, size_t ws_bytes, int* two_sm, int* grid, int* group_n,
+                           int* splits);
 
 /*
  * Synchronizes `stream`, then reports and clears device-side errors recorded

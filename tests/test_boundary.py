@@ -70,10 +70,18 @@ def test_workspace_and_dispatch(L):
     for M in (1, 2, 8, 15, 16):
         assert F.fp8_uses_gemv(M, 4096, 4096)
         assert F.fp8_workspace_bytes(M, 4096, 4096) == 0
-    # GEMM shapes hold the partial amax values, s_a and qA [M, min_ld(K)]
+    # GEMM shapes hold the partial amax values, s_a and qA [M, min_ld(K)]; small M adds the
+    # split-K fp32 partials [splits, M, N rounded up to 4] from the next 256-byte boundary
     for M, K in ((17, 4096), (16384, 14336), (100, 4100)):
         assert not F.fp8_uses_gemv(M, K, 4096)
-        assert F.fp8_workspace_bytes(M, K, 4096) == base + M * F.min_ld(K)
+        assert F.min_workspace_bytes(M, K, 4096) == base + M * F.min_ld(K)
+        ws = F.fp8_workspace_bytes(M, K, 4096)
+        assert ws >= base + M * F.min_ld(K)
+        if ws > base + M * F.min_ld(K):
+            split = ws - (base + M * F.min_ld(K) + 255) // 256 * 256
+            assert split > 0 and split % (M * 4096 * 4) == 0 and 2 <= split // (M * 4096 * 4) <= 16
+    assert F.fp8_workspace_bytes(16384, 14336, 4096) == base + 16384 * F.min_ld(14336)  # enough tiles: no split
+    assert F.fp8_workspace_bytes(17, 4096, 4096) > F.min_workspace_bytes(17, 4096, 4096)  # one row block: split
     assert F.fp8_workspace_bytes(0, 4096, 4096) == 0
     assert not F.fp8_uses_gemv(4, 40000, 4096)  # K beyond the GEMV's slice budget -> GEMM
 

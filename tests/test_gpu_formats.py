@@ -220,7 +220,9 @@ def test_scaled_mm_formats_equal_linear(fmt_a, fmt_w):
         qw, s_w = F.fp8_quantize_weight_ex(I.weights_normal(N, K, (189,)).to(DEV), fmt_w)
         qa, s_a = F.fp8_quantize_act_ex(a, fmt_a)
         y1 = F.fp8_scaled_mm_ex(qa, fmt_a, K, s_a, qw, fmt_w, s_w)
-        y2 = F.fp8_linear_ex(a, qw, s_w, fmt_a=fmt_a, fmt_w=fmt_w)
+        # the least workspace: no K split, the GEMM sums in fp8_scaled_mm's order
+        ws = torch.empty(max(1, F.min_workspace_bytes(M, K, N)), dtype=torch.uint8, device=DEV)
+        y2 = F.fp8_linear_ex(a, qw, s_w, fmt_a=fmt_a, fmt_w=fmt_w, ws=ws)
         torch.cuda.synchronize()
         assert torch.equal(y1, y2), (M, fmt_a, fmt_w)
 

@@ -185,7 +185,9 @@ def test_scaled_mm_equals_linear(M):
     a = I.activations_normal(M, K, (910, M)).to(DEV)
     w = I.weights_row_std(N, K, (911,)).to(DEV)
     qw, s_w = F.fp8_quantize_weight(w, per_channel=True)
-    y1 = F.fp8_linear_channelwise(a, qw, s_w)
+    # the least workspace: no K split, so the GEMM sums in the same order as fp8_scaled_mm
+    ws = torch.empty(max(1, F.min_workspace_bytes(M, K, N)), dtype=torch.uint8, device=DEV)
+    y1 = F.fp8_linear_channelwise(a, qw, s_w, ws=ws)
     qa, s_a = F.fp8_quantize_act(a)
     y2 = F.fp8_scaled_mm(qa, K, s_a, qw, s_w, per_channel=True)
     torch.cuda.synchronize()
@@ -297,3 +299,58 @@ def test_gemm_raster_keeps_smaller_operand_hot(M, K, N):
         assert cfg["group_n"] == n_tiles
     elif M * K <= 72 << 20:
         assert cfg["group_n"] == 1
+
+
+SPLIT_SHAPES = [(17, 5632, 2048), (32, 14336, 4096), (64, 4096, 4096), (100, 4096, 6144), (128, 5632, 2048),
+                (33, 4100, 1027)]
+
+
+@pytest.mark.parametrize("M,K,N", SPLIT_SHAPES)
+def test_gemm_split_k(M, K, N):
+    """Shapes with too few output tiles to fill the GPU split K across CTAs (fp32 partials in the
+    workspace, reduced in split order by the tile's last CTA): Y against the oracle, both scale
+    modes with bias, guard bands intact, and the same bits on a second call."""
+    assert not F.fp8_uses_gemv(M, K, N)
+    a = I.activations_heavy_tail(M, K, (919, M, K))
+    w = I.weights_row_std(N, K, (920, N, K))
+    b = I.bias_normal(N, (921, N))
+    qa = torch.zeros((M, F.min_ld(K)), dtype=torch.uint8, device=DEV)
+    qw = torch.zeros((N, F.min_ld(K)), dtype=torch.uint8, device=DEV)
+    cfg = F.fp8_gemm_config(qa, qw, K, F.fp8_workspace_bytes(M, K, N))
+    assert cfg["splits"] > 1, cfg
+    for pc in (False, True):
+        check(a, w, pc, b, f"split-K {M}x{K}x{N} pc={pc}", check_w=False)
+    qw, s_w = F.fp8_quantize_weight(w.to(DEV), per_channel=True)
+    ad = a.to(DEV)
+    y1 = F.fp8_linear_channelwise(ad, qw, s_w, b.to(DEV))
+    y2 = F.fp8_linear_channelwise(ad, qw, s_w, b.to(DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("M", [100, 200])
+@pytest.mark.parametrize("splits", [2, 3, 7, 16])
+def test_gemm_forced_split_counts(M, splits, monkeypatch):
+    """Split counts forced over the planner's range on a ragged K (17 blocks: a request is
+    lowered until every split owns blocks), one CTA per tile (M = 100) and pairs with a partial
+    second row block (M = 200), per-channel scales and bias."""
+    monkeypatch.setenv("FP8W8A8_GEMM_SPLITK", str(splits))
+    K, N = 2050, 777
+    kb = (K + 127) // 128
+    expect = -(-kb // -(-kb // splits))
+    a = I.activations_heavy_tail(M, K, (922, splits))
+    w = I.weights_row_std(N, K, (923,))
+    b = I.bias_normal(N, (924,))
+    qa = torch.zeros((M, F.min_ld(K)), dtype=torch.uint8, device=DEV)
+    qw = torch.zeros((N, F.min_ld(K)), dtype=torch.uint8, device=DEV)
+    cfg = F.fp8_gemm_config(qa, qw, K, F.fp8_workspace_bytes(M, K, N) + splits * M * 780 * 4)
+    assert cfg["splits"] == expect and cfg["two_sm"] == (M > 128)
+    ws = torch.empty(F.min_workspace_bytes(M, K, N) + 256 + 4096 + splits * M * 780 * 4, dtype=torch.uint8,
+                     device=DEV)
+    qw, s_w = F.fp8_quantize_weight(w.to(DEV), per_channel=True)
+    buf, y, base, row_bytes, used = guarded((M, N), torch.bfloat16, DEV)
+    F.fp8_linear_channelwise(a.to(DEV), qw, s_w, b.to(DEV), out=y, ws=ws)
+    torch.cuda.synchronize()
+    assert F.fp8_last_device_status() == F.FP8_OK
+    assert_guards_intact(buf, base, row_bytes, used, M)
+    linear_parity(y, a, w, True, b, what=f"forced split {splits}")
