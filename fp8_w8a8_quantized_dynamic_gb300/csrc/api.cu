@@ -137,11 +137,14 @@ struct BF16Mat {
   int vec() const { return aligned(p, 16) && ld % 8 == 0; }
 };
 
+// CTAs of the amax pass: at most the partial slots of a workspace, and a whole number per SM
+// (6 on a 152-SM GB300) so that no SM carries one more CTA than the others at the end.
 int amax_grid(const BF16Mat& a, int sms) {
   const int64_t units = (a.rows * a.cols + 7) / 8;
   const int64_t per_block = int64_t(kQuantThreads) * 4;
   int64_t g = (units + per_block - 1) / per_block;
-  g = std::min<int64_t>(g, std::min<int64_t>(kAmaxMaxBlocks, int64_t(sms) * 8));
+  const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>(8, kAmaxMaxBlocks / std::max(sms, 1)));
+  g = std::min<int64_t>(g, std::min<int64_t>(kAmaxMaxBlocks, int64_t(sms) * per_sm));
   return int(std::max<int64_t>(g, 1));
 }
 

@@ -709,8 +709,8 @@ int env_int(const char* name, int dflt) {
 }
 
 // Run-time switches (read once per process): FP8W8A8_GEMM_PAIR=0 selects one CTA per tile;
-// FP8W8A8_GEMM_GROUP_N fixes the raster group; FP8W8A8_GEMM_L2_MB sets the L2 bytes the
-// raster may keep hot for one operand; FP8W8A8_GEMM_L2HINT=0 drops the eviction hints.
+// FP8W8A8_GEMM_GROUP_N fixes the raster group; FP8W8A8_GEMM_L2_MB sets the largest W the
+// raster keeps hot whole; FP8W8A8_GEMM_L2HINT=0 drops the eviction hints.
 struct GemmSwitches {
   bool pair;
   int group_n;
@@ -801,21 +801,20 @@ GemmPlan plan_gemm(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_
   const int units = m_units * pl.n_tiles;
   pl.splits = 1;
   pl.grid = pl.two_sm ? 2 * std::min(units, pair_clusters_available) : std::min(units, num_sms);
-  // raster: keep the smaller operand hot in L2 when it fits the budget, stream the other once
-  const int64_t a_bytes = int64_t(M) * lda_bytes, w_bytes = int64_t(N) * ldw_bytes;
+  // raster (GB300 ncu sweeps of the group size, hints on and off): when all of W fits the
+  // budget it is kept hot (loaded evict_last, qA evict_first) while the row blocks stream past;
+  // otherwise column groups of a ~28 MB W slice with no hints. Keeping qA hot instead (one
+  // column at a time, W evict_first) re-read qA ~13 times on the 117 MB gate_up layer.
+  const int64_t w_bytes = int64_t(N) * ldw_bytes;
   const int64_t w_tile_bytes = int64_t(BN) * ldw_bytes;
+  (void)lda_bytes;
   pl.hint_a = pl.hint_b = kHintNormal;
-  if (w_bytes <= sw.l2_budget && (w_bytes <= a_bytes || a_bytes > sw.l2_budget)) {
-    pl.group_n = pl.n_tiles;  // W resident, qA streamed once
+  if (w_bytes <= sw.l2_budget) {
+    pl.group_n = pl.n_tiles;
     pl.hint_a = kHintFirst;
     pl.hint_b = kHintLast;
-  } else if (a_bytes <= sw.l2_budget) {
-    pl.group_n = 1;  // qA resident, W streamed once
-    pl.hint_a = kHintLast;
-    pl.hint_b = kHintFirst;
   } else {
-    // neither fits: a W slice of about a third of the budget stays hot per group
-    pl.group_n = int(std::max<int64_t>(1, std::min<int64_t>(pl.n_tiles, (sw.l2_budget / 3) / w_tile_bytes)));
+    pl.group_n = int(std::max<int64_t>(1, std::min<int64_t>(pl.n_tiles, (int64_t(28) << 20) / w_tile_bytes)));
   }
   if (sw.group_n > 0) pl.group_n = std::min(sw.group_n, pl.n_tiles);
   pl.hint_y = kHintFirst;  // Y is written once

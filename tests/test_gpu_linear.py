@@ -288,17 +288,17 @@ def test_pair_mode_needs_local_device_memory():
 
 
 @pytest.mark.parametrize("M,K,N", [(16384, 4096, 4096), (16384, 14336, 4096), (16384, 4096, 28672), (300, 4096, 512)])
-def test_gemm_raster_keeps_smaller_operand_hot(M, K, N):
-    """Launch plan of the prefill layers: W resident (one raster group) when it is the smaller
-    operand and fits the L2 budget, qA resident (groups of one column tile) otherwise."""
+def test_gemm_raster_groups(M, K, N):
+    """Launch plan of the prefill layers: one raster group (all of W kept hot) when W fits the
+    72 MB budget, else column groups of a ~28 MB W slice."""
     qa = torch.empty((M, K), dtype=torch.uint8, device=DEV)
     qw = torch.empty((N, K), dtype=torch.uint8, device=DEV)
     cfg = F.fp8_gemm_config(qa, qw)
     n_tiles = (N + 255) // 256
-    if N * K <= 72 << 20 and N * K <= M * K:
+    if N * K <= 72 << 20:
         assert cfg["group_n"] == n_tiles
-    elif M * K <= 72 << 20:
-        assert cfg["group_n"] == 1
+    else:
+        assert cfg["group_n"] == max(1, min(n_tiles, (28 << 20) // (256 * K)))
 
 
 SPLIT_SHAPES = [(17, 5632, 2048), (32, 14336, 4096), (64, 4096, 4096), (100, 4096, 6144), (128, 5632, 2048),
