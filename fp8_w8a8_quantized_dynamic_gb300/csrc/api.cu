@@ -2,6 +2,7 @@
 // M-based dispatch between the decode GEMV and the tcgen05 GEMM, launch configuration.
 // Every step of the layer runs in this library's kernels; nothing falls back to the CPU.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -12,6 +13,7 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <utility>
 
 #include "fp8w8a8.h"
 #include "device_common.cuh"
@@ -782,19 +784,52 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[FP8_NOALLOC_SCR
 namespace {
 
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[64] = {};
+struct NoallocAddr {
+  void* ptr = nullptr;
+  unsigned long long ctx = 0;  // id of the context the address belongs to
+};
+NoallocAddr g_noalloc_addr[64];
 
-// Device address of g_noalloc_scratch on the current device (looked up on first use).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current CUDA context (0 when it cannot be read). A device
+// reset destroys the primary context and the library's module with it; the next context gets
+// a new id, so an address cached for the old one is never reused.
+unsigned long long current_context_id() {
+  static const std::pair<CtxGetCurrentFn, CtxGetIdFn> fns = [] {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    const bool ok = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) ==
+                        cudaSuccess && qa == cudaDriverEntryPointSuccess &&
+                    cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) ==
+                        cudaSuccess && qb == cudaDriverEntryPointSuccess;
+    return ok ? std::make_pair(reinterpret_cast<CtxGetCurrentFn>(a), reinterpret_cast<CtxGetIdFn>(b))
+              : std::make_pair(static_cast<CtxGetCurrentFn>(nullptr), static_cast<CtxGetIdFn>(nullptr));
+  }();
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (fns.first && fns.second && fns.first(&c) == CUDA_SUCCESS && c != nullptr && fns.second(c, &id) == CUDA_SUCCESS)
+    return id;
+  return 0;
+}
+
+// Device address of g_noalloc_scratch on the current device, looked up on first use and again
+// whenever the current context is a different one (after a device reset).
 fp8_status noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8_ERR_CUDA;
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_addr[dev] == nullptr) {
+  NoallocAddr& e = g_noalloc_addr[dev];
+  if (e.ptr == nullptr || ctx == 0 || e.ctx != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return FP8_ERR_CUDA;
-    g_noalloc_addr[dev] = p;
+    e.ptr = p;
+    e.ctx = current_context_id();  // the lookup above creates the context if there was none
   }
-  *out = g_noalloc_addr[dev];
+  *out = e.ptr;
   return FP8_OK;
 }
 

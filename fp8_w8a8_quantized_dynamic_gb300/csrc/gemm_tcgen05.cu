@@ -805,11 +805,17 @@ GemmPlan plan_gemm(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_
   // budget it is kept hot (loaded evict_last, qA evict_first) while the row blocks stream past;
   // otherwise column groups of a ~28 MB W slice with no hints. Keeping qA hot instead (one
   // column at a time, W evict_first) re-read qA ~13 times on the 117 MB gate_up layer.
+  // With a single row block (or pair) every W tile is read once: W streams (evict_first) and
+  // the few qA rows, read by every column tile, stay (evict_last).
   const int64_t w_bytes = int64_t(N) * ldw_bytes;
   const int64_t w_tile_bytes = int64_t(BN) * ldw_bytes;
   (void)lda_bytes;
   pl.hint_a = pl.hint_b = kHintNormal;
-  if (w_bytes <= sw.l2_budget) {
+  if (m_units == 1) {
+    pl.group_n = pl.n_tiles;
+    pl.hint_a = kHintLast;
+    pl.hint_b = kHintFirst;
+  } else if (w_bytes <= sw.l2_budget) {
     pl.group_n = pl.n_tiles;
     pl.hint_a = kHintFirst;
     pl.hint_b = kHintLast;

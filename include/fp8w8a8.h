@@ -194,7 +194,9 @@ fp8_status fp8_linear_channelwise(const void* a_bf16, int64_t M, int64_t K, int6
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture. All calls share the one array and it keeps the
+ * before any stream capture. After a device reset (cudaDeviceReset) the
+ * address is looked up again on the next call, which then also belongs
+ * outside any capture. All calls share the one array and it keeps the
  * previous call's contents: nothing in it has to start at zero (each call
  * writes every scratch byte it reads before reading it), but two calls whose
  * kernels overlap on the GPU — on different streams or from different host
