@@ -596,9 +596,11 @@ def run_ours(args):
             compute.wait_stream(s_in)
             compute.wait_stream(s_out)
 
-        te = time_loop(torch, estep, max(3, args.steps // 4), 2)
-        t_chain = time_loop(torch, lambda: estep(False), max(3, args.steps // 4), 2)
-        t_link = time_loop(torch, copies_only, max(3, args.steps // 4), 2)
+        # median of three repetitions each: the host link is shared with the rest of the machine
+        reps = max(3, args.steps // 4)
+        te = statistics.median(time_loop(torch, estep, reps, 2) for _ in range(3))
+        t_chain = statistics.median(time_loop(torch, lambda: estep(False), reps, 2) for _ in range(3))
+        t_link = statistics.median(time_loop(torch, copies_only, reps, 2) for _ in range(3))
         h2d = int(sum(a.numel() * 2 for a in A_h))
         d2h = int(sum(y.numel() * 2 for y in Y_h))
         e2e = {"value": round(total_flops / (te * 1e-3) / 1e12, 2), "unit": "TFLOP/s",

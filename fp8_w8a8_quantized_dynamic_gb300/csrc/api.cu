@@ -76,7 +76,19 @@ std::atomic<int>& gemv_max_m_value() {
 
 int gemv_max_m() { return gemv_max_m_value().load(std::memory_order_relaxed); }
 
-bool use_gemv(int64_t M, int64_t K) { return M <= gemv_max_m() && K <= kGemvMaxK; }
+// Past the crossover, small layers keep the GEMV up to its largest M: measured per layer on a
+// GB300 (CUDA graph replay), the GEMV at 17..32 tokens beats the split GEMM on weights of up to
+// ~8 M elements (TinyLlama qkv and o_proj: 7.4-8.5 vs 12.3-12.7 us) and ties or loses above
+// (TinyLlama gate_up 23 M, Mistral-7B 17-117 M). Applies while the crossover is at least its
+// default (fp8_set_gemv_max_m(0) still sends everything to the GEMM).
+constexpr int64_t kSmallWeightElems = int64_t(8) << 20;
+
+bool use_gemv(int64_t M, int64_t K, int64_t N) {
+  if (K > kGemvMaxK) return false;
+  const int t = gemv_max_m();
+  if (M <= t) return true;
+  return t >= gemv::kDefaultMaxM && M <= gemv::kMaxTokens && N * K <= kSmallWeightElems;
+}
 
 // Weight tiles the GEMV issues before its activation loads have landed (FP8W8A8_GEMV_HEAD
 // overrides the default of 4; 0 holds the whole stream, gemv::kMaxStages lets it run free).
@@ -398,8 +410,8 @@ fp8_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
 
 // Decode shapes need no workspace (the GEMV quantizes A itself); the GEMM path holds the
 // partial amax values, s_a and qA [M, round_up(K, 16)]: the least a GEMM-path call accepts.
-size_t linear_ws_bytes(int64_t M, int64_t K) {
-  if (M <= 0 || K <= 0 || use_gemv(M, K)) return 0;
+size_t linear_ws_bytes(int64_t M, int64_t K, int64_t N) {
+  if (M <= 0 || K <= 0 || use_gemv(M, K, N)) return 0;
   return FP8_QUANT_WORKSPACE_BYTES + size_t(M) * size_t(round_up16(K));
 }
 
@@ -409,7 +421,7 @@ size_t round_up_256(size_t b) { return (b + 255) / 256 * 256; }
 // split-K fp32 partials of the split a 152-SM GB300 (76 CTA pairs) would use.
 // A call given less (but at least linear_ws_bytes) splits only as far as its workspace holds.
 size_t linear_ws_bytes_full(int64_t M, int64_t K, int64_t N) {
-  const size_t base = linear_ws_bytes(M, K);
+  const size_t base = linear_ws_bytes(M, K, N);
   if (base == 0 || N <= 0) return base;
   const int S = fp8k::plan_splits(M, N, K, 152, 76, SIZE_MAX);
   return S > 1 ? round_up_256(base) + fp8k::splitk_bytes(M, N, S) : base;
@@ -425,14 +437,14 @@ fp8_status linear_impl(const void* a, int64_t M, int64_t K, int64_t lda, int fmt
   if (N > 0 && s_w == nullptr) return FP8_ERR_INVALID_ARG;
   if (!aligned(bias, 2) || !aligned(s_static, 4)) return FP8_ERR_MISALIGNED;
   if (M == 0 || N == 0) return FP8_OK;
-  FP8_TRY(check_ws(ws, ws_bytes, linear_ws_bytes(M, K)));
+  FP8_TRY(check_ws(ws, ws_bytes, linear_ws_bytes(M, K, N)));
   int sms = 0;
   FP8_TRY(current_device(&sms));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (K == 0) return launch_fill_bias(bias, y, M, N, ldy, sms, st);
 
   const BF16Mat A{static_cast<const uint16_t*>(a), M, K, lda};
-  if (use_gemv(M, K)) {
+  if (use_gemv(M, K, N)) {
     // decode: one persistent GEMV kernel quantizes A (cluster-wide amax, or the static
     // scale) and streams qW
     gemv::Params p = gemv_params(nullptr, 0, nullptr, s_w, per_channel, bias, y, ldy, M, N, K);
@@ -447,7 +459,7 @@ fp8_status linear_impl(const void* a, int64_t M, int64_t K, int64_t lda, int fmt
   uint8_t* qa = wsb + kWsQaOffset;
   const int64_t ldqa = round_up16(K);
   // split-K scratch past qA, when the workspace holds it
-  const size_t split_off = round_up_256(linear_ws_bytes(M, K));
+  const size_t split_off = round_up_256(linear_ws_bytes(M, K, N));
   const fp8k::SplitK sk =
       ws_bytes > split_off
           ? fp8k::gemm_split_plan(qa, ldqa, qw, ldqw, int(M), int(N), int(K), sms, wsb + split_off, ws_bytes - split_off)
@@ -529,7 +541,7 @@ fp8_status scaled_mm_impl(const uint8_t* qa, int fmt_a, int64_t M, int64_t K, in
   FP8_TRY(current_device(&sms));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (K == 0) return launch_fill_bias(bias_bf16, y_bf16, M, N, ldy, sms, st);
-  if (use_gemv(M, K))
+  if (use_gemv(M, K, N))
     return launch_gemv(gemv_params(qa, ldqa, s_a, s_w, per_channel, bias_bf16, y_bf16, ldy, M, N, K), gemv::kModePrequant,
                        fmt_a, fmt_w, qw, ldqw, st);
   if (fp8k::gemm_launch(qa, ldqa, s_a, qw, ldqw, s_w, per_channel, static_cast<const uint16_t*>(bias_bf16),
@@ -630,8 +642,7 @@ FP8_API int fp8_set_gemv_max_m(int m) {
 }
 
 FP8_API int fp8_uses_gemv(int64_t M, int64_t K, int64_t N) {
-  (void)N;
-  return use_gemv(M, K) ? 1 : 0;
+  return use_gemv(M, K, N) ? 1 : 0;
 }
 
 FP8_API fp8_status fp8_quantize_weight(const void* w_bf16, int64_t N, int64_t K, int64_t ldw, int per_channel,
@@ -726,9 +737,9 @@ FP8_API fp8_status fp8_gemm_config(const uint8_t* qa, int64_t M, int64_t ldqa, c
   const fp8k::GemmPlan pl = fp8k::gemm_plan(qa, ldqa, qw, ldqw, int(M), int(N), sms);
   if (pl.grid <= 0) return FP8_ERR_CUDA;
   // the split fp8_linear would take with a workspace of ws_bytes (the planning needs no memory)
-  const size_t split_off = round_up_256(linear_ws_bytes(M, K));
+  const size_t split_off = round_up_256(linear_ws_bytes(M, K, N));
   int S = 1;
-  if (!use_gemv(M, K) && ws_bytes > split_off) {
+  if (!use_gemv(M, K, N) && ws_bytes > split_off) {
     alignas(256) static unsigned char probe[256];
     S = fp8k::gemm_split_plan(qa, ldqa, qw, ldqw, int(M), int(N), int(K), sms, probe, ws_bytes - split_off).splits;
   }
@@ -846,7 +857,7 @@ FP8_API fp8_status fp8_linear_noalloc(const void* a_bf16, int64_t M, int64_t K, 
     return linear_impl(a_bf16, M, K, lda, kFmtE4M3, nullptr, qw, kFmtE4M3, N, ldqw, s_w, per_channel, bias_bf16,
                        y_bf16, ldy, nullptr, 0, stream);
   // shapes whose scratch would not fit are refused before anything is enqueued
-  if (linear_ws_bytes(M, K) > size_t(FP8_NOALLOC_SCRATCH_BYTES)) return FP8_ERR_WORKSPACE;
+  if (linear_ws_bytes(M, K, N) > size_t(FP8_NOALLOC_SCRATCH_BYTES)) return FP8_ERR_WORKSPACE;
   void* scratch = nullptr;
   FP8_TRY(noalloc_scratch(&scratch));
   return linear_impl(a_bf16, M, K, lda, kFmtE4M3, nullptr, qw, kFmtE4M3, N, ldqw, s_w, per_channel, bias_bf16,

@@ -41,16 +41,11 @@ __device__ __forceinline__ float block_max_to_thread0(float v, float* red) {
   return v;
 }
 
-// Partial max |x| over a bf16 matrix [rows, cols] with row stride ld (elements).
-// contiguous != 0: ld == cols and the base is 16-byte aligned (flat 16-byte loads).
-// vec != 0: base 16-byte aligned and ld % 8 == 0 (16-byte loads per row).
-// Writes partials[blockIdx.x]. `pdl` lets the next kernel launch early (activations only).
-__global__ void __launch_bounds__(kQuantThreads)
-amax_partials_kernel(const uint16_t* __restrict__ a, int64_t rows, int64_t cols, int64_t ld,
-                     int contiguous, int vec, float* __restrict__ partials, int pdl) {
-  __shared__ float red[kQuantThreads / 32];
-  if (pdl) pdl_trigger();
-  pdl_wait();
+// Max |x| over this thread's grid-stride share of a bf16 matrix [rows, cols] with row stride
+// ld (elements), as two packed bf16 magnitudes. contiguous != 0: ld == cols and the base is
+// 16-byte aligned (flat 16-byte loads). vec != 0: base 16-byte aligned and ld % 8 == 0.
+__device__ __forceinline__ uint32_t amax_share(const uint16_t* __restrict__ a, int64_t rows, int64_t cols,
+                                               int64_t ld, int contiguous, int vec) {
   uint32_t m2 = 0;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -82,6 +77,18 @@ amax_partials_kernel(const uint16_t* __restrict__ a, int64_t rows, int64_t cols,
       }
     }
   }
+  return m2;
+}
+
+// Partial max |x| over a bf16 matrix (see amax_share); writes partials[blockIdx.x].
+// `pdl` lets the next kernel launch early (activations only).
+__global__ void __launch_bounds__(kQuantThreads)
+amax_partials_kernel(const uint16_t* __restrict__ a, int64_t rows, int64_t cols, int64_t ld,
+                     int contiguous, int vec, float* __restrict__ partials, int pdl) {
+  __shared__ float red[kQuantThreads / 32];
+  if (pdl) pdl_trigger();
+  pdl_wait();
+  const uint32_t m2 = amax_share(a, rows, cols, ld, contiguous, vec);
   const float m = block_max_to_thread0(u16x2_max_to_float(m2), red);
   if (threadIdx.x == 0) partials[blockIdx.x] = m;
 }

@@ -226,3 +226,23 @@ def test_weight_only_rejects_bad_arguments(L):
     assert F.fp8_weight_only_workspace_bytes(4, 4096, 4096) == 0
     assert wo(L, M=0, a=None, y=None) == F.FP8_OK
     assert wo(L, N=0, qw=None, s_w=None, ldy=1) == F.FP8_OK
+
+
+def test_crossover_rule(L):
+    """M <= 16 runs the GEMV; 17..32 too for layers of at most 8 Mi weight elements (measured
+    faster there), unless the crossover is lowered; fp8_set_gemv_max_m(32) sends every M <= 32
+    to the GEMV and 0 sends everything to the GEMM."""
+    prev = F.fp8_set_gemv_max_m(-1)
+    try:
+        assert F.fp8_set_gemv_max_m(16) == prev
+        assert F.fp8_uses_gemv(16, 4096, 4096) and F.fp8_uses_gemv(17, 2048, 2560) and F.fp8_uses_gemv(32, 2048, 4096)
+        assert not F.fp8_uses_gemv(17, 4096, 4096) and not F.fp8_uses_gemv(33, 2048, 2560)
+        assert F.fp8_workspace_bytes(32, 2048, 2560) == 0 and F.fp8_workspace_bytes(17, 4096, 4096) > 0
+        F.fp8_set_gemv_max_m(32)
+        assert F.fp8_uses_gemv(32, 14336, 4096)
+        F.fp8_set_gemv_max_m(8)
+        assert not F.fp8_uses_gemv(9, 2048, 2560)
+        F.fp8_set_gemv_max_m(0)
+        assert not F.fp8_uses_gemv(1, 2048, 2560)
+    finally:
+        F.fp8_set_gemv_max_m(prev)

@@ -101,7 +101,7 @@ def test_decode_config_layers(layer, M):
 
 # --------------------------------------------------------------------------- prefill GEMM
 
-@pytest.mark.parametrize("M,K,N", [(17, 256, 256), (128, 128, 256), (130, 1000, 1027), (300, 4100, 257),
+@pytest.mark.parametrize("M,K,N", [(17, 4096, 2304), (33, 256, 256), (128, 128, 256), (130, 1000, 1027), (300, 4100, 257),
                                    (257, 2050, 3001), (512, 4096, 512), (1000, 96, 520)])
 @pytest.mark.parametrize("per_channel", [False, True])
 def test_gemm_ragged(M, K, N, per_channel):

@@ -86,6 +86,15 @@ def test_prefill_sized_activations():
     check_act(a, "prefill down 2048x14336")
 
 
+@pytest.mark.parametrize("M,K,pad", [(64, 4096, 0), (65, 4096, 0), (64, 4096, 5), (1, 262144, 0), (17, 15421, 0),
+                                     (40, 1000, 3)])
+def test_activation_quantization_shapes(M, K, pad):
+    """Gap-free and strided rows, one long row, ragged K, grids from a few CTAs to hundreds:
+    bit-exact codes and scale."""
+    a = I.activations_heavy_tail(M, K, (960, M, K))
+    check_act(a, f"{M}x{K} pad={pad}", lda_pad=pad)
+
+
 def test_zero_activations():
     qa, s_a = run_act(torch.zeros((5, 33), dtype=torch.bfloat16))
     assert s_a.item() == 1.0 and not qa.any()
