@@ -354,3 +354,25 @@ def test_gemm_forced_split_counts(M, splits, monkeypatch):
     assert F.fp8_last_device_status() == F.FP8_OK
     assert_guards_intact(buf, base, row_bytes, used, M)
     linear_parity(y, a, w, True, b, what=f"forced split {splits}")
+
+
+def test_gemm_split_k_strided_activations_and_odd_ldy():
+    """K split with a strided A (TMA reads the padded rows) and an output whose row stride is
+    odd (the reduce kernel's scalar stores): guard bands and the oracle's tolerance."""
+    M, K, N = 40, 4100, 1027
+    a = I.activations_heavy_tail(M, K, (928,))
+    w = I.weights_row_std(N, K, (929,))
+    b = I.bias_normal(N, (930,))
+    qw, s_w = F.fp8_quantize_weight(w.to(DEV), per_channel=True)
+    big = torch.zeros((M, K + 24), dtype=torch.bfloat16)
+    big[:, :K] = a
+    ad = big.to(DEV)[:, :K]
+    ws = F.workspace(M, K, N, DEV)
+    qa0 = torch.zeros((M, F.min_ld(K)), dtype=torch.uint8, device=DEV)
+    assert F.fp8_gemm_config(qa0, qw, K, ws.numel())["splits"] > 1
+    ybig = torch.full((M, N + 3), 7.0, dtype=torch.bfloat16, device=DEV)
+    F.fp8_linear_channelwise(ad, qw, s_w, b.to(DEV), out=ybig[:, :N], ws=ws)
+    torch.cuda.synchronize()
+    assert F.fp8_last_device_status() == F.FP8_OK
+    assert torch.all(ybig[:, N:] == 7.0)
+    linear_parity(ybig[:, :N], a, w, True, b, what="split-K strided A, odd ldy")
