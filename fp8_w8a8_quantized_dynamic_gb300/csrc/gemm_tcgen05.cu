@@ -38,6 +38,12 @@
 //            tensor memory (the accumulator rows of its A tile). The weight tile crosses
 //            from L2 to the SMs once per pair, not once per CTA.
 //
+// Split-K (one row block, too few column tiles to fill the GPU, a workspace that holds the
+// partials): each tile's K blocks are divided among S work units; each unit writes its unscaled
+// fp32 partial to the workspace instead of Y, and splitk_reduce_kernel, launched right after
+// with programmatic dependent launch, sums the S partials in split order and applies the
+// epilogue. The split count comes from a cost model calibrated on a GB300 (plan_splits).
+//
 // Every wait is bounded (2 s); on expiry the kernel records an error for the host (with a
 // bit naming the wait), stops its peer, drains every copy either CTA issued, frees its
 // TMEM and returns.
@@ -830,8 +836,6 @@ GemmPlan plan_gemm(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_
 
 namespace {
 
-size_t round_up_256(size_t b) { return (b + 255) / 256 * 256; }
-
 // Split count for `units` work units on `slots` parallel slots with `num_kb` K blocks each.
 // Time is modelled in K blocks of one unit: ceil(units * S / slots) waves of ceil(num_kb / S)
 // blocks, plus the cost of splitting, measured on a GB300 at about 8 us per linear (the reduce
@@ -876,7 +880,7 @@ int plan_splits(int64_t M, int64_t N, int64_t K, int num_sms, int pair_slots, si
   const bool two = pair_slots > 0 && m_tiles >= 2 && 2 * pair_slots >= (3 * num_sms) / 4;
   const int units = (two ? (m_tiles + 1) / 2 : m_tiles) * n_tiles;
   const int slots = two ? pair_slots : num_sms;
-  // the partials should stay in L2 (they are written once and read once by the tile's last CTA)
+  // the partials should stay in L2 (written once by the GEMM, read once by the reduce kernel)
   const size_t cap = std::min(ws_bytes, size_t(64) << 20);
   int max_s = kMaxSplits;
   while (max_s > 1 && splitk_bytes(M, N, max_s) > cap) --max_s;
