@@ -608,6 +608,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   }
 }
 
+constexpr int kMaxSplitParts = 16;  // largest K split (the host planner's limit)
+
 // Split-K epilogue: Y[m, n] = bf16(s_a * s_w[n] * sum_j part[j][m][n] (+ bias[n])), the splits
 // summed in order 0, 1, ... (deterministic). One thread per four consecutive columns of a row;
 // the partials were written by the GEMM just before (L2-resident), read once.
@@ -625,21 +627,17 @@ splitk_reduce_kernel(const float* __restrict__ part, int64_t ldp, int splits, in
     const int m = int(i / c4);
     const int n = int(i - int64_t(m) * c4) * 4;
     const float* src = part + int64_t(m) * ldp + n;
-    float4 acc = __ldcs(reinterpret_cast<const float4*>(src));
-    int j = 1;
-    for (; j + 3 < splits; j += 4) {  // four loads in flight, summed in split order
-      const float4 v1 = __ldcs(reinterpret_cast<const float4*>(src + j * plane));
-      const float4 v2 = __ldcs(reinterpret_cast<const float4*>(src + (j + 1) * plane));
-      const float4 v3 = __ldcs(reinterpret_cast<const float4*>(src + (j + 2) * plane));
-      const float4 v4 = __ldcs(reinterpret_cast<const float4*>(src + (j + 3) * plane));
-      acc.x += v1.x; acc.y += v1.y; acc.z += v1.z; acc.w += v1.w;
-      acc.x += v2.x; acc.y += v2.y; acc.z += v2.z; acc.w += v2.w;
-      acc.x += v3.x; acc.y += v3.y; acc.z += v3.z; acc.w += v3.w;
-      acc.x += v4.x; acc.y += v4.y; acc.z += v4.z; acc.w += v4.w;
-    }
-    for (; j < splits; ++j) {
-      const float4 v = __ldcs(reinterpret_cast<const float4*>(src + j * plane));
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    // every split's load in flight at once (one memory round trip), then the sum in split order
+    float4 v[kMaxSplitParts];
+#pragma unroll
+    for (int j = 0; j < kMaxSplitParts; ++j)
+      v[j] = j < splits ? __ldcs(reinterpret_cast<const float4*>(src + j * plane)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc = v[0];
+#pragma unroll
+    for (int j = 1; j < kMaxSplitParts; ++j) {
+      if (j < splits) {
+        acc.x += v[j].x; acc.y += v[j].y; acc.z += v[j].z; acc.w += v[j].w;
+      }
     }
     const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
     float o[4];
@@ -836,16 +834,20 @@ GemmPlan plan_gemm(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_
 
 namespace {
 
-// Split count for `units` work units on `slots` parallel slots with `num_kb` K blocks each.
-// Time is modelled in K blocks of one unit: ceil(units * S / slots) waves of ceil(num_kb / S)
-// blocks, plus the cost of splitting, measured on a GB300 at about 8 us per linear (the reduce
-// kernel's launch and dependency wait, the partial stores and loads): about 18 K blocks of one
-// unit (~0.45 us each while the weight streams through few SMs). A split must save 15 %.
-int choose_splits(int units, int slots, int num_kb, int max_splits) {
-  constexpr double kSplitCost = 18.0;
+// Split count for `units` work units on `slots` parallel slots with `num_kb` K blocks each, for
+// M x N outputs. Time model in us, fitted to GB300 measurements of the Mistral-7B and TinyLlama
+// linears at M = 32, 64 and 128 with every split count forced: each of ceil(units * S / slots)
+// waves streams ceil(num_kb / S) K blocks at ~0.38 us a block, the first ~4 of them hidden behind
+// the pipeline fill; a split adds ~2 us (the reduce kernel) and ~0.5 us per MB of fp32 partials
+// (written by the GEMM, read back by the reduce kernel). A split is taken only if it saves 1.5 us.
+int choose_splits(int units, int slots, int num_kb, int64_t M, int64_t N, int max_splits) {
+  constexpr double kBlockUs = 0.38, kSplitUs = 2.0, kPartialUsPerMB = 0.5, kMinGainUs = 1.5;
+  constexpr int kHiddenBlocks = 4;
   auto cost = [&](int S, int kbs) {
     const double waves = double((int64_t(units) * S + slots - 1) / slots);
-    return waves * kbs + (S > 1 ? kSplitCost : 0.0);
+    double t = waves * std::max(kbs - kHiddenBlocks, 0) * kBlockUs;
+    if (S > 1) t += kSplitUs + kPartialUsPerMB * double(splitk_bytes(M, N, S)) / 1e6;
+    return t;
   };
   const double base = cost(1, num_kb);
   int best = 1;
@@ -859,10 +861,10 @@ int choose_splits(int units, int slots, int num_kb, int max_splits) {
       best_cost = c;
     }
   }
-  return best_cost < 0.85 * base ? best : 1;
+  return best_cost < base - kMinGainUs ? best : 1;
 }
 
-constexpr int kMaxSplits = 16;
+constexpr int kMaxSplits = gemm::kMaxSplitParts;
 
 }  // namespace
 
@@ -893,7 +895,7 @@ int plan_splits(int64_t M, int64_t N, int64_t K, int num_sms, int pair_slots, si
   }
   // measured: with CTA pairs (two or more row blocks) a split never paid for itself
   if (two) return 1;
-  return choose_splits(units, slots, num_kb, max_s);
+  return choose_splits(units, slots, num_kb, M, N, max_s);
 }
 
 namespace {

@@ -308,7 +308,7 @@ SPLIT_SHAPES = [(17, 5632, 2048), (32, 14336, 4096), (64, 4096, 4096), (100, 409
 @pytest.mark.parametrize("M,K,N", SPLIT_SHAPES)
 def test_gemm_split_k(M, K, N):
     """Shapes with too few output tiles to fill the GPU split K across CTAs (fp32 partials in the
-    workspace, reduced in split order by the tile's last CTA): Y against the oracle, both scale
+    workspace, reduced in split order by a second kernel): Y against the oracle, both scale
     modes with bias, guard bands intact, and the same bits on a second call."""
     assert not F.fp8_uses_gemv(M, K, N)
     a = I.activations_heavy_tail(M, K, (919, M, K))
