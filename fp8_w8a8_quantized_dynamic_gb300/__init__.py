@@ -65,7 +65,7 @@ _SIGNATURES = {
     "fp8_weight_only_workspace_bytes": (_sz, [_i64, _i64, _i64]),
     "fp8_linear_weight_only": (_int, [_vp, _i64, _i64, _i64, _vp, _int, _i64, _i64, _vp, _int, _vp, _vp, _i64,
                                       _vp, _sz, _vp]),
-    "fp8_gemm_config": (_int, [_vp, _i64, _i64, _vp, _i64, _i64, _i64, _sz, _vp, _vp, _vp, _vp]),
+    "fp8_gemm_config": (_int, [_vp, _i64, _i64, _vp, _i64, _i64, _i64, _sz, _vp, _vp, _vp, _vp, _vp]),
     "fp8_last_device_status": (_int, [_vp]),
     "fp8_selftest_timeout": (_int, [_i64, _vp]),
     "fp8_status_string": (ctypes.c_char_p, [_int]),
@@ -368,15 +368,16 @@ def fp8_last_device_status(stream=None) -> int:
 def fp8_gemm_config(qa, qw, K: Optional[int] = None, ws_bytes: int = 0) -> dict:
     """The GEMM launch the library would use for FP8 operands qa [M, ld] and qw [N, ld] (K columns;
     default: the row length) with a linear workspace of ws_bytes, on the current device:
-    {"two_sm": bool, "grid": int, "group_n": int, "splits": int}. Enqueues nothing."""
-    two, grid, gn, sp = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    {"two_sm": bool, "grid": int, "group_n": int, "splits": int, "tail_split": int}. Enqueues nothing."""
+    two, grid, gn, sp, ts = (ctypes.c_int(0) for _ in range(5))
     K = qa.shape[1] if K is None else int(K)
     st = lib().fp8_gemm_config(qa.data_ptr(), qa.shape[0], qa.stride(0), qw.data_ptr(), qw.shape[0], qw.stride(0),
                                K, int(ws_bytes), ctypes.byref(two), ctypes.byref(grid), ctypes.byref(gn),
-                               ctypes.byref(sp))
+                               ctypes.byref(sp), ctypes.byref(ts))
     if st != FP8_OK:
         raise FP8Error(st, "fp8_gemm_config")
-    return {"two_sm": bool(two.value), "grid": grid.value, "group_n": gn.value, "splits": sp.value}
+    return {"two_sm": bool(two.value), "grid": grid.value, "group_n": gn.value, "splits": sp.value,
+            "tail_split": ts.value}
 
 
 def min_workspace_bytes(M: int, K: int, N: int) -> int:

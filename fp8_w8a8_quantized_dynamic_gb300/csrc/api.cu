@@ -729,7 +729,7 @@ FP8_API fp8_status fp8_linear_weight_only(const void* a_bf16, int64_t M, int64_t
 
 FP8_API fp8_status fp8_gemm_config(const uint8_t* qa, int64_t M, int64_t ldqa, const uint8_t* qw, int64_t N,
                                    int64_t ldqw, int64_t K, size_t ws_bytes, int* two_sm, int* grid, int* group_n,
-                                   int* splits) {
+                                   int* splits, int* tail_split) {
   if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim || ldqa <= 0 || ldqw <= 0)
     return FP8_ERR_INVALID_ARG;
   int sms = 0;
@@ -750,6 +750,7 @@ FP8_API fp8_status fp8_gemm_config(const uint8_t* qa, int64_t M, int64_t ldqa, c
                           : pl.grid;
   if (group_n) *group_n = pl.group_n;
   if (splits) *splits = S;
+  if (tail_split) *tail_split = S > 1 ? 1 : pl.tail_split;
   return FP8_OK;
 }
 

@@ -44,6 +44,11 @@
 // with programmatic dependent launch, sums the S partials in split order and applies the
 // epilogue. The split count comes from a cost model calibrated on a GB300 (plan_splits).
 //
+// Last wave: when the tiles left after the full waves number at most half of the slots (CTA
+// pairs, or CTAs), each of them is computed as 2 units of 128 columns over all of K (4 units of
+// 64 on request), so the partial last wave ends sooner. Those units load their weight rows
+// through a second tensor map with the narrower box and issue MMAs with the smaller N.
+//
 // Every wait is bounded (2 s); on expiry the kernel records an error for the host (with a
 // bit naming the wait), stops its peer, drains every copy either CTA issued, frees its
 // TMEM and returns.
@@ -121,6 +126,11 @@ constexpr uint32_t make_idesc(int fmt_a, int fmt_w) {
 
 // kind::f16 with bf16 A and B: the format fields hold BF16 = 1.
 constexpr uint32_t kIdescBf16 = kIdescBase | (1u << 7) | (1u << 10);
+
+// The same descriptor for an MMA of n columns (a multiple of 16, at most BN).
+__host__ __device__ constexpr uint32_t idesc_with_n(uint32_t idesc, int n) {
+  return (idesc & ~(0x3Fu << 17)) | (uint32_t(n >> 3) << 17);
+}
 
 // The two-SM MMA covers both CTAs' rows: M = 256 in the descriptor.
 __host__ __device__ constexpr uint32_t idesc_two_sm(uint32_t idesc) {
@@ -300,7 +310,7 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int m
 template <bool kBf16, bool kTwo>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-            const __grid_constant__ GemmParams p) {
+            const __grid_constant__ CUtensorMap tmap_bt, const __grid_constant__ GemmParams p) {
   constexpr int kElemsPerStage = kBf16 ? BK / 2 : BK;  // K elements per stage
   constexpr int kStages = Ring<kTwo>::stages;
   constexpr uint32_t kStageBytes = Ring<kTwo>::stage_bytes;
@@ -318,15 +328,33 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   const bool leader = rank == 0;
   const int m_units = kTwo ? (p.m_tiles + 1) / 2 : p.m_tiles;
   const int S = p.k_splits;  // split-K: work unit = (tile, split); the splits of a tile are adjacent
-  const int num_tiles = m_units * p.n_tiles * S;
+  // tail: the tiles from p.tail_start on (the last, partial wave) are split by columns into
+  // p.tail_split units of BN / tail_split columns each, all of K (tail_split == 1: none)
+  const int TS = p.tail_split;
+  const int num_tiles = TS > 1 ? p.tail_start + (m_units * p.n_tiles - p.tail_start) * TS : m_units * p.n_tiles * S;
   const int first_unit = kTwo ? int(blockIdx.x >> 1) : int(blockIdx.x);
   const int unit_stride = kTwo ? int(gridDim.x >> 1) : int(gridDim.x);
-  auto coords = [&](int unit, int& m_idx, int& n_idx, int& ks) {
-    const int tu = unit / S;
-    ks = unit - tu * S;
+  // unit -> tile coordinates, K split, first column and column count (BN, or BN / TS in the tail)
+  auto coords = [&](int unit, int& m_idx, int& n0, int& ks, int& width) {
+    int tu, sub = 0;
+    width = BN;
+    if (TS > 1 && unit >= p.tail_start) {
+      const int v = unit - p.tail_start;
+      tu = p.tail_start + v / TS;
+      sub = v - (v / TS) * TS;
+      width = BN / TS;
+      ks = 0;
+    } else {
+      tu = unit / S;
+      ks = unit - tu * S;
+    }
+    int n_idx;
     tile_coords(tu, p, m_units, m_idx, n_idx);
     if (kTwo) m_idx = 2 * m_idx + int(rank);
+    n0 = n_idx * BN + sub * width;
   };
+  // bytes one CTA's copies bring into a stage for a unit of `width` columns
+  auto stage_bytes_for = [&](int width) { return kABytes + uint32_t(kTwo ? width / 2 : width) * BK; };
   const int num_kb = (p.K + kElemsPerStage - 1) / kElemsPerStage;
   volatile int* abort_flag = &ctl->abort_flag;
   // after a wait gives up: stop the peer CTA as well, so the pair leaves together
@@ -338,6 +366,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   if (threadIdx.x == 0) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
+    if (TS > 1) asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap_bt)) : "memory");
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
       mbar_init(smem_u32(&ctl->empty[s]), 1);  // one commit per stage (two-SM: the leader's, in both CTAs)
@@ -380,8 +409,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       uint32_t it = 0;
       bool ok = true;
       for (int tile = first_unit; tile < num_tiles && ok; tile += unit_stride) {
-        int m_idx, n_idx, ks;
-        coords(tile, m_idx, n_idx, ks);
+        int m_idx, n0, ks, width;
+        coords(tile, m_idx, n0, ks, width);
+        const CUtensorMap* mapb = width == BN ? &tmap_b : &tmap_bt;
+        const uint32_t bytes = stage_bytes_for(width);
         const int kb_end = min(num_kb, (ks + 1) * p.kb_per_split);
         for (int kb = ks * p.kb_per_split; kb < kb_end; ++kb, ++it) {
           const int s = it % kStages;
@@ -395,14 +426,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
           if (kTwo) {
             // both CTAs' copies complete on the leader's barrier, which expects all of them
             const uint32_t lb = map_to_rank(fb, 0);
-            if (leader) mbar_arrive_expect_tx(fb, 2 * kStageBytes);
+            if (leader) mbar_arrive_expect_tx(fb, 2 * bytes);
             tma_load_2d_pair(a_stage(s), &tmap_a, lb, kb * kElemsPerStage, m_idx * BM, pol_a);
-            tma_load_2d_pair(b_stage(s), &tmap_b, lb, kb * kElemsPerStage, n_idx * BN + int(rank) * (BN / 2),
-                             pol_b);
+            tma_load_2d_pair(b_stage(s), mapb, lb, kb * kElemsPerStage, n0 + int(rank) * (width / 2), pol_b);
           } else {
-            mbar_arrive_expect_tx(fb, kStageBytes);
+            mbar_arrive_expect_tx(fb, bytes);
             tma_load_2d(a_stage(s), &tmap_a, fb, kb * kElemsPerStage, m_idx * BM, pol_a);
-            tma_load_2d(b_stage(s), &tmap_b, fb, kb * kElemsPerStage, n_idx * BN, pol_b);
+            tma_load_2d(b_stage(s), mapb, fb, kb * kElemsPerStage, n0, pol_b);
           }
         }
       }
@@ -432,7 +462,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         }
         tmem_fence_after();
         const uint32_t d_tmem = tmem_base + ab * BN;
-        const int ks = tile % S;
+        int m_idx, n0, ks, width;
+        coords(tile, m_idx, n0, ks, width);
+        const uint32_t idesc_u = width == BN ? idesc : idesc_with_n(idesc, width);
         const int kb_begin = ks * p.kb_per_split, kb_end = min(num_kb, kb_begin + p.kb_per_split);
         for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
           const int s = it % kStages;
@@ -449,7 +481,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
           for (int kk = 0; kk < BK / kMmaK; ++kk) {
             // advance the start address by 32 bytes of K inside the swizzled 128-byte row
             mma_issue<kBf16, kTwo>(d_tmem, adesc + uint64_t(kk * kMmaK >> 4), bdesc + uint64_t(kk * kMmaK >> 4),
-                                   idesc, (kb != kb_begin || kk != 0) ? 1u : 0u);
+                                   idesc_u, (kb != kb_begin || kk != 0) ? 1u : 0u);
           }
           mma_commit<kTwo>(smem_u32(&ctl->empty[s]));  // frees the stage once these MMAs have read it
         }
@@ -473,14 +505,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     const uint32_t tempty_bar = kTwo ? map_to_rank(smem_u32(&ctl->tempty[0]), 0) : smem_u32(&ctl->tempty[0]);
     uint32_t acc_it = 0;
     for (int tile = first_unit; tile < num_tiles; tile += unit_stride, ++acc_it) {
-      int m_idx, n_idx, ks;
-      coords(tile, m_idx, n_idx, ks);
+      int m_idx, col0, ks, width;
+      coords(tile, m_idx, col0, ks, width);
       const int ab = acc_it % kAccBufs;
       const uint32_t aph = (acc_it / kAccBufs) & 1u;
       // column scales/bias of this tile, double-buffered by accumulator: a warp can only
       // rewrite buffer ab after every epilogue warp passed the barrier of the tile between.
-      for (int j = et; j < BN; j += kEpiThreads) {
-        const int n = n_idx * BN + j;
+      for (int j = et; j < width; j += kEpiThreads) {
+        const int n = col0 + j;
         float sc = 0.0f, bb = 0.0f;
         if (n < p.N) {
           sc = s_a * p.s_w[p.per_channel ? n : 0];
@@ -508,8 +540,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         // split-K: this unit's fp32 partial rows go to the workspace (unscaled)
         float* prow = p.part + ((int64_t)ks * p.M + m) * p.ldp;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          const int n0 = n_idx * BN + c * 32;
+        for (int c = 0; c < width / 32; ++c) {
+          const int n0 = col0 + c * 32;
           if (n0 >= p.N) break;  // warp-uniform
           uint32_t r[32];
           tmem_ld32(tbase + c * 32, r);
@@ -535,8 +567,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         continue;
       }
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int n0 = n_idx * BN + c * 32;
+      for (int c = 0; c < width / 32; ++c) {
+        const int n0 = col0 + c * 32;
         if (n0 >= p.N) break;  // warp-uniform
         uint32_t r[32];
         tmem_ld32(tbase + c * 32, r);
@@ -589,8 +621,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       // everything below hi - kStages is complete; each j above it is its stage's open phase
       for (uint32_t j = hi > uint32_t(kStages) ? hi - kStages : 0u; j < hi; ++j) {
         const uint32_t fb = smem_u32(&ctl->full[j % kStages]);
-        if (j >= n0) mbar_arrive_expect_tx(fb, kStageBytes);  // only the follower filled it
-        else if (j >= n1) mbar_complete_tx(fb, kStageBytes);  // the follower's half never came
+        // both CTAs walk the same units, each unit with the same number of K blocks when
+        // units have fewer columns (the tail is never split along K)
+        int jm, jn, jks, jw = BN;
+        if (TS > 1) coords(first_unit + int(j / uint32_t(num_kb)) * unit_stride, jm, jn, jks, jw);
+        const uint32_t jb = stage_bytes_for(jw);
+        if (j >= n0) mbar_arrive_expect_tx(fb, jb);  // only the follower filled it
+        else if (j >= n1) mbar_complete_tx(fb, jb);  // the follower's half never came
         if (!mbar_wait_bounded(fb, (j / kStages) & 1u, nullptr, &g_gemm_error)) atomicOr(&g_gemm_error, kSiteDrain);
       }
     }
@@ -720,6 +757,7 @@ struct GemmSwitches {
   int group_n;
   int64_t l2_budget;
   bool hints;
+  int tail;  // largest column split of the last wave's tiles (1: none)
 };
 
 const GemmSwitches& switches() {
@@ -729,6 +767,8 @@ const GemmSwitches& switches() {
     v.group_n = env_int("FP8W8A8_GEMM_GROUP_N", 0);
     v.l2_budget = int64_t(std::max(1, env_int("FP8W8A8_GEMM_L2_MB", 72))) << 20;
     v.hints = env_int("FP8W8A8_GEMM_L2HINT", 1) != 0;
+    const int t = env_int("FP8W8A8_GEMM_TAIL", 2);
+    v.tail = t >= 4 ? 4 : t >= 2 ? 2 : 1;
     return v;
   }();
   return s;
@@ -829,6 +869,20 @@ GemmPlan plan_gemm(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_
   if (sw.group_n > 0) pl.group_n = std::min(sw.group_n, pl.n_tiles);
   pl.hint_y = kHintFirst;  // Y is written once
   if (!sw.hints) pl.hint_a = pl.hint_b = pl.hint_y = kHintNormal;
+  // the last wave: when fewer tiles than slots are left after the full waves, split each of
+  // them by columns into 2 or 4 units (all of K each) so that the wave ends sooner
+  const int slots = pl.two_sm ? std::min(units, pair_clusters_available) : std::min(units, num_sms);
+  pl.tail_split = 1;
+  pl.tail_start = units;
+  const int rem = slots > 0 ? units % slots : 0;
+  if (units > slots && rem > 0) {
+    for (int f = sw.tail; f >= 2; f /= 2)
+      if (f * rem <= slots) {
+        pl.tail_split = f;
+        pl.tail_start = units - rem;
+        break;
+      }
+  }
   return pl;
 }
 
@@ -942,11 +996,16 @@ int launch_kind(const void* a, int64_t lda_bytes, const float* s_a, const void* 
   p.part = split.part;
   p.ldp = split.ldp;
   if (S > 1 && (split.part == nullptr || (num_kb + p.kb_per_split - 1) / p.kb_per_split != S)) return 4;
+  p.tail_split = S > 1 ? 1 : pl.tail_split;  // a K split already fills the GPU
+  p.tail_start = p.tail_split > 1 ? pl.tail_start : units;
 
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mbt;
+  const uint32_t b_rows = pl.two_sm ? BN / 2 : BN;
   if (!make_tensor_map(&ma, a, kBf16, M, K, lda_bytes, BM) ||
-      !make_tensor_map(&mb, w, kBf16, N, K, ldw_bytes, pl.two_sm ? BN / 2 : BN))
+      !make_tensor_map(&mb, w, kBf16, N, K, ldw_bytes, b_rows))
     return 2;
+  mbt = mb;
+  if (p.tail_split > 1 && !make_tensor_map(&mbt, w, kBf16, N, K, ldw_bytes, b_rows / p.tail_split)) return 2;
 
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
@@ -964,12 +1023,12 @@ int launch_kind(const void* a, int64_t lda_bytes, const float* s_a, const void* 
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, two_sm, ma, mb, p) != cudaSuccess) return 3;
+    if (cudaLaunchKernelEx(&cfg, two_sm, ma, mb, mbt, p) != cudaSuccess) return 3;
   } else {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, single, ma, mb, p) != cudaSuccess) return 3;
+    if (cudaLaunchKernelEx(&cfg, single, ma, mb, mbt, p) != cudaSuccess) return 3;
   }
   if (S == 1) return 0;
   // the split-K epilogue, launched early (programmatic) so it is resident when the GEMM ends

@@ -26,6 +26,9 @@ struct GemmParams {
   int k_splits, kb_per_split;
   float* part;
   int64_t ldp;
+  // last wave: work units from tail_start on are tiles split by columns into tail_split units
+  // of BN / tail_split columns (all of K); tail_split == 1: no such units
+  int tail_start, tail_split;
 };
 
 // Workspace of a split-K GEMM: the fp32 partials [splits][M][ldp].
@@ -50,6 +53,8 @@ struct GemmPlan {
   int group_n;   // raster group (column tiles per group)
   int hint_a, hint_b, hint_y;
   int splits;    // K split count (1: none)
+  int tail_split;  // column split of the last wave's tiles (1: none; never with a K split)
+  int tail_start;  // first work unit of the split tail
 };
 
 // The plan for operands a [M, lda_bytes] and w [N, ldw_bytes] on device `dev` with

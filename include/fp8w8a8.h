@@ -311,13 +311,16 @@ fp8_status fp8_linear_weight_only(const void* a_bf16, int64_t M, int64_t K, int6
  * another GPU's memory) takes one CTA per tile, *two_sm = 0. *grid = CTAs
  * launched; *group_n = column tiles per raster group; *splits = CTAs that
  * share each output tile's K (1: no split; more when there are too few tiles
- * to fill the GPU and ws_bytes holds the fp32 partials). Output pointers may
- * be NULL. Enqueues nothing; FP8_ERR_INVALID_ARG for non-positive sizes,
+ * to fill the GPU and ws_bytes holds the fp32 partials); *tail_split = column
+ * units each tile of the last, partial wave is divided into (1: none; 2 or 4
+ * when that many units per left-over tile still fit one wave, each computing
+ * 256 / tail_split columns over all of K). Output pointers may be NULL.
+ * Enqueues nothing; FP8_ERR_INVALID_ARG for non-positive sizes,
  * FP8_ERR_CUDA or FP8_ERR_UNSUPPORTED_DEVICE when the device cannot be queried.
  */
 fp8_status fp8_gemm_config(const uint8_t* qa, int64_t M, int64_t ldqa, const uint8_t* qw, int64_t N,
                            int64_t ldqw, int64_t K, size_t ws_bytes, int* two_sm, int* grid, int* group_n,
-                           int* splits);
+                           int* splits, int* tail_split);
 
 /*
  * Synchronizes `stream`, then reports and clears device-side errors recorded
