@@ -29,6 +29,7 @@ struct GemmParams {
   // last wave: work units from tail_start on are tiles split by columns into tail_split units
   // of BN / tail_split columns (all of K); tail_split == 1: no such units
   int tail_start, tail_split;
+  int serpentine;  // 1: every other work unit of a CTA walks its K blocks backwards
 };
 
 // Workspace of a split-K GEMM: the fp32 partials [splits][M][ldp].
@@ -55,6 +56,7 @@ struct GemmPlan {
   int splits;    // K split count (1: none)
   int tail_split;  // column split of the last wave's tiles (1: none; never with a K split)
   int tail_start;  // first work unit of the split tail
+  int serpentine;  // 1: every other work unit of a CTA walks K backwards
 };
 
 // The plan for operands a [M, lda_bytes] and w [N, ldw_bytes] on device `dev` with

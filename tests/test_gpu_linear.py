@@ -112,34 +112,35 @@ def test_gemm_ragged(M, K, N, per_channel):
     check(a, w, per_channel, b, f"gemm {M}x{K}x{N} pc={per_channel}")
 
 
-def _tail_split_expected(tiles, slots):
-    """Column split of the last wave's tiles: the largest of 4, 2 whose units still fit one wave."""
+def _tail_split_expected(tiles, slots, largest):
+    """Column split of the last wave's tiles: the largest factor (4, 2, at most `largest`) whose
+    units still fit one wave."""
     rem = tiles % slots
     if tiles <= slots or rem == 0:
         return 1
-    return next((f for f in (4, 2) if f * rem <= slots), 1)
+    return next((f for f in (4, 2) if f <= largest and f * rem <= slots), 1)
 
 
 def _tail_rows(n_tiles, slots, split, rows_per_unit):
     """Smallest M (ragged: short of a whole last unit) whose tile count leaves a tail that splits
     into `split` units per tile on `slots` slots."""
     for units in range(2, 512):
-        if _tail_split_expected(units * n_tiles, slots) == split:
+        if _tail_split_expected(units * n_tiles, slots, split) == split:
             return units * rows_per_unit - rows_per_unit // 3
     raise AssertionError("no such M")
 
 
 def _tail_case(split, K=520, N=2500):
-    """One GEMM whose last wave is split by columns, parity-checked against the oracle; the
-    mode (pairs or one CTA per tile) is whatever the process's switches give."""
+    """One GEMM whose last wave is split by columns into `split` units per tile (the process's
+    FP8W8A8_GEMM_TAIL allows it), parity-checked against the oracle; the mode (pairs or one CTA
+    per tile) is whatever the process's switches give."""
     qa0 = torch.zeros((4096, F.min_ld(K)), dtype=torch.uint8, device=DEV)
     qw0 = torch.zeros((N, F.min_ld(K)), dtype=torch.uint8, device=DEV)
-    two = F.fp8_gemm_config(qa0, qw0, K)["two_sm"]
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    slots = F.fp8_gemm_config(qa0, qw0, K)["grid"] // (2 if two else 1)
-    assert slots <= sms
-    n_tiles = (N + 255) // 256
-    M = _tail_rows(n_tiles, slots, split, 256 if two else 128)
+    cfg0 = F.fp8_gemm_config(qa0, qw0, K)
+    two = cfg0["two_sm"]
+    slots = cfg0["grid"] // (2 if two else 1)
+    assert slots <= torch.cuda.get_device_properties(0).multi_processor_count
+    M = _tail_rows((N + 255) // 256, slots, split, 256 if two else 128)
     cfg = F.fp8_gemm_config(qa0[:M], qw0, K, F.fp8_workspace_bytes(M, K, N))  # the workspace fp8_linear takes
     assert cfg["tail_split"] == split and cfg["splits"] == 1, cfg
     a = I.activations_heavy_tail(M, K, (931, M, split))
@@ -148,25 +149,30 @@ def _tail_case(split, K=520, N=2500):
     check(a, w, True, b, f"tail split {split} {M}x{K}x{N} two_sm={two}", check_w=False)
 
 
-@pytest.mark.parametrize("split", [2, 4])
-def test_gemm_tail_split_pairs(split):
-    """CTA pairs: the last, partial wave's tiles divided by columns into 2 or 4 units over all of
-    K (ragged M, N and K, per-channel scales, bias), against the oracle with guard bands."""
-    _tail_case(split)
-
-
-@pytest.mark.parametrize("split", [2, 4])
-def test_gemm_tail_split_single_cta(split):
-    """The same with one CTA per tile (pairs switched off for a child process)."""
+def _in_child(call, **env):
+    """Runs `call` (an expression over this module, as t) in a fresh process with extra
+    environment switches (read once per process by the library)."""
     import os
     import subprocess
     import sys
     here = os.path.dirname(os.path.abspath(__file__))
-    code = (f"import sys; sys.path[:0] = [{here!r}, {os.path.dirname(here)!r}]\n"
-            f"import test_gpu_linear as t; t._tail_case({split})\n")
-    env = dict(os.environ, FP8W8A8_GEMM_PAIR="0")
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    code = f"import sys; sys.path[:0] = [{here!r}, {os.path.dirname(here)!r}]\nimport test_gpu_linear as t\n{call}\n"
+    r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, **env), capture_output=True, text=True,
+                       timeout=600)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+
+
+def test_gemm_tail_split_pairs():
+    """CTA pairs: the last, partial wave's tiles divided by columns into 2 units over all of K
+    (ragged M, N and K, per-channel scales, bias), against the oracle with guard bands."""
+    _tail_case(2)
+
+
+@pytest.mark.parametrize("pair,split", [("1", 4), ("0", 2), ("0", 4)])
+def test_gemm_tail_split_other_modes(pair, split):
+    """The same with quarters (FP8W8A8_GEMM_TAIL=4) and with one CTA per tile
+    (FP8W8A8_GEMM_PAIR=0), each in a child process."""
+    _in_child(f"t._tail_case({split})", FP8W8A8_GEMM_PAIR=pair, FP8W8A8_GEMM_TAIL=str(split))
 
 
 def test_gemm_strided_activations_and_output():
