@@ -76,12 +76,14 @@ std::atomic<int>& gemv_max_m_value() {
 
 int gemv_max_m() { return gemv_max_m_value().load(std::memory_order_relaxed); }
 
-// Past the crossover, small layers keep the GEMV up to its largest M: measured per layer on a
-// GB300 (CUDA graph replay), the GEMV at 17..32 tokens beats the split GEMM on weights of up to
-// ~8 M elements (TinyLlama qkv and o_proj: 7.4-8.5 vs 12.3-12.7 us) and ties or loses above
-// (TinyLlama gate_up 23 M, Mistral-7B 17-117 M). Applies while the crossover is at least its
-// default (fp8_set_gemv_max_m(0) still sends everything to the GEMM).
-constexpr int64_t kSmallWeightElems = int64_t(8) << 20;
+// Past the crossover, layers of up to 24 Mi weight elements keep the GEMV up to its largest M:
+// measured per layer on a GB300 (CUDA graph replay, the GEMV's tcgen05 main loop at 17..32
+// tokens against the split GEMM), the GEMV wins on TinyLlama's four linears (4-23 M: 7.4-14.5
+// vs 11.3-15.0 us) and Mistral-7B o_proj (16 M: 11.7-13.1 vs 14.0-14.4 us), ties on qkv (24 M:
+// 14.4-16.5 vs 15.7-16.5 us), and loses on gate_up and down (117 and 59 M) from 24 or 17
+// tokens on. Applies while the crossover is at least its default (fp8_set_gemv_max_m(0) still
+// sends everything to the GEMM).
+constexpr int64_t kSmallWeightElems = int64_t(24) << 20;
 
 bool use_gemv(int64_t M, int64_t K, int64_t N) {
   if (K > kGemvMaxK) return false;
@@ -98,6 +100,13 @@ int gemv_head_tiles() {
     const int x = e ? std::atoi(e) : 4;
     return std::max(0, std::min(x, 1 << 20));
   }();
+  return v;
+}
+
+// FP8W8A8_GEMV_SLICE=1: the dynamic-scale GEMV always copies only each rank's slice of A and
+// exchanges slice maxima over the cluster (measurement switch).
+bool gemv_slice_only() {
+  static const bool v = std::getenv("FP8W8A8_GEMV_SLICE") != nullptr && std::atoi(std::getenv("FP8W8A8_GEMV_SLICE")) != 0;
   return v;
 }
 
@@ -269,9 +278,26 @@ int gemv_max_clusters(gemv::KernelFn kfn, int S, size_t smem) {
 // Shared-memory row stride (bytes) of a K-slice of activations: FP8 rows are padded to 64 mod
 // 128, bf16 rows (two bytes an element) to 16 mod 128, so the fragment loads of a warp spread
 // over all banks.
-int gemv_act_stride(int mode, int kslice) {
+// The tcgen05 main loop (tc) keeps the FP8 activations as 128-byte swizzled K blocks of
+// [tokens][128 B], kslice bytes a token in all.
+int gemv_act_stride(int mode, int kslice, bool tc) {
   if (mode == gemv::kModeBf16) return 2 * kslice + 16;
+  if (tc) return kslice;
   return kslice % 128 == 0 ? kslice + 64 : kslice;
+}
+
+// 17 to 32 tokens with FP8 activations run the GEMV's main loop on tcgen05: four n8 token tiles
+// on mma.sync take about twice the weight stream's time per tile, while at two tiles mma.sync
+// keeps up and the tensor-memory round trip only adds latency (measured per layer on a GB300:
+// Mistral-7B gate_up at M = 32, 49.6 -> 40.5 us; qkv at M = 12, 12.3 -> 12.9 us).
+// FP8W8A8_GEMV_TC: 0 never, 2 from two token tiles on (measurement switches).
+bool gemv_tc(int NT, int mode) {
+  static const int from = [] {
+    const char* e = std::getenv("FP8W8A8_GEMV_TC");
+    const int v = e ? std::atoi(e) : 4;
+    return v <= 0 ? 1 << 20 : v <= 2 ? 2 : 4;
+  }();
+  return NT >= from && mode != gemv::kModeBf16;
 }
 
 fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uint8_t* qw, int64_t ldqw,
@@ -283,7 +309,8 @@ fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uin
   const int max_slice = mode == kModeBf16 ? kMaxSliceBf16 : kMaxSlice;
   const int NT = p.M <= 8 ? 1 : p.M <= 16 ? 2 : 4;
   const int act_rows = 8 * NT;
-  const KernelFn kfn = kernel_for(NT, mode, fmt_a, fmt_w);
+  const bool tc = gemv_tc(NT, mode);
+  const KernelFn kfn = kernel_for(NT, mode, fmt_a, fmt_w, tc);
   const int smem_limit = gemv_smem_limit(kfn);
   auto smem_for = [&](int stg, int act_stride, int nrb) {
     return size_t(layout(stg, act_stride, act_rows, nrb).total) + 1024;
@@ -296,7 +323,7 @@ fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uin
     if ((KT + slice_tiles - 1) / slice_tiles != S) continue;  // every rank must own tiles
     const int kslice = slice_tiles * kTileK;
     if (kslice > max_slice) continue;
-    const int act_stride = gemv_act_stride(mode, kslice);
+    const int act_stride = gemv_act_stride(mode, kslice, tc);
     if (smem_for(kMinStages, act_stride, 1) > size_t(smem_limit)) continue;
     // co-resident clusters at the largest shared memory any configuration may take (a lower
     // bound for every configuration, so the grid never runs in waves)
@@ -329,7 +356,7 @@ fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uin
     return FP8_ERR_CUDA;
   }
   p.kslice = bslice;
-  p.act_stride = gemv_act_stride(mode, bslice);
+  p.act_stride = gemv_act_stride(mode, bslice, tc);
   p.act_rows = act_rows;
   p.head_tiles = gemv_head_tiles();
   // dynamic scale: every CTA reads all of A when that is at most two load batches per thread
@@ -351,7 +378,7 @@ fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uin
     const int64_t slice_bytes = int64_t(p.M) * bslice * 2;
     if (p.s_static != nullptr) {
       if (head_for(slice_bytes) >= 1) { p.scratch_a = 2; p.head_tiles = head_for(slice_bytes); }
-    } else if (head_for(full_bytes) >= 1) {
+    } else if (!gemv_slice_only() && head_for(full_bytes) >= 1) {
       p.scratch_a = 1;
       p.head_tiles = head_for(full_bytes);
       p.cluster_amax = 0;

@@ -9,28 +9,31 @@ namespace gemv {
 
 namespace {
 
-template <int NT, int Mode>
+template <int NT, int Mode, bool Tc>
 KernelFn pick(int fa, int fw) {
   if constexpr (Mode == kModeBf16) {
-    return fw == kFmtE4M3 ? gemv_kernel<NT, Mode, kFmtE4M3, kFmtE4M3> : gemv_kernel<NT, Mode, kFmtE4M3, kFmtE5M2>;
+    return fw == kFmtE4M3 ? gemv_kernel<NT, Mode, kFmtE4M3, kFmtE4M3, false>
+                          : gemv_kernel<NT, Mode, kFmtE4M3, kFmtE5M2, false>;
   } else {
     if (fa == kFmtE4M3)
-      return fw == kFmtE4M3 ? gemv_kernel<NT, Mode, kFmtE4M3, kFmtE4M3> : gemv_kernel<NT, Mode, kFmtE4M3, kFmtE5M2>;
-    return fw == kFmtE4M3 ? gemv_kernel<NT, Mode, kFmtE5M2, kFmtE4M3> : gemv_kernel<NT, Mode, kFmtE5M2, kFmtE5M2>;
+      return fw == kFmtE4M3 ? gemv_kernel<NT, Mode, kFmtE4M3, kFmtE4M3, Tc> : gemv_kernel<NT, Mode, kFmtE4M3, kFmtE5M2, Tc>;
+    return fw == kFmtE4M3 ? gemv_kernel<NT, Mode, kFmtE5M2, kFmtE4M3, Tc> : gemv_kernel<NT, Mode, kFmtE5M2, kFmtE5M2, Tc>;
   }
 }
 
-template <int NT>
+template <int NT, bool Tc>
 KernelFn pick_mode(int mode, int fa, int fw) {
-  if (mode == kModeQuantize) return pick<NT, kModeQuantize>(fa, fw);
-  if (mode == kModeBf16) return pick<NT, kModeBf16>(fa, fw);
-  return pick<NT, kModePrequant>(fa, fw);
+  if (mode == kModeQuantize) return pick<NT, kModeQuantize, Tc>(fa, fw);
+  if (mode == kModeBf16) return pick<NT, kModeBf16, false>(fa, fw);
+  return pick<NT, kModePrequant, Tc>(fa, fw);
 }
 
 }  // namespace
 
-KernelFn kernel_for(int NT, int mode, int fa, int fw) {
-  return NT == 1 ? pick_mode<1>(mode, fa, fw) : NT == 2 ? pick_mode<2>(mode, fa, fw) : pick_mode<4>(mode, fa, fw);
+KernelFn kernel_for(int NT, int mode, int fa, int fw, bool tc) {
+  if (NT == 1) return pick_mode<1, false>(mode, fa, fw);
+  if (NT == 2) return tc ? pick_mode<2, true>(mode, fa, fw) : pick_mode<2, false>(mode, fa, fw);
+  return tc ? pick_mode<4, true>(mode, fa, fw) : pick_mode<4, false>(mode, fa, fw);
 }
 
 // Failure-path self-test. A two-warp pipeline on a two-stage mbarrier ring, shaped like the

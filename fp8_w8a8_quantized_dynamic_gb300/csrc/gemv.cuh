@@ -135,6 +135,69 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y) : "memory");
 }
 
+// ---- tcgen05 consumer (several token tiles) ----
+
+__device__ __forceinline__ void st_dsmem_v4(uint32_t local_addr, uint32_t rank, float a, float b, float c, float d) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" :: "r"(remote), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// Shared-memory descriptor of a K-major operand in the 128-byte swizzle layout: rows of 128
+// bytes, 8-row atoms of 1024 bytes (stride byte offset), start address >> 4 in bits 0-13,
+// descriptor version 1 at bit 46, swizzle mode 2 (128B) at bits 61-63; the leading byte
+// offset is unused for this layout (1).
+__device__ __forceinline__ uint64_t tc_sdesc(uint32_t saddr) {
+  return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
+         (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// D[128 rows x N tokens] (+)= W tile (128 x 32 bytes of K) * A block^T, FP8 operands, fp32 in
+// tensor memory; issued by one thread.
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+// Arrives once on `bar` when every MMA this thread issued before has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// N fp32 columns of this thread's tensor-memory lane (warp-collective).
+template <int N>
+__device__ __forceinline__ void tc_ld(uint32_t taddr, uint32_t (&r)[N]) {
+  static_assert(N == 16 || N == 32, "16 or 32 token columns");
+  if constexpr (N == 16)
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+  else
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+constexpr int kTcCols = 64;  // tensor memory columns of a tcgen05 GEMV CTA: two accumulators of <= 32
+
 // Loads the 8-element units [i0 + b * kConsumerThreads, b < kRegUnits) of a [rows][upt units]
 // bf16 slice starting at column k0 (zero past `units`, past row M and past K) into v.
 __device__ __forceinline__ void load_units(uint4 (&v)[kRegUnits], const Params& p, int i0, int units, int upt,
@@ -167,9 +230,19 @@ __device__ __forceinline__ uint32_t abs_max_units(uint32_t m2, const uint4 (&v)[
 // dependent activation round trip takes several times longer. The dynamic amax is the maximum
 // over all of A computed by every CTA (p.cluster_amax == 0, small M*K), or each rank's slice
 // maximum exchanged over the cluster through distributed shared memory.
-template <int NT, int kMode, int FA, int FW>
+//
+// kTc (FP8 activations, two or four token tiles; the host takes it for four): the tensor
+// cores' tcgen05 path runs the main loop instead of mma.sync, whose FP8 rate (about 38 cycles
+// per m16n8k32 per SM sub-partition, measured on the GB300 through the per-token-tile cost)
+// makes four token tiles about twice as slow as the weight stream. Each weight tile is the M = 128 operand as TMA left it; the quantized
+// activations are stored per 128-byte K block as [tokens][128 B] in the same 128-byte swizzle
+// and are the N = 8 * NT operand; accumulators (two, alternating by row block) live in tensor
+// memory. Warp 0's first lane issues the MMAs and commits each stage back to the producer;
+// warps 4..7 read finished accumulators and push the partials to their owners.
+template <int NT, int kMode, int FA, int FW, bool kTc>
 __global__ void __launch_bounds__(kThreads, 1)
 gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ Params p) {
+  static_assert(!kTc || (NT >= 2 && kMode != kModeBf16), "tcgen05 path: FP8 activations, 9 to 32 tokens");
   unsigned int* err = &g_gemv_error;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -192,8 +265,18 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
   const int ntiles = (kspan + kTileK - 1) / kTileK;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool cluster_amax = kMode == kModeQuantize && p.s_static == nullptr && p.cluster_amax;
+  // FP8 activation byte (token m, slice column kk; kk % 8 == 0 for the stores below)
+  auto act_at = [&](int m, int kk) -> uint32_t {
+    if constexpr (kTc)
+      return act + uint32_t((kk >> 7) * (p.act_rows * 128) + m * 128 + ((((kk >> 4) & 7) ^ (m & 7)) << 4) + (kk & 15));
+    else
+      return act + uint32_t(m * p.act_stride + kk);
+  };
 
   __shared__ int abort_flag;
+  __shared__ uint32_t tmem_sh;
+  __shared__ __align__(8) uint64_t tc_bars[5];  // kTc: accumulator full[2], empty[2], drain
+  const uint32_t accfull0 = smem_u32(&tc_bars[0]), accempty0 = smem_u32(&tc_bars[2]), drain = smem_u32(&tc_bars[4]);
   __shared__ float s_a_out;
   __shared__ float slice_amax;
   __shared__ float red[kConsumerWarps];
@@ -203,13 +286,29 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     abort_flag = 0;
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, kConsumerWarps);
+      mbar_init(empty0 + 8 * s, kTc ? 1 : kConsumerWarps);  // kTc: one MMA commit frees a stage
     }
     mbar_init(aready, kConsumerWarps);
     mbar_init(abar, 1);
+    if constexpr (kTc) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(accfull0 + 8 * b, 1);
+        mbar_init(accempty0 + 8 * b, 4);  // the four reading warps
+      }
+      mbar_init(drain, 1);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if constexpr (kTc) {
+    if (warp == 1) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                   :: "r"(smem_u32(&tmem_sh)), "n"(kTcCols) : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+  }
   __syncthreads();
+  if constexpr (kTc) tc_fence_after();
   pdl_trigger();
   volatile int* ab = &abort_flag;
 
@@ -311,7 +410,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
             const int i = i0 + j * kConsumerThreads;
             const int m = int((float(i) + 0.5f) * inv_upt), kk = (i - m * upt) << 3;
             inside[j] = i < total && k0 + kk < p.K;
-            dst[j] = i < total ? act + m * p.act_stride + kk : 0u;
+            dst[j] = i < total ? act_at(m, kk) : 0u;
             x[j] = inside[j] ? lds_v4(scratch + uint32_t(m * rowlen + (full ? k0 : 0) + kk) * 2u)
                              : make_uint4(0, 0, 0, 0);
           }
@@ -375,8 +474,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
           const int m = i / upt, kk = (i - (i / upt) * upt) << 3;
           uint2 q = make_uint2(0, 0);
           if (k0 + kk < p.K) q = quant8_exact<FA>(x, kq, s_a, check);
-          asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(act + m * p.act_stride + kk), "r"(q.x), "r"(q.y)
-                       : "memory");
+          asm volatile("st.shared.v2.u32 [%0], {%1,%2};" :: "r"(act_at(m, kk)), "r"(q.x), "r"(q.y) : "memory");
         };
 #pragma unroll
         for (int b = 0; b < kRegUnits; ++b) {
@@ -397,7 +495,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
       for (int i = threadIdx.x; i < (p.act_rows - p.M) * zu; i += kConsumerThreads) {
         const int m = p.M + i / zu;
         const int kk = (i - (i / zu) * zu) << 4;
-        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" :: "r"(act + m * p.act_stride + kk), "r"(0u) : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" :: "r"(act_at(m, kk)), "r"(0u) : "memory");
       }
     } else if constexpr (kMode == kModeBf16) {
       s_a = 1.0f;
@@ -442,87 +540,150 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
           if (i < units) {
             const int m = i / upt, kk = (i - (i / upt) * upt) * 16;
             asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};"
-                         :: "r"(act + m * p.act_stride + kk), "r"(v[b].x), "r"(v[b].y), "r"(v[b].z), "r"(v[b].w)
-                         : "memory");
+                         :: "r"(act_at(m, kk)), "r"(v[b].x), "r"(v[b].y), "r"(v[b].z), "r"(v[b].w) : "memory");
           }
         }
       }
       loads_back();
     }
     if (threadIdx.x == 0) s_a_out = s_a;
+    if constexpr (kTc) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // activations -> tensor cores
     consumer_bar_sync();
-    const int g = lane >> 2, t = lane & 3;
-    const uint32_t row_lo = (warp * 16 + g) * kTileK, row_hi = row_lo + 8 * kTileK;
-    // this lane's activation fragment: token g, the 16 K of unit (4j + t) of each half-row j
-    const uint32_t act_lane = act + g * p.act_stride + (kMode == kModeBf16 ? 32 : 16) * t;
-    uint32_t it = 0;
-    for (int r = 0; r < rb_count; ++r) {
-      float acc[NT][4];
+    if constexpr (kTc) {
+      if (!cluster_amax) cluster_wait();  // every CTA of the cluster runs before partials are pushed to it
+      const uint32_t tmem = tmem_sh;
+      constexpr int N = 8 * NT;
+      if (warp == 0) {
+        if (lane == 0) {
+          // ---------------- MMA issuer ----------------
+          // D f32 (bit 4), A = weights (format at bits 7-9), B = activations (10-12), both K-major,
+          // N >> 3 at bits 17-22, M >> 4 at bits 24-28
+          const uint32_t idesc = (1u << 4) | (uint32_t(FW) << 7) | (uint32_t(FA) << 10) | (uint32_t(N >> 3) << 17) |
+                                 (uint32_t(kRows >> 4) << 24);
+          uint32_t it = 0;
+          bool ok = true;
+          for (int r = 0; r < rb_count && ok; ++r) {
+            const int b = r & 1;
+            if (!mbar_wait_bounded(accempty0 + 8 * b, ((r >> 1) & 1) ^ 1u, ab, err)) break;
+            tc_fence_after();
+            const uint32_t d = tmem + uint32_t(b * 32);
+            for (int kt = 0; kt < ntiles; ++kt, ++it) {
+              const int s = it % p.stages;
+              const uint32_t ph = (it / p.stages) & 1u;
+              if (!mbar_wait_bounded(full0 + 8 * s, ph, ab, err)) { ok = false; break; }
+              tc_fence_after();
+              const uint64_t adesc = tc_sdesc(ring + s * kTileBytes);
+              const uint64_t bdesc = tc_sdesc(act + uint32_t(kt * p.act_rows * 128));
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
-      for (int kt = 0; kt < ntiles; ++kt, ++it) {
-        const int s = it % p.stages;
-        const uint32_t ph = (it / p.stages) & 1u;
-        const bool ok = mbar_wait_bounded(full0 + 8 * s, ph, ab, err);
-        if (ok) {
-          const uint32_t tile = ring + s * kTileBytes;
+              for (int kk = 0; kk < kTileK / 32; ++kk)  // 32 bytes of K per MMA: +2 in the address field
+                tc_mma(d, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc, (kt | kk) != 0 ? 1u : 0u);
+              tc_commit(empty0 + 8 * s);  // the stage is free once these MMAs have read it
+            }
+            if (!ok) break;
+            tc_commit(accfull0 + 8 * b);
+          }
+          // every MMA issued must finish before tensor and shared memory are released
+          tc_commit(drain);
+          mbar_wait_bounded(drain, 0, nullptr, err);
+        }
+        __syncwarp();
+      } else if (warp >= 4) {
+        // ---------------- accumulators -> partials of the owning ranks ----------------
+        const int row = (warp & 3) * 32 + lane;  // tensor-memory lane quarter of this warp
+        const int owner = row / rows_per;
+        for (int r = 0; r < rb_count; ++r) {
+          const int b = r & 1;
+          bool ok = true;
+          if (lane == 0) ok = mbar_wait_bounded(accfull0 + 8 * b, (r >> 1) & 1u, ab, err);
+          if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
+          tc_fence_after();
+          uint32_t v[N];
+          tc_ld<N>(tmem + (uint32_t((warp & 3) * 32) << 16) + uint32_t(b * 32), v);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(accempty0 + 8 * b);
+          const uint32_t dst = part + r * part_bytes(p.act_rows) +
+                               uint32_t((rank * rows_per + (row - owner * rows_per)) * p.act_rows) * 4u;
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            // 16-byte unit (4j + t) of rows g / g+8, at its 128B-swizzled position (row % 8 == g)
-            const uint32_t unit = uint32_t(((4 * j + t) ^ g) * 16);
-            const uint4 wlo = lds_v4(tile + row_lo + unit);
-            const uint4 whi = lds_v4(tile + row_hi + unit);
-            if constexpr (kMode == kModeBf16) {
-              // 4-byte group i of the unit feeds one k16 MMA: bytes (4i, 4i+1) are its K pair
-              // (2t, 2t+1) and bytes (4i+2, 4i+3) its pair (2t+8, 2t+9); the activations use the
-              // same order, 8 consecutive bytes of bf16 per MMA
-              const uint32_t wl[4] = {wlo.x, wlo.y, wlo.z, wlo.w}, wh[4] = {whi.x, whi.y, whi.z, whi.w};
-              uint32_t fa[4][4];
+          for (int c = 0; c < N / 4; ++c)
+            st_dsmem_v4(dst + 16 * c, owner, __uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                        __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+        }
+      }
+    } else {
+      const int g = lane >> 2, t = lane & 3;
+      const uint32_t row_lo = (warp * 16 + g) * kTileK, row_hi = row_lo + 8 * kTileK;
+      // this lane's activation fragment: token g, the 16 K of unit (4j + t) of each half-row j
+      const uint32_t act_lane = act + g * p.act_stride + (kMode == kModeBf16 ? 32 : 16) * t;
+      uint32_t it = 0;
+      for (int r = 0; r < rb_count; ++r) {
+        float acc[NT][4];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                fa[i][0] = fp8x2_to_bf16x2<FW>(wl[i]);
-                fa[i][1] = fp8x2_to_bf16x2<FW>(wh[i]);
-                fa[i][2] = fp8x2_to_bf16x2<FW>(wl[i] >> 16);
-                fa[i][3] = fp8x2_to_bf16x2<FW>(wh[i] >> 16);
-              }
+        for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+        for (int kt = 0; kt < ntiles; ++kt, ++it) {
+          const int s = it % p.stages;
+          const uint32_t ph = (it / p.stages) & 1u;
+          const bool ok = mbar_wait_bounded(full0 + 8 * s, ph, ab, err);
+          if (ok) {
+            const uint32_t tile = ring + s * kTileBytes;
 #pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                const uint32_t boff = act_lane + nt * 8 * p.act_stride + 2 * (kt * kTileK + 64 * j);
-                const uint4 b0 = lds_v4(boff), b1 = lds_v4(boff + 16);
-                mma_bf16(acc[nt], fa[0][0], fa[0][1], fa[0][2], fa[0][3], b0.x, b0.y);
-                mma_bf16(acc[nt], fa[1][0], fa[1][1], fa[1][2], fa[1][3], b0.z, b0.w);
-                mma_bf16(acc[nt], fa[2][0], fa[2][1], fa[2][2], fa[2][3], b1.x, b1.y);
-                mma_bf16(acc[nt], fa[3][0], fa[3][1], fa[3][2], fa[3][3], b1.z, b1.w);
-              }
-            } else {
+            for (int j = 0; j < 2; ++j) {
+              // 16-byte unit (4j + t) of rows g / g+8, at its 128B-swizzled position (row % 8 == g)
+              const uint32_t unit = uint32_t(((4 * j + t) ^ g) * 16);
+              const uint4 wlo = lds_v4(tile + row_lo + unit);
+              const uint4 whi = lds_v4(tile + row_hi + unit);
+              if constexpr (kMode == kModeBf16) {
+                // 4-byte group i of the unit feeds one k16 MMA: bytes (4i, 4i+1) are its K pair
+                // (2t, 2t+1) and bytes (4i+2, 4i+3) its pair (2t+8, 2t+9); the activations use the
+                // same order, 8 consecutive bytes of bf16 per MMA
+                const uint32_t wl[4] = {wlo.x, wlo.y, wlo.z, wlo.w}, wh[4] = {whi.x, whi.y, whi.z, whi.w};
+                uint32_t fa[4][4];
 #pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                const uint4 b = lds_v4(act_lane + nt * 8 * p.act_stride + kt * kTileK + 64 * j);
-                mma_fp8<FW, FA>(acc[nt], wlo.x, whi.x, wlo.y, whi.y, b.x, b.y);
-                mma_fp8<FW, FA>(acc[nt], wlo.z, whi.z, wlo.w, whi.w, b.z, b.w);
+                for (int i = 0; i < 4; ++i) {
+                  fa[i][0] = fp8x2_to_bf16x2<FW>(wl[i]);
+                  fa[i][1] = fp8x2_to_bf16x2<FW>(wh[i]);
+                  fa[i][2] = fp8x2_to_bf16x2<FW>(wl[i] >> 16);
+                  fa[i][3] = fp8x2_to_bf16x2<FW>(wh[i] >> 16);
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                  const uint32_t boff = act_lane + nt * 8 * p.act_stride + 2 * (kt * kTileK + 64 * j);
+                  const uint4 b0 = lds_v4(boff), b1 = lds_v4(boff + 16);
+                  mma_bf16(acc[nt], fa[0][0], fa[0][1], fa[0][2], fa[0][3], b0.x, b0.y);
+                  mma_bf16(acc[nt], fa[1][0], fa[1][1], fa[1][2], fa[1][3], b0.z, b0.w);
+                  mma_bf16(acc[nt], fa[2][0], fa[2][1], fa[2][2], fa[2][3], b1.x, b1.y);
+                  mma_bf16(acc[nt], fa[3][0], fa[3][1], fa[3][2], fa[3][3], b1.z, b1.w);
+                }
+              } else {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                  const uint4 b = lds_v4(act_lane + nt * 8 * p.act_stride + kt * kTileK + 64 * j);
+                  mma_fp8<FW, FA>(acc[nt], wlo.x, whi.x, wlo.y, whi.y, b.x, b.y);
+                  mma_fp8<FW, FA>(acc[nt], wlo.z, whi.z, wlo.w, whi.w, b.z, b.w);
+                }
               }
             }
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty0 + 8 * s);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * s);
-      }
-      // push the partials of this row block to the ranks that own their rows:
-      // part[r][source rank][row - owner's first row][token] in the owner's shared memory
-      if (r == 0 && !cluster_amax) cluster_wait();  // every CTA of the cluster is running
+        // push the partials of this row block to the ranks that own their rows:
+        // part[r][source rank][row - owner's first row][token] in the owner's shared memory
+        if (r == 0 && !cluster_amax) cluster_wait();  // every CTA of the cluster is running
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
+        for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int row = warp * 16 + g + 8 * h, col = nt * 8 + 2 * t;
-          const int owner = row / rows_per;
-          const uint32_t dst = part + r * part_bytes(p.act_rows) +
-                               ((rank * rows_per + (row - owner * rows_per)) * p.act_rows + col) * 4;
-          st_dsmem_v2(dst, owner, acc[nt][2 * h], acc[nt][2 * h + 1]);
+          for (int h = 0; h < 2; ++h) {
+            const int row = warp * 16 + g + 8 * h, col = nt * 8 + 2 * t;
+            const int owner = row / rows_per;
+            const uint32_t dst = part + r * part_bytes(p.act_rows) +
+                                 ((rank * rows_per + (row - owner * rows_per)) * p.act_rows + col) * 4;
+            st_dsmem_v2(dst, owner, acc[nt][2 * h], acc[nt][2 * h + 1]);
+          }
         }
       }
+      if (rb_count == 0 && !cluster_amax) cluster_wait();
     }
-    if (rb_count == 0 && !cluster_amax) cluster_wait();
   }
 
   // split-K reduction work of this rank: its share of the rows of every row block
@@ -576,6 +737,13 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     }
   }
   // no rank reads another's shared memory after the barrier above, so no second barrier
+  if constexpr (kTc) {
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem_sh), "n"(kTcCols) : "memory");
+  }
 }
 
 }  // namespace gemv

@@ -52,7 +52,8 @@ struct Params {
   int M, N, K;
   int kslice;          // bytes of K per rank, multiple of kTileK
   int act_stride;      // smem row stride (bytes) of the activation slice: == 64 mod 128 for FP8
-                       // activations, == 16 mod 128 for bf16 (conflict-free fragment loads)
+                       // activations, == 16 mod 128 for bf16 (conflict-free fragment loads);
+                       // the tcgen05 path stores [K block][token][128 B] instead (stride = kslice)
   int stages;          // ring depth
   int row_blocks;      // ceil(N / kRows)
   int num_clusters;    // C
@@ -80,9 +81,10 @@ __host__ __device__ inline Layout layout(int stages, int act_stride, int act_row
 }
 
 // One instantiation of the kernel: NT n8 token tiles (1: M <= 8, 2: M <= 16, 4: M <= 32), activation
-// mode (kMode*), FP8 formats of the activations (fa, unused for kModeBf16) and weights (fw).
+// mode (kMode*), FP8 formats of the activations (fa, unused for kModeBf16) and weights (fw), and
+// the main loop on tcgen05 (tc; NT >= 2 with FP8 activations) or on mma.sync.
 using KernelFn = void (*)(CUtensorMap, Params);
-KernelFn kernel_for(int NT, int mode, int fa, int fw);
+KernelFn kernel_for(int NT, int mode, int fa, int fw, bool tc);
 
 // Enqueues the failure-path self-test kernel (a bounded wait made to run out after limit_ns).
 void selftest_timeout(unsigned long long limit_ns, cudaStream_t st);

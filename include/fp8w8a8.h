@@ -98,7 +98,7 @@ size_t fp8_workspace_bytes(int64_t M, int64_t K, int64_t N);
 
 /* 1 when fp8_linear takes the decode GEMV path for this shape, 0 for the GEMM path:
  * M <= the crossover (16 by default, see fp8_set_gemv_max_m), and, while the crossover is at
- * least 16, also M <= 32 for small layers (N * K <= 8 Mi elements), where the GEMV was
+ * least 16, also M <= 32 for layers of N * K <= 24 Mi elements, where the GEMV was
  * measured faster; K <= 32768 in both cases. Host-only. */
 int fp8_uses_gemv(int64_t M, int64_t K, int64_t N);
 

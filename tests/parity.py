@@ -110,3 +110,21 @@ def weight_only_parity(y: torch.Tensor, a: torch.Tensor, w: torch.Tensor, per_ch
                            f"{bad[:3].tolist()} got {y_gpu[tuple(bad[:3].T)]} want {y_ref[tuple(bad[:3].T)]} "
                            f"tol {tol[tuple(bad[:3].T)]}")
     return float(np.max(err / tol)) if err.size else 0.0
+
+
+def tail_split_expected(tiles: int, slots: int, largest: int) -> int:
+    """Column split of a GEMM's last wave: the largest factor (4, 2, at most `largest`) whose
+    units still fit one wave of `slots`; 1 when the tiles fill whole waves or fit one."""
+    rem = tiles % slots
+    if tiles <= slots or rem == 0:
+        return 1
+    return next((f for f in (4, 2) if f <= largest and f * rem <= slots), 1)
+
+
+def tail_rows(n_tiles: int, slots: int, split: int, rows_per_unit: int) -> int:
+    """Smallest M (ragged: short of a whole last unit) whose tile count leaves a last wave that
+    splits into `split` units per tile on `slots` slots."""
+    for units in range(2, 512):
+        if tail_split_expected(units * n_tiles, slots, split) == split:
+            return units * rows_per_unit - rows_per_unit // 3
+    raise AssertionError("no such M")

@@ -15,7 +15,7 @@ import fp8_w8a8_quantized_dynamic_gb300 as F
 from fp8_w8a8_quantized_dynamic_gb300 import _build
 from fp8_w8a8_quantized_dynamic_gb300 import inputs as I
 from parity import (assert_codes_equal, assert_guards_intact, assert_scale_equal, guarded, linear_parity,
-                    oracle_weight)
+                    oracle_weight, tail_rows)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -101,7 +101,7 @@ def test_decode_config_layers(layer, M):
 
 # --------------------------------------------------------------------------- prefill GEMM
 
-@pytest.mark.parametrize("M,K,N", [(17, 4096, 2304), (33, 256, 256), (128, 128, 256), (130, 1000, 1027), (300, 4100, 257),
+@pytest.mark.parametrize("M,K,N", [(17, 4096, 6401), (33, 256, 256), (128, 128, 256), (130, 1000, 1027), (300, 4100, 257),
                                    (257, 2050, 3001), (512, 4096, 512), (1000, 96, 520)])
 @pytest.mark.parametrize("per_channel", [False, True])
 def test_gemm_ragged(M, K, N, per_channel):
@@ -110,24 +110,6 @@ def test_gemm_ragged(M, K, N, per_channel):
     w = I.weights_row_std(N, K, (906, N, K))
     b = I.bias_normal(N, (907, N))
     check(a, w, per_channel, b, f"gemm {M}x{K}x{N} pc={per_channel}")
-
-
-def _tail_split_expected(tiles, slots, largest):
-    """Column split of the last wave's tiles: the largest factor (4, 2, at most `largest`) whose
-    units still fit one wave."""
-    rem = tiles % slots
-    if tiles <= slots or rem == 0:
-        return 1
-    return next((f for f in (4, 2) if f <= largest and f * rem <= slots), 1)
-
-
-def _tail_rows(n_tiles, slots, split, rows_per_unit):
-    """Smallest M (ragged: short of a whole last unit) whose tile count leaves a tail that splits
-    into `split` units per tile on `slots` slots."""
-    for units in range(2, 512):
-        if _tail_split_expected(units * n_tiles, slots, split) == split:
-            return units * rows_per_unit - rows_per_unit // 3
-    raise AssertionError("no such M")
 
 
 def _tail_case(split, K=520, N=2500):
@@ -140,7 +122,7 @@ def _tail_case(split, K=520, N=2500):
     two = cfg0["two_sm"]
     slots = cfg0["grid"] // (2 if two else 1)
     assert slots <= torch.cuda.get_device_properties(0).multi_processor_count
-    M = _tail_rows((N + 255) // 256, slots, split, 256 if two else 128)
+    M = tail_rows((N + 255) // 256, slots, split, 256 if two else 128)
     cfg = F.fp8_gemm_config(qa0[:M], qw0, K, F.fp8_workspace_bytes(M, K, N))  # the workspace fp8_linear takes
     assert cfg["tail_split"] == split and cfg["splits"] == 1, cfg
     a = I.activations_heavy_tail(M, K, (931, M, split))
@@ -364,7 +346,7 @@ def test_gemm_raster_groups(M, K, N):
         assert cfg["group_n"] == max(1, min(n_tiles, (28 << 20) // (256 * K)))
 
 
-SPLIT_SHAPES = [(17, 5632, 2048), (32, 14336, 4096), (64, 4096, 4096), (100, 4096, 6144), (128, 5632, 2048),
+SPLIT_SHAPES = [(17, 5632, 5120), (32, 14336, 4096), (64, 4096, 4096), (100, 4096, 6144), (128, 5632, 2048),
                 (33, 4100, 1027)]
 
 

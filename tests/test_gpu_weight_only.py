@@ -11,7 +11,7 @@ from fp8_w8a8_quantized_dynamic_gb300 import _build
 from fp8_w8a8_quantized_dynamic_gb300 import inputs as I
 from oracle import fp8_oracle as O
 from parity import (assert_codes_equal, assert_guards_intact, assert_scale_equal, f32, guarded, oracle_weight,
-                    weight_only_parity)
+                    tail_rows, weight_only_parity)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -113,6 +113,24 @@ def test_weight_only_prefill_sampled():
     y = run_wo(a, w, "e4m3", True, check_w=False)
     rows = np.sort(np.random.default_rng(310).choice(M, 24, replace=False))
     weight_only_parity(y, a, w, True, rows=rows, what=f"wo prefill {L.name}")
+
+
+def test_weight_only_tail_split():
+    """bf16 kernel (kind::f16) with the last, partial wave split by columns into 128-column units
+    over all of K: ragged M, N and K against the oracle, both scale modes."""
+    K, N = 520, 2500
+    qa0 = torch.zeros((4096, F.min_ld(K)), dtype=torch.uint8, device=DEV)
+    qw0 = torch.zeros((N, F.min_ld(K)), dtype=torch.uint8, device=DEV)
+    cfg0 = F.fp8_gemm_config(qa0, qw0, K)  # the same tile grid and slots as the bf16 kernel
+    assert cfg0["two_sm"]
+    M = tail_rows((N + 255) // 256, cfg0["grid"] // 2, 2, 256)
+    assert F.fp8_gemm_config(qa0[:M], qw0, K)["tail_split"] == 2
+    a = I.activations_heavy_tail(M, K, (311, M))
+    w = I.weights_row_std(N, K, (312, N))
+    b = I.bias_normal(N, (313, N))
+    for per_channel in (False, True):
+        y = run_wo(a, w, "e4m3", per_channel, b, check_w=False)
+        weight_only_parity(y, a, w, per_channel, b, what=f"wo tail {M}x{K}x{N} pc={per_channel}")
 
 
 def test_weight_only_matches_scaled_bf16_product_of_upconverted_weights():
