@@ -381,7 +381,8 @@ def fp8_gemm_config(qa, qw, K: Optional[int] = None, ws_bytes: int = 0) -> dict:
 
 
 def min_workspace_bytes(M: int, K: int, N: int) -> int:
-    """The least workspace fp8_linear accepts for this shape (no K split): 0 for decode shapes."""
-    if M <= 0 or K <= 0 or fp8_uses_gemv(M, K, N):
+    """The least workspace fp8_linear accepts for this shape (no K split): 0 for decode shapes of
+    up to 16 tokens, which the GEMV quantizes itself."""
+    if M <= 0 or K <= 0 or (M <= 16 and fp8_uses_gemv(M, K, N)):
         return 0
     return FP8_QUANT_WORKSPACE_BYTES + M * min_ld(K)

@@ -29,6 +29,19 @@ using namespace fp8k;
 
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 constexpr int kGemvMaxK = gemv::kMaxCluster * gemv::kMaxSlice;  // 32768
+// Tokens up to which the GEMV quantizes A itself (two n8 token tiles). With four, the 32-token
+// activation area leaves the ring too shallow to hold A, which every cluster would fetch twice
+// (for the amax, then for the cast) by per-thread round trips while the weight stream waits
+// (measured: 15-25 us on the Mistral-7B gate_up and down layers at 32 tokens); there A is
+// quantized once beforehand and the GEMV loads the FP8 slice by TMA.
+// FP8W8A8_GEMV_SELFQUANT overrides it (measurement switch; at most 32).
+int64_t gemv_self_quant_max_m() {
+  static const int64_t v = [] {
+    const char* e = std::getenv("FP8W8A8_GEMV_SELFQUANT");
+    return e ? std::max<int64_t>(0, std::min<int64_t>(std::atoi(e), gemv::kMaxTokens)) : int64_t(2 * 8);
+  }();
+  return v;
+}
 
 // ---------------------------------------------------------------------------
 // device properties (cached per device)
@@ -76,20 +89,14 @@ std::atomic<int>& gemv_max_m_value() {
 
 int gemv_max_m() { return gemv_max_m_value().load(std::memory_order_relaxed); }
 
-// Past the crossover, layers of up to 24 Mi weight elements keep the GEMV up to its largest M:
-// measured per layer on a GB300 (CUDA graph replay, the GEMV's tcgen05 main loop at 17..32
-// tokens against the split GEMM), the GEMV wins on TinyLlama's four linears (4-23 M: 7.4-14.5
-// vs 11.3-15.0 us) and Mistral-7B o_proj (16 M: 11.7-13.1 vs 14.0-14.4 us), ties on qkv (24 M:
-// 14.4-16.5 vs 15.7-16.5 us), and loses on gate_up and down (117 and 59 M) from 24 or 17
-// tokens on. Applies while the crossover is at least its default (fp8_set_gemv_max_m(0) still
-// sends everything to the GEMM).
-constexpr int64_t kSmallWeightElems = int64_t(24) << 20;
-
+// The GEMV runs every M up to the crossover (default 32, its largest): measured per layer on a
+// GB300 (CUDA graph replay), at 17..32 tokens the GEMV on once-quantized activations with its
+// tcgen05 main loop beats or ties the split GEMM on every Mistral-7B and TinyLlama linear
+// (Mistral-7B down at 32 tokens 19.9 vs 22.6 us, gate_up 29.8 vs 29.1, qkv 13.7 vs 15.6;
+// TinyLlama 8.0-13.5 vs 11.1-14.8 us), and below 17 tokens by more.
 bool use_gemv(int64_t M, int64_t K, int64_t N) {
-  if (K > kGemvMaxK) return false;
-  const int t = gemv_max_m();
-  if (M <= t) return true;
-  return t >= gemv::kDefaultMaxM && M <= gemv::kMaxTokens && N * K <= kSmallWeightElems;
+  (void)N;
+  return K <= kGemvMaxK && M <= gemv_max_m();
 }
 
 // Weight tiles the GEMV issues before its activation loads have landed (FP8W8A8_GEMV_HEAD
@@ -297,7 +304,7 @@ bool gemv_tc(int NT, int mode) {
     const int v = e ? std::atoi(e) : 4;
     return v <= 0 ? 1 << 20 : v <= 2 ? 2 : 4;
   }();
-  return NT >= from && mode != gemv::kModeBf16;
+  return NT >= from && mode == gemv::kModePrequant;
 }
 
 fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uint8_t* qw, int64_t ldqw,
@@ -396,9 +403,12 @@ fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uin
     std::fprintf(stderr, "fp8w8a8: gemv M=%d N=%d K=%d mode=%d cluster=%d clusters=%d stages=%d kslice=%d smem=%zu "
                  "scratch=%d cluster_amax=%d\n", p.M, p.N, p.K, mode, bS, bC, bstages, bslice, bsmem, p.scratch_a,
                  p.cluster_amax);
-  CUtensorMap map;
+  CUtensorMap map, amap;
   if (!make_fp8_tensor_map(&map, qw, p.N, p.K, ldqw, kRows)) return FP8_ERR_CUDA;
-  return launch(kfn, dim3(bC * bS), dim3(kThreads), bsmem, st, true, dim3(bS, 1, 1), map, p);
+  amap = map;  // unused unless the pre-quantized tcgen05 kernel loads qA by TMA
+  if (tc && mode == kModePrequant && !make_fp8_tensor_map(&amap, p.qa, p.M, p.K, p.ldqa, uint32_t(act_rows)))
+    return FP8_ERR_CUDA;
+  return launch(kfn, dim3(bC * bS), dim3(kThreads), bsmem, st, true, dim3(bS, 1, 1), map, amap, p);
 }
 
 // ---------------------------------------------------------------------------
@@ -437,8 +447,10 @@ fp8_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
 
 // Decode shapes need no workspace (the GEMV quantizes A itself); the GEMM path holds the
 // partial amax values, s_a and qA [M, round_up(K, 16)]: the least a GEMM-path call accepts.
+// Workspace of fp8_linear: the partial amax values, s_a and qA, except for the GEMV at up to
+// 16 tokens, which quantizes A itself.
 size_t linear_ws_bytes(int64_t M, int64_t K, int64_t N) {
-  if (M <= 0 || K <= 0 || use_gemv(M, K, N)) return 0;
+  if (M <= 0 || K <= 0 || (use_gemv(M, K, N) && M <= gemv_self_quant_max_m())) return 0;
   return FP8_QUANT_WORKSPACE_BYTES + size_t(M) * size_t(round_up16(K));
 }
 
@@ -449,7 +461,7 @@ size_t round_up_256(size_t b) { return (b + 255) / 256 * 256; }
 // A call given less (but at least linear_ws_bytes) splits only as far as its workspace holds.
 size_t linear_ws_bytes_full(int64_t M, int64_t K, int64_t N) {
   const size_t base = linear_ws_bytes(M, K, N);
-  if (base == 0 || N <= 0) return base;
+  if (base == 0 || N <= 0 || use_gemv(M, K, N)) return base;
   const int S = fp8k::plan_splits(M, N, K, 152, 76, SIZE_MAX);
   return S > 1 ? round_up_256(base) + fp8k::splitk_bytes(M, N, S) : base;
 }
@@ -471,7 +483,8 @@ fp8_status linear_impl(const void* a, int64_t M, int64_t K, int64_t lda, int fmt
   if (K == 0) return launch_fill_bias(bias, y, M, N, ldy, sms, st);
 
   const BF16Mat A{static_cast<const uint16_t*>(a), M, K, lda};
-  if (use_gemv(M, K, N)) {
+  const bool gemv = use_gemv(M, K, N);
+  if (gemv && M <= gemv_self_quant_max_m()) {
     // decode: one persistent GEMV kernel quantizes A (cluster-wide amax, or the static
     // scale) and streams qW
     gemv::Params p = gemv_params(nullptr, 0, nullptr, s_w, per_channel, bias, y, ldy, M, N, K);
@@ -481,16 +494,12 @@ fp8_status linear_impl(const void* a, int64_t M, int64_t K, int64_t lda, int fmt
     p.s_static = s_static;
     return launch_gemv(p, gemv::kModeQuantize, fmt_a, fmt_w, qw, ldqw, st);
   }
+  // A is quantized once into the workspace (amax pass and cast, or the cast with the static
+  // scale), then the GEMM, or for 17..32 tokens the GEMV on the pre-quantized activations
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* partials = reinterpret_cast<float*>(wsb);
   uint8_t* qa = wsb + kWsQaOffset;
   const int64_t ldqa = round_up16(K);
-  // split-K scratch past qA, when the workspace holds it
-  const size_t split_off = round_up_256(linear_ws_bytes(M, K, N));
-  const fp8k::SplitK sk =
-      ws_bytes > split_off
-          ? fp8k::gemm_split_plan(qa, ldqa, qw, ldqw, int(M), int(N), int(K), sms, wsb + split_off, ws_bytes - split_off)
-          : fp8k::SplitK();
   const float* s_a = s_static;
   if (s_static == nullptr) {
     float* s_dyn = reinterpret_cast<float*>(wsb + kWsScaleOffset);
@@ -501,6 +510,15 @@ fp8_status linear_impl(const void* a, int64_t M, int64_t K, int64_t lda, int fmt
   } else {
     FP8_TRY(launch_cast(A, nullptr, 0, s_static, nullptr, qa, ldqa, fmt_a, sms, st, true));
   }
+  if (gemv)
+    return launch_gemv(gemv_params(qa, ldqa, s_a, s_w, per_channel, bias, y, ldy, M, N, K), gemv::kModePrequant,
+                       fmt_a, fmt_w, qw, ldqw, st);
+  // split-K scratch past qA, when the workspace holds it
+  const size_t split_off = round_up_256(linear_ws_bytes(M, K, N));
+  const fp8k::SplitK sk =
+      ws_bytes > split_off
+          ? fp8k::gemm_split_plan(qa, ldqa, qw, ldqw, int(M), int(N), int(K), sms, wsb + split_off, ws_bytes - split_off)
+          : fp8k::SplitK();
   if (gemm_launch(qa, ldqa, s_a, qw, ldqw, s_w, per_channel, static_cast<const uint16_t*>(bias),
                   static_cast<uint16_t*>(y), ldy, int(M), int(N), int(K), fmt_a, fmt_w, sms, st, sk) != 0)
     return FP8_ERR_CUDA;

@@ -23,7 +23,7 @@ KernelFn pick(int fa, int fw) {
 
 template <int NT, bool Tc>
 KernelFn pick_mode(int mode, int fa, int fw) {
-  if (mode == kModeQuantize) return pick<NT, kModeQuantize, Tc>(fa, fw);
+  if (mode == kModeQuantize) return pick<NT, kModeQuantize, false>(fa, fw);
   if (mode == kModeBf16) return pick<NT, kModeBf16, false>(fa, fw);
   return pick<NT, kModePrequant, Tc>(fa, fw);
 }

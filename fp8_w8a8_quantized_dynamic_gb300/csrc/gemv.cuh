@@ -231,18 +231,20 @@ __device__ __forceinline__ uint32_t abs_max_units(uint32_t m2, const uint4 (&v)[
 // over all of A computed by every CTA (p.cluster_amax == 0, small M*K), or each rank's slice
 // maximum exchanged over the cluster through distributed shared memory.
 //
-// kTc (FP8 activations, two or four token tiles; the host takes it for four): the tensor
-// cores' tcgen05 path runs the main loop instead of mma.sync, whose FP8 rate (about 38 cycles
-// per m16n8k32 per SM sub-partition, measured on the GB300 through the per-token-tile cost)
-// makes four token tiles about twice as slow as the weight stream. Each weight tile is the M = 128 operand as TMA left it; the quantized
-// activations are stored per 128-byte K block as [tokens][128 B] in the same 128-byte swizzle
-// and are the N = 8 * NT operand; accumulators (two, alternating by row block) live in tensor
-// memory. Warp 0's first lane issues the MMAs and commits each stage back to the producer;
-// warps 4..7 read finished accumulators and push the partials to their owners.
+// kTc (pre-quantized FP8 activations, two or four token tiles; the host takes it for four):
+// the tensor cores' tcgen05 path runs the main loop instead of mma.sync, whose FP8 rate (about
+// 38 cycles per m16n8k32 per SM sub-partition, measured on the GB300 through the per-token-tile
+// cost) makes four token tiles about twice as slow as the weight stream. Each weight tile is
+// the M = 128 operand as TMA left it; the activations arrive by TMA per 128-byte K block as
+// [tokens][128 B] in the same 128-byte swizzle and are the N = 8 * NT operand; accumulators
+// (two, alternating by row block) live in tensor memory. Warp 0's first lane issues the MMAs
+// and commits each stage back to the producer; warps 4..7 read finished accumulators and push
+// the partials to their owners.
 template <int NT, int kMode, int FA, int FW, bool kTc>
 __global__ void __launch_bounds__(kThreads, 1)
-gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ Params p) {
-  static_assert(!kTc || (NT >= 2 && kMode != kModeBf16), "tcgen05 path: FP8 activations, 9 to 32 tokens");
+gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
+            const __grid_constant__ Params p) {
+  static_assert(!kTc || (NT >= 2 && kMode == kModePrequant), "tcgen05 path: pre-quantized FP8 activations");
   unsigned int* err = &g_gemv_error;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -265,13 +267,8 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
   const int ntiles = (kspan + kTileK - 1) / kTileK;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool cluster_amax = kMode == kModeQuantize && p.s_static == nullptr && p.cluster_amax;
-  // FP8 activation byte (token m, slice column kk; kk % 8 == 0 for the stores below)
-  auto act_at = [&](int m, int kk) -> uint32_t {
-    if constexpr (kTc)
-      return act + uint32_t((kk >> 7) * (p.act_rows * 128) + m * 128 + ((((kk >> 4) & 7) ^ (m & 7)) << 4) + (kk & 15));
-    else
-      return act + uint32_t(m * p.act_stride + kk);
-  };
+  // FP8 activation byte (token m, slice column kk) of the mma.sync layout
+  auto act_at = [&](int m, int kk) -> uint32_t { return act + uint32_t(m * p.act_stride + kk); };
 
   __shared__ int abort_flag;
   __shared__ uint32_t tmem_sh;
@@ -516,6 +513,17 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
           }
         }
       }
+      loads_back();
+    } else if constexpr (kTc) {
+      s_a = *p.s_a;
+      // the qA slice arrives by TMA, one [act_rows tokens x 128 B] box per K block, already in
+      // the swizzled layout the MMAs read (zero past M and K)
+      if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(abar, uint32_t(ntiles * p.act_rows * kTileK));
+        for (int kt = 0; kt < ntiles; ++kt)
+          tma_load_2d(act + uint32_t(kt * p.act_rows * kTileK), &tmap_a, abar, k0 + kt * kTileK, 0);
+      }
+      mbar_wait_bounded(abar, 0, ab, err);
       loads_back();
     } else {
       s_a = *p.s_a;

@@ -18,7 +18,7 @@ constexpr int kTileBytes = kRows * kTileK;            // 16 KB
 constexpr int kMaxStages = 12;
 constexpr int kMinStages = 4;
 constexpr int kMaxTokens = 32;                        // largest M (four n8 token tiles)
-constexpr int kDefaultMaxM = 16;                      // default decode crossover (M <= this runs the GEMV)
+constexpr int kDefaultMaxM = 32;                      // default decode crossover (M <= this runs the GEMV)
 constexpr int kMaxCluster = 8;
 constexpr int kMaxRowBlocks = 8;                      // per cluster (partials live in smem)
 
@@ -83,7 +83,9 @@ __host__ __device__ inline Layout layout(int stages, int act_stride, int act_row
 // One instantiation of the kernel: NT n8 token tiles (1: M <= 8, 2: M <= 16, 4: M <= 32), activation
 // mode (kMode*), FP8 formats of the activations (fa, unused for kModeBf16) and weights (fw), and
 // the main loop on tcgen05 (tc; NT >= 2 with FP8 activations) or on mma.sync.
-using KernelFn = void (*)(CUtensorMap, Params);
+// The second tensor map covers qA [M, K] in [8 * NT rows x 128 B] boxes (pre-quantized mode on
+// tcgen05); the other kernels ignore it.
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, Params);
 KernelFn kernel_for(int NT, int mode, int fa, int fw, bool tc);
 
 // Enqueues the failure-path self-test kernel (a bounded wait made to run out after limit_ns).

@@ -85,27 +85,26 @@ typedef enum fp8_format {
 int64_t fp8_min_ld(int64_t K);
 
 /* Bytes of workspace fp8_linear / fp8_linear_channelwise use for this shape.
- * 0 for decode shapes (fp8_uses_gemv): the GEMV quantizes A itself. GEMM
- * shapes need at least FP8_QUANT_WORKSPACE_BYTES (partial amax values, s_a)
- * plus the quantized activations qA [M, fp8_min_ld(K)]. Shapes with too few
+ * 0 for decode shapes of up to 16 tokens (fp8_uses_gemv): the GEMV quantizes A
+ * itself. Every other shape (the GEMV at 17..32 tokens, the GEMM) needs at
+ * least FP8_QUANT_WORKSPACE_BYTES (partial amax values, s_a) plus the
+ * quantized activations qA [M, fp8_min_ld(K)]. GEMM shapes with too few
  * output tiles to fill the GPU (small M) split K across CTAs when the
- * workspace also holds, from the next 256-byte boundary, a per-tile arrival
- * counter and fp32 partials [splits, M, N rounded up to 4]; the value returned
- * includes that space for the split a GB300 (152 SMs) takes. A workspace
- * between the two sizes works too, with a smaller split or none. 0 when M or
- * K is 0. Host-only, never touches the device. */
+ * workspace also holds, from the next 256-byte boundary, fp32 partials
+ * [splits, M, N rounded up to 4]; the value returned includes that space for
+ * the split a GB300 (152 SMs) takes. A workspace between the two sizes works
+ * too, with a smaller split or none. 0 when M or K is 0. Host-only, never
+ * touches the device. */
 size_t fp8_workspace_bytes(int64_t M, int64_t K, int64_t N);
 
 /* 1 when fp8_linear takes the decode GEMV path for this shape, 0 for the GEMM path:
- * M <= the crossover (16 by default, see fp8_set_gemv_max_m), and, while the crossover is at
- * least 16, also M <= 32 for layers of N * K <= 24 Mi elements, where the GEMV was
- * measured faster; K <= 32768 in both cases. Host-only. */
+ * M <= the crossover (32 by default, see fp8_set_gemv_max_m) and K <= 32768. Host-only. */
 int fp8_uses_gemv(int64_t M, int64_t K, int64_t N);
 
 /* Sets the decode crossover: calls with M <= m (and K <= 32768) run the GEMV,
  * larger M the GEMM. m is clamped to [0, 32] (32 is the GEMV's largest M; 0
  * sends every shape to the GEMM); m < 0 only queries. Returns the previous
- * value. The start-up value is 16, or FP8W8A8_GEMV_MAX_M from the environment.
+ * value. The start-up value is 32, or FP8W8A8_GEMV_MAX_M from the environment.
  * Process-wide; it changes which kernels later calls enqueue (and so
  * fp8_workspace_bytes), never their results beyond the stated tolerance.
  * ("[WIP] FP8 support": decode runs at sequence length < 16 and wants its own

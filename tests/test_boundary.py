@@ -72,7 +72,7 @@ def test_workspace_and_dispatch(L):
         assert F.fp8_workspace_bytes(M, 4096, 4096) == 0
     # GEMM shapes hold the partial amax values, s_a and qA [M, min_ld(K)]; small M adds the
     # split-K fp32 partials [splits, M, N rounded up to 4] from the next 256-byte boundary
-    for M, K in ((17, 8192), (16384, 14336), (100, 4100)):
+    for M, K in ((33, 8192), (16384, 14336), (100, 4100)):
         assert not F.fp8_uses_gemv(M, K, 4096)
         assert F.min_workspace_bytes(M, K, 4096) == base + M * F.min_ld(K)
         ws = F.fp8_workspace_bytes(M, K, 4096)
@@ -81,7 +81,7 @@ def test_workspace_and_dispatch(L):
             split = ws - (base + M * F.min_ld(K) + 255) // 256 * 256
             assert split > 0 and split % (M * 4096 * 4) == 0 and 2 <= split // (M * 4096 * 4) <= 16
     assert F.fp8_workspace_bytes(16384, 14336, 4096) == base + 16384 * F.min_ld(14336)  # enough tiles: no split
-    assert F.fp8_workspace_bytes(17, 8192, 4096) > F.min_workspace_bytes(17, 8192, 4096)  # one row block: split
+    assert F.fp8_workspace_bytes(33, 8192, 4096) > F.min_workspace_bytes(33, 8192, 4096)  # one row block: split
     assert F.fp8_workspace_bytes(0, 4096, 4096) == 0
     assert not F.fp8_uses_gemv(4, 40000, 4096)  # K beyond the GEMV's slice budget -> GEMM
 
@@ -229,18 +229,24 @@ def test_weight_only_rejects_bad_arguments(L):
 
 
 def test_crossover_rule(L):
-    """M <= 16 runs the GEMV; 17..32 too for layers of at most 24 Mi weight elements (measured
-    faster there), unless the crossover is lowered; fp8_set_gemv_max_m(32) sends every M <= 32
-    to the GEMV and 0 sends everything to the GEMM."""
+    """M <= 32 runs the GEMV by default (the crossover): up to 16 tokens it quantizes A itself
+    (no workspace), from 17 on A is quantized once into the workspace first (no split-K
+    partials). fp8_set_gemv_max_m moves the crossover (32 at most; 0 sends everything to the
+    GEMM), and K beyond 32768 always takes the GEMM."""
+    import os
     prev = F.fp8_set_gemv_max_m(-1)
+    if "FP8W8A8_GEMV_MAX_M" not in os.environ:
+        assert prev == 32
     try:
-        assert F.fp8_set_gemv_max_m(16) == prev
-        assert F.fp8_uses_gemv(16, 4096, 4096) and F.fp8_uses_gemv(17, 2048, 2560) and F.fp8_uses_gemv(32, 2048, 4096)
-        assert F.fp8_uses_gemv(17, 4096, 6144) and F.fp8_uses_gemv(32, 4096, 4096)  # 24 Mi, 16 Mi
-        assert not F.fp8_uses_gemv(17, 4096, 6160) and not F.fp8_uses_gemv(33, 2048, 2560)
-        assert F.fp8_workspace_bytes(32, 2048, 2560) == 0 and F.fp8_workspace_bytes(17, 4096, 8192) > 0
         F.fp8_set_gemv_max_m(32)
-        assert F.fp8_uses_gemv(32, 14336, 4096)
+        assert F.fp8_uses_gemv(32, 14336, 28672) and not F.fp8_uses_gemv(33, 2048, 2560)
+        assert not F.fp8_uses_gemv(1, 40000, 2048)
+        base = F.FP8_QUANT_WORKSPACE_BYTES
+        assert F.fp8_workspace_bytes(16, 2048, 2560) == 0
+        assert F.fp8_workspace_bytes(32, 2048, 2560) == F.min_workspace_bytes(32, 2048, 2560) == base + 32 * 2048
+        assert F.fp8_workspace_bytes(33, 8192, 4096) > F.min_workspace_bytes(33, 8192, 4096)  # GEMM: partials
+        F.fp8_set_gemv_max_m(16)
+        assert F.fp8_uses_gemv(16, 4096, 4096) and not F.fp8_uses_gemv(17, 2048, 2560)
         F.fp8_set_gemv_max_m(8)
         assert not F.fp8_uses_gemv(9, 2048, 2560)
         F.fp8_set_gemv_max_m(0)

@@ -101,7 +101,7 @@ def test_decode_config_layers(layer, M):
 
 # --------------------------------------------------------------------------- prefill GEMM
 
-@pytest.mark.parametrize("M,K,N", [(17, 4096, 6401), (33, 256, 256), (128, 128, 256), (130, 1000, 1027), (300, 4100, 257),
+@pytest.mark.parametrize("M,K,N", [(40, 4096, 6401), (33, 256, 256), (128, 128, 256), (130, 1000, 1027), (300, 4100, 257),
                                    (257, 2050, 3001), (512, 4096, 512), (1000, 96, 520)])
 @pytest.mark.parametrize("per_channel", [False, True])
 def test_gemm_ragged(M, K, N, per_channel):
@@ -201,11 +201,12 @@ def _tinyllama_layer(depth, li, per_channel):
 
 
 @pytest.mark.parametrize("depth", [0, I.TINYLLAMA_DEPTH - 1])
-@pytest.mark.parametrize("M", sorted(set(I.TINYLLAMA_MS) | {17}))
+@pytest.mark.parametrize("M", sorted(set(I.TINYLLAMA_MS) | {17, 33}))
 def test_tinyllama_sweep_sampled(M, depth):
-    """Every M of the TinyLlama sweep (and M = 17, the first GEMM row count above the GEMV),
-    first and last layer of the stack, both weight modes: Y against the oracle on sampled rows
-    (all rows up to M = 64) and 386 sampled columns."""
+    """Every M of the TinyLlama sweep, plus M = 17 (the first row count the GEMV runs on
+    activations quantized beforehand) and 33 (the first on the GEMM), first and last layer of
+    the stack, both weight modes: Y against the oracle on sampled rows (all rows up to M = 64)
+    and 386 sampled columns."""
     from parity import assert_y_within_tolerance, f32, oracle_act
     for li, L in enumerate(I.TINYLLAMA_LAYERS):
         a = I.tinyllama_activations(M, depth, li)
@@ -346,7 +347,7 @@ def test_gemm_raster_groups(M, K, N):
         assert cfg["group_n"] == max(1, min(n_tiles, (28 << 20) // (256 * K)))
 
 
-SPLIT_SHAPES = [(17, 5632, 5120), (32, 14336, 4096), (64, 4096, 4096), (100, 4096, 6144), (128, 5632, 2048),
+SPLIT_SHAPES = [(40, 5632, 5120), (48, 14336, 4096), (64, 4096, 4096), (100, 4096, 6144), (128, 5632, 2048),
                 (33, 4100, 1027)]
 
 

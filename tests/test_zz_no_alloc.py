@@ -42,6 +42,7 @@ def call_noalloc(L, a, qw, s_w, per_channel, bias, y):
 @pytest.mark.gpu
 @pytest.mark.parametrize("M,K,N,per_channel", [(7, 2050, 3001, False),    # decode GEMV path
                                                (15, 4096, 4096, True),
+                                               (24, 4096, 2048, True),    # GEMV on A quantized first
                                                (300, 4100, 1027, True),   # tcgen05 GEMM path
                                                (1900, 4096, 768, False)])  # near the scratch limit
 def test_noalloc_matches_workspace_entry_point(L, M, K, N, per_channel):
