@@ -1,4 +1,4 @@
-// Decode-shape FP8 GEMV: Y[M<=16, N] = bf16(s_a * s_w[n] * sum_k qA[m,k] qW[n,k] (+ bias[n])).
+// Decode-shape FP8 GEMV: Y[M<=32, N] = bf16(s_a * s_w[n] * sum_k qA[m,k] qW[n,k] (+ bias[n])).
 // qA and qW are e4m3 or e5m2 ("Fp8 Quantization Support", the other FP8 dtype), each
 // operand's format a template parameter of the kernel.
 //

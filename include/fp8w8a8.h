@@ -279,7 +279,7 @@ fp8_status fp8_linear_ex(const void* a_bf16, int64_t M, int64_t K, int64_t lda, 
  * Every e4m3 / e5m2 value is a bf16 value, so the up-conversion is exact; the
  * weight scale multiplies the fp32 accumulator in the epilogue, as in the
  * channelwise identity (s_w,n W_n) A = s_w,n (W_n A).
- * Decode shapes (M <= 16, K <= 32768) run the split-K GEMV, which up-converts
+ * Decode shapes (M <= the crossover, K <= 32768) run the split-K GEMV, which up-converts
  * each weight tile in registers and needs no workspace; larger shapes
  * up-convert W into the workspace once per call and run a bf16 tcgen05 GEMM.
  * ---------------------------------------------------------------------------
