@@ -46,8 +46,10 @@
 //
 // Last wave: when the tiles left after the full waves number at most half of the slots (CTA
 // pairs, or CTAs), each of them is computed as 2 units of 128 columns over all of K (4 units of
-// 64 on request), so the partial last wave ends sooner. Those units load their weight rows
-// through a second tensor map with the narrower box and issue MMAs with the smaller N.
+// 64 on request), so the partial last wave ends sooner. When all tiles fit in half the slots
+// (small M) every tile is split that way, into 4 units where they fit, unless K is long enough
+// for the K split to win. Those units load their weight rows through a second tensor map with
+// the narrower box and issue MMAs with the smaller N.
 //
 // Every wait is bounded (2 s); on expiry the kernel records an error for the host (with a
 // bit naming the wait), stops its peer, drains every copy either CTA issued, frees its
@@ -763,6 +765,7 @@ struct GemmSwitches {
   int64_t l2_budget;
   bool hints;
   int tail;  // largest column split of the last wave's tiles (1: none)
+  bool fill;  // also split every tile (up to 4 ways) when the whole grid is one partial wave
   int serpentine;  // -1: planned, 0: never, 1: always
 };
 
@@ -775,6 +778,7 @@ const GemmSwitches& switches() {
     v.hints = env_int("FP8W8A8_GEMM_L2HINT", 1) != 0;
     const int t = env_int("FP8W8A8_GEMM_TAIL", 2);
     v.tail = t >= 4 ? 4 : t >= 2 ? 2 : 1;
+    v.fill = env_int("FP8W8A8_GEMM_FILL", 1) != 0;
     v.serpentine = env_int("FP8W8A8_GEMM_SERPENTINE", -1);
     return v;
   }();
@@ -838,6 +842,20 @@ int pair_clusters(int dev, const void* kernel) {
 
 }  // namespace
 
+namespace {
+
+// Small M, where all tiles fit in half the slots (CTA pairs or CTAs): every tile is split by
+// columns into 2 or 4 units over all of K. Measured per layer on a GB300 against the K split
+// (Mistral-7B and TinyLlama linears at 33..512 tokens): quarter tiles took TinyLlama qkv at 128
+// tokens 15.4 -> 11.8 us and Mistral-7B qkv 22.6 -> 17.9 us, and beat the K split up to 32 K
+// blocks (TinyLlama qkv at 33 tokens 13.3 -> 11.8 us); with longer K (the down projections'
+// 44-112 blocks) the K split stays far ahead.
+constexpr int kFillMaxKb = 32;
+
+bool fill_applies(int units, int slots) { return units > 0 && 2 * units <= slots && switches().fill; }
+
+}  // namespace
+
 // The launch configuration (host logic only; see GemmPlan).
 GemmPlan plan_gemm(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_bytes, int M, int N, int dev,
                    int num_sms, int pair_clusters_available) {
@@ -883,7 +901,7 @@ GemmPlan plan_gemm(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_
   pl.serpentine = sw.serpentine >= 0 ? sw.serpentine : (m_units > 1 && w_bytes > sw.l2_budget / 2 ? 1 : 0);
   // the last wave: when fewer tiles than slots are left after the full waves, split each of
   // them by columns into 2 or 4 units (all of K each) so that the wave ends sooner
-  const int slots = pl.two_sm ? std::min(units, pair_clusters_available) : std::min(units, num_sms);
+  const int slots = pl.two_sm ? pair_clusters_available : num_sms;  // co-resident CTA pairs or CTAs
   pl.tail_split = 1;
   pl.tail_start = units;
   const int rem = slots > 0 ? units % slots : 0;
@@ -894,6 +912,18 @@ GemmPlan plan_gemm(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_
         pl.tail_start = units - rem;
         break;
       }
+  } else if (fill_applies(units, slots)) {
+    // one partial wave only (small M): every tile split by columns, as far as the slots allow
+    for (int f = 4; f >= 2; f /= 2)
+      if (f * units <= slots) {
+        pl.tail_split = f;
+        pl.tail_start = 0;
+        break;
+      }
+  }
+  if (pl.tail_split > 1) {
+    const int split_units = pl.tail_start + (units - pl.tail_start) * pl.tail_split;
+    pl.grid = pl.two_sm ? 2 * std::min(split_units, pair_clusters_available) : std::min(split_units, num_sms);
   }
   return pl;
 }
@@ -961,6 +991,8 @@ int plan_splits(int64_t M, int64_t N, int64_t K, int num_sms, int pair_slots, si
   }
   // measured: with CTA pairs (two or more row blocks) a split never paid for itself
   if (two) return 1;
+  // short K on few tiles: the column split of every tile (plan_gemm) is faster
+  if (num_kb <= kFillMaxKb && fill_applies(units, slots)) return 1;
   return choose_splits(units, slots, num_kb, M, N, max_s);
 }
 
@@ -982,8 +1014,8 @@ int launch_kind(const void* a, int64_t lda_bytes, const float* s_a, const void* 
   GemmPlan pl = plan_gemm(a, lda_bytes, w, ldw_bytes, M, N, dev, num_sms, clusters);
   const int S = std::max(1, split.splits);
   const int num_kb = kBf16 ? (K + BK / 2 - 1) / (BK / 2) : (K + BK - 1) / BK;  // K blocks of 128 bytes
-  const int units = (pl.two_sm ? (pl.m_tiles + 1) / 2 : pl.m_tiles) * pl.n_tiles * S;
-  pl.grid = pl.two_sm ? 2 * std::min(units, clusters) : std::min(units, num_sms);
+  const int tiles = (pl.two_sm ? (pl.m_tiles + 1) / 2 : pl.m_tiles) * pl.n_tiles;
+  const int units = tiles * S;
 
   GemmParams p;
   p.M = M;
@@ -1010,6 +1042,8 @@ int launch_kind(const void* a, int64_t lda_bytes, const float* s_a, const void* 
   if (S > 1 && (split.part == nullptr || (num_kb + p.kb_per_split - 1) / p.kb_per_split != S)) return 4;
   p.tail_split = S > 1 ? 1 : pl.tail_split;  // a K split already fills the GPU
   p.tail_start = p.tail_split > 1 ? pl.tail_start : units;
+  const int work = p.tail_split > 1 ? p.tail_start + (tiles - p.tail_start) * p.tail_split : units;
+  pl.grid = pl.two_sm ? 2 * std::min(work, clusters) : std::min(work, num_sms);
   p.serpentine = pl.serpentine;
 
   CUtensorMap ma, mb, mbt;

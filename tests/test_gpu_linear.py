@@ -157,6 +157,22 @@ def test_gemm_tail_split_other_modes(pair, split):
     _in_child(f"t._tail_case({split})", FP8W8A8_GEMM_PAIR=pair, FP8W8A8_GEMM_TAIL=str(split))
 
 
+@pytest.mark.parametrize("M,K,N,f", [(100, 2048, 2560, 4), (300, 1000, 1027, 4), (257, 2050, 3001, 2)])
+def test_gemm_fill_split(M, K, N, f):
+    """Few tiles and short K: every tile of the one partial wave split by columns into f units
+    over all of K (one CTA per tile, and CTA pairs with a ragged second row block; four units
+    while they fit one wave of the 76 pairs / 152 CTAs, else two), per-channel scales and bias,
+    against the oracle with guard bands."""
+    qa = torch.zeros((M, F.min_ld(K)), dtype=torch.uint8, device=DEV)
+    qw = torch.zeros((N, F.min_ld(K)), dtype=torch.uint8, device=DEV)
+    cfg = F.fp8_gemm_config(qa, qw, K, F.fp8_workspace_bytes(M, K, N))
+    assert cfg["splits"] == 1 and cfg["tail_split"] == f, cfg
+    a = I.activations_heavy_tail(M, K, (934, M))
+    w = I.weights_row_std(N, K, (935, N))
+    b = I.bias_normal(N, (936, N))
+    check(a, w, True, b, f"fill split {M}x{K}x{N}", check_w=False)
+
+
 def test_gemm_strided_activations_and_output():
     M, K, N = 200, 1000, 300
     a = I.activations_normal(M, K, (908,))
@@ -347,7 +363,7 @@ def test_gemm_raster_groups(M, K, N):
         assert cfg["group_n"] == max(1, min(n_tiles, (28 << 20) // (256 * K)))
 
 
-SPLIT_SHAPES = [(40, 5632, 5120), (48, 14336, 4096), (64, 4096, 4096), (100, 4096, 6144), (128, 5632, 2048),
+SPLIT_SHAPES = [(40, 5632, 5120), (48, 14336, 4096), (64, 8192, 4096), (100, 8192, 6144), (128, 5632, 2048),
                 (33, 4100, 1027)]
 
 
