@@ -6,30 +6,30 @@
 // for a custom gemv rather than a 16-padded GEMM. The weight matrix is streamed from HBM
 // exactly once.
 //
-// Dynamic activation quantization happens inside this kernel: the ranks of a cluster
-// together cover all of K, so each rank's max |A| over its own K-slice, combined across the
-// cluster through distributed shared memory, is the global amax. Every CTA derives the same
-// s_a = amax / 448 and quantizes only its own slice, straight from the registers that
-// loaded it, while its TMA ring is already filling with weights. A static (calibrated)
-// activation scale skips the amax exchange. With pre-quantized activations
-// (fp8_scaled_mm) qA and s_a are read instead.
+// Up to 16 tokens, dynamic activation quantization happens inside this kernel: the ranks of
+// a cluster together cover all of K, so the maximum of the ranks' max |A| over their
+// K-slices, exchanged through distributed shared memory (or every CTA's maximum over all of a
+// small A), is the global amax. Every CTA derives the same s_a = amax / 448 and quantizes only
+// its own slice while its TMA ring is already filling with weights. A static (calibrated)
+// activation scale skips the amax. With pre-quantized activations (fp8_scaled_mm, and
+// fp8_linear from 17 tokens on, which quantizes A beforehand) qA and s_a are read instead.
 //
 // Work split. Rows of W come in blocks of 128; K is split over the S CTAs of a
 // thread-block cluster (rank r owns K-range [r*kslice, (r+1)*kslice)). The grid is
 // persistent: cluster c processes row blocks c, c + C, c + 2C, ... with C chosen on the
-// host so every CTA streams the same number of tiles. Each CTA keeps the fp32 partial sums
-// of its row blocks in shared memory; at the end one cluster barrier publishes them and
-// rank r reduces its share of the rows over all ranks in a fixed order (deterministic,
-// no global scratch), applies the scale/bias epilogue and writes Y.
+// host so every CTA streams the same number of tiles. Each CTA pushes the fp32 partial sums
+// of its row blocks into the shared memory of the ranks that own those rows; one cluster
+// barrier publishes them and rank r reduces its share of the rows over all ranks in a fixed
+// order (deterministic, no global scratch), applies the scale/bias epilogue and writes Y.
 //
 // Streaming. Warp 8 is a TMA producer: 2-D tensor-map loads of [128 rows x 128 B] weight
-// tiles (128B-swizzled, 16 KB) into an mbarrier ring of up to 8 stages, issued from kernel
-// entry — before the wait on the preceding (quantize) kernel — so up to 128 KB per SM is in
-// flight at once. Warps 0..7 (16 rows each) read their rows from the tile and run
-// mma.sync m16n8k32 e4m3 x e4m3 -> f32 with W rows as the MMA's M dimension and tokens as
-// its N dimension. The k order inside each 64-byte half-row is permuted so that a lane
-// (group g, thread t) takes one 16-byte load of row g and one of row g+8 per half; the
-// activation fragment uses the same permutation, which is plain row-major [token][k].
+// tiles (128B-swizzled, 16 KB) into an mbarrier ring of up to 12 stages; the first tiles are
+// issued from kernel entry, before the wait on the preceding kernel. Up to two n8 token tiles,
+// warps 0..7 (16 rows each) read their rows from the tile and run mma.sync m16n8k32 with W
+// rows as the MMA's M dimension and tokens as its N dimension. The k order inside each 64-byte
+// half-row is permuted so that a lane (group g, thread t) takes one 16-byte load of row g and
+// one of row g+8 per half; the activation fragment uses the same permutation, which is plain
+// row-major [token][k]. With four token tiles the main loop runs on tcgen05 (kTc, below).
 #pragma once
 
 #include "device_common.cuh"
