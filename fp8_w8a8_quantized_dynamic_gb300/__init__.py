@@ -66,6 +66,7 @@ _SIGNATURES = {
     "fp8_linear_weight_only": (_int, [_vp, _i64, _i64, _i64, _vp, _int, _i64, _i64, _vp, _int, _vp, _vp, _i64,
                                       _vp, _sz, _vp]),
     "fp8_gemm_config": (_int, [_vp, _i64, _i64, _vp, _i64, _i64, _i64, _sz, _vp, _vp, _vp, _vp, _vp]),
+    "fp8_gemm_plan_model": (_int, [_i64, _i64, _i64, _int, _int, _sz, _vp, _vp, _vp, _vp, _vp]),
     "fp8_last_device_status": (_int, [_vp]),
     "fp8_selftest_timeout": (_int, [_i64, _vp]),
     "fp8_status_string": (ctypes.c_char_p, [_int]),
@@ -376,6 +377,19 @@ def fp8_gemm_config(qa, qw, K: Optional[int] = None, ws_bytes: int = 0) -> dict:
                                ctypes.byref(sp), ctypes.byref(ts))
     if st != FP8_OK:
         raise FP8Error(st, "fp8_gemm_config")
+    return {"two_sm": bool(two.value), "grid": grid.value, "group_n": gn.value, "splits": sp.value,
+            "tail_split": ts.value}
+
+
+def fp8_gemm_plan_model(M: int, N: int, K: int, num_sms: int = 152, pair_slots: int = 76, ws_bytes: int = 0) -> dict:
+    """The GEMM launch plan fp8_gemm_config would report for gap-free FP8 operands in a GPU's own
+    memory, computed on the host (no device): same keys."""
+    two, grid, gn, sp, ts = (ctypes.c_int(0) for _ in range(5))
+    st = lib().fp8_gemm_plan_model(int(M), int(N), int(K), int(num_sms), int(pair_slots), int(ws_bytes),
+                                   ctypes.byref(two), ctypes.byref(grid), ctypes.byref(gn), ctypes.byref(sp),
+                                   ctypes.byref(ts))
+    if st != FP8_OK:
+        raise FP8Error(st, "fp8_gemm_plan_model")
     return {"two_sm": bool(two.value), "grid": grid.value, "group_n": gn.value, "splits": sp.value,
             "tail_split": ts.value}
 

@@ -772,6 +772,19 @@ FP8_API fp8_status fp8_linear_weight_only(const void* a_bf16, int64_t M, int64_t
                           ws_bytes, stream);
 }
 
+// The launch a plan and a K split give: CTAs, raster group, split counts (both queries below).
+void report_plan(const fp8k::GemmPlan& pl, int S, int sms, int* two_sm, int* grid, int* group_n, int* splits,
+                 int* tail_split) {
+  const int m_units = pl.two_sm ? (pl.m_tiles + 1) / 2 : pl.m_tiles;
+  if (two_sm) *two_sm = pl.two_sm;
+  if (grid) *grid = S > 1 ? (pl.two_sm ? std::min(pl.grid, 2 * m_units * pl.n_tiles * S)
+                                       : std::min(sms, m_units * pl.n_tiles * S))
+                          : pl.grid;
+  if (group_n) *group_n = pl.group_n;
+  if (splits) *splits = S;
+  if (tail_split) *tail_split = S > 1 ? 1 : pl.tail_split;
+}
+
 FP8_API fp8_status fp8_gemm_config(const uint8_t* qa, int64_t M, int64_t ldqa, const uint8_t* qw, int64_t N,
                                    int64_t ldqw, int64_t K, size_t ws_bytes, int* two_sm, int* grid, int* group_n,
                                    int* splits, int* tail_split) {
@@ -788,14 +801,21 @@ FP8_API fp8_status fp8_gemm_config(const uint8_t* qa, int64_t M, int64_t ldqa, c
     alignas(256) static unsigned char probe[256];
     S = fp8k::gemm_split_plan(qa, ldqa, qw, ldqw, int(M), int(N), int(K), sms, probe, ws_bytes - split_off).splits;
   }
-  const int m_units = pl.two_sm ? (pl.m_tiles + 1) / 2 : pl.m_tiles;
-  if (two_sm) *two_sm = pl.two_sm;
-  if (grid) *grid = S > 1 ? (pl.two_sm ? std::min(pl.grid, 2 * m_units * pl.n_tiles * S)
-                                       : std::min(sms, m_units * pl.n_tiles * S))
-                          : pl.grid;
-  if (group_n) *group_n = pl.group_n;
-  if (splits) *splits = S;
-  if (tail_split) *tail_split = S > 1 ? 1 : pl.tail_split;
+  report_plan(pl, S, sms, two_sm, grid, group_n, splits, tail_split);
+  return FP8_OK;
+}
+
+FP8_API fp8_status fp8_gemm_plan_model(int64_t M, int64_t N, int64_t K, int num_sms, int pair_slots, size_t ws_bytes,
+                                       int* two_sm, int* grid, int* group_n, int* splits, int* tail_split) {
+  if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim || num_sms <= 0 || pair_slots < 0)
+    return FP8_ERR_INVALID_ARG;
+  const int64_t ld = round_up16(K);
+  const fp8k::GemmPlan pl = fp8k::plan_gemm_model(ld, ld, int(M), int(N), true, num_sms, pair_slots);
+  const size_t split_off = round_up_256(linear_ws_bytes(M, K, N));
+  int S = 1;
+  if (!use_gemv(M, K, N) && ws_bytes > split_off)
+    S = fp8k::plan_splits(M, N, K, num_sms, pl.two_sm ? pair_slots : 0, ws_bytes - split_off);
+  report_plan(pl, S, num_sms, two_sm, grid, group_n, splits, tail_split);
   return FP8_OK;
 }
 

@@ -859,13 +859,19 @@ bool fill_applies(int units, int slots) { return units > 0 && 2 * units <= slots
 // The launch configuration (host logic only; see GemmPlan).
 GemmPlan plan_gemm(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_bytes, int M, int N, int dev,
                    int num_sms, int pair_clusters_available) {
+  return plan_gemm_model(lda_bytes, ldw_bytes, M, N, local_device_memory(a, dev) && local_device_memory(w, dev),
+                         num_sms, pair_clusters_available);
+}
+
+GemmPlan plan_gemm_model(int64_t lda_bytes, int64_t ldw_bytes, int M, int N, bool local, int num_sms,
+                         int pair_clusters_available) {
   using namespace gemm;
+  (void)lda_bytes;
   const GemmSwitches& sw = switches();
   GemmPlan pl;
   pl.m_tiles = (M + BM - 1) / BM;
   pl.n_tiles = (N + BN - 1) / BN;
-  pl.two_sm = sw.pair && pl.m_tiles >= 2 && 2 * pair_clusters_available >= (3 * num_sms) / 4 &&
-              local_device_memory(a, dev) && local_device_memory(w, dev);
+  pl.two_sm = sw.pair && pl.m_tiles >= 2 && 2 * pair_clusters_available >= (3 * num_sms) / 4 && local;
   const int m_units = pl.two_sm ? (pl.m_tiles + 1) / 2 : pl.m_tiles;
   const int units = m_units * pl.n_tiles;
   pl.splits = 1;

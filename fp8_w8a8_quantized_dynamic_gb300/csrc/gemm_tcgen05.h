@@ -65,6 +65,11 @@ struct GemmPlan {
 GemmPlan plan_gemm(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_bytes, int M, int N, int dev,
                    int num_sms, int pair_clusters_available);
 
+// The same rules without a device: `local` says whether both operands are this GPU's own memory,
+// `pair_clusters_available` how many CTA pairs are co-resident (host logic only).
+GemmPlan plan_gemm_model(int64_t lda_bytes, int64_t ldw_bytes, int M, int N, bool local, int num_sms,
+                         int pair_clusters_available);
+
 // The plan gemm_launch would use on the current device (queries pointer attributes and occupancy).
 GemmPlan gemm_plan(const void* a, int64_t lda_bytes, const void* w, int64_t ldw_bytes, int M, int N, int num_sms);
 

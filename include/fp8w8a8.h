@@ -321,6 +321,14 @@ fp8_status fp8_gemm_config(const uint8_t* qa, int64_t M, int64_t ldqa, const uin
                            int64_t ldqw, int64_t K, size_t ws_bytes, int* two_sm, int* grid, int* group_n,
                            int* splits, int* tail_split);
 
+/* The same plan as fp8_gemm_config, computed on the host without a device for a GPU with
+ * num_sms SMs and pair_slots co-resident CTA pairs (0: no pair mode), with both operands in
+ * that GPU's own memory and gap-free (leading dimension fp8_min_ld(K)). Outputs as above
+ * (NULL allowed). FP8_ERR_INVALID_ARG for non-positive sizes or num_sms, negative pair_slots.
+ * Host-only, never touches the device. */
+fp8_status fp8_gemm_plan_model(int64_t M, int64_t N, int64_t K, int num_sms, int pair_slots, size_t ws_bytes,
+                               int* two_sm, int* grid, int* group_n, int* splits, int* tail_split);
+
 /*
  * Synchronizes `stream`, then reports and clears device-side errors recorded
  * by the library's kernels on the current device since the last query
