@@ -745,6 +745,11 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     }
   }
   // no rank reads another's shared memory after the barrier above, so no second barrier
+  // the activation copies into shared memory (TMA boxes of qA, or bulk copies of A) complete
+  // on abar: after a wait that gave up they may still be landing, so the issuing thread
+  // waits for them (bounded) before the CTA's shared memory is released
+  if (threadIdx.x == 0 && ((kTc && kMode == kModePrequant) || (kMode == kModeQuantize && p.scratch_a != 0)))
+    mbar_wait_bounded(abar, 0, nullptr, err);
   if constexpr (kTc) {
     tc_fence_before();
     __syncthreads();
