@@ -395,8 +395,8 @@ def fp8_gemm_plan_model(M: int, N: int, K: int, num_sms: int = 152, pair_slots: 
 
 
 def min_workspace_bytes(M: int, K: int, N: int) -> int:
-    """The least workspace fp8_linear accepts for this shape (no K split): 0 for decode shapes the
-    GEMV quantizes itself (up to 8 tokens, and up to 16 with K <= 8192)."""
-    if M <= 0 or K <= 0 or ((M <= 8 or (M <= 16 and K <= 8192)) and fp8_uses_gemv(M, K, N)):
+    """The least workspace fp8_linear accepts for this shape (no K split): 0 for decode shapes of
+    up to 16 tokens, which the GEMV quantizes itself."""
+    if M <= 0 or K <= 0 or (M <= 16 and fp8_uses_gemv(M, K, N)):
         return 0
     return FP8_QUANT_WORKSPACE_BYTES + M * min_ld(K)

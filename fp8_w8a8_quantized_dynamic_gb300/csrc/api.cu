@@ -43,17 +43,6 @@ int64_t gemv_self_quant_max_m() {
   return v;
 }
 
-// Long K (more than 8192) from 9 tokens on: quantizing A once and running the two-token-tile
-// GEMV on tcgen05 measured faster than the in-kernel quantization (Mistral-7B down, K = 14336,
-// at M = 9 / 12 / 16: 19.8 / 20.5 / 21.4 -> 19.2 / 19.2 / 19.3 us); with K <= 8192 it was
-// slower on every layer measured (+0.7 to +1.6 us).
-constexpr int64_t kLongK = 8192;
-
-// The GEMV quantizes A itself (no workspace) for this shape.
-bool gemv_self_quant(int64_t M, int64_t K) {
-  return M <= gemv_self_quant_max_m() && !(M > 8 && K > kLongK);
-}
-
 // ---------------------------------------------------------------------------
 // device properties (cached per device)
 // ---------------------------------------------------------------------------
@@ -309,15 +298,13 @@ int gemv_act_stride(int mode, int kslice, bool tc) {
 // keeps up and the tensor-memory round trip only adds latency (measured per layer on a GB300:
 // Mistral-7B gate_up at M = 32, 49.6 -> 40.5 us; qkv at M = 12, 12.3 -> 12.9 us).
 // FP8W8A8_GEMV_TC: 0 never, 2 from two token tiles on (measurement switches).
-// Two token tiles take it too when K is long (see kLongK).
-bool gemv_tc(int NT, int mode, int64_t K) {
+bool gemv_tc(int NT, int mode) {
   static const int from = [] {
     const char* e = std::getenv("FP8W8A8_GEMV_TC");
     const int v = e ? std::atoi(e) : 4;
     return v <= 0 ? 1 << 20 : v <= 2 ? 2 : 4;
   }();
-  if (mode != gemv::kModePrequant || from > 4) return false;
-  return NT >= from || (NT == 2 && K > kLongK);
+  return NT >= from && mode == gemv::kModePrequant;
 }
 
 fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uint8_t* qw, int64_t ldqw,
@@ -329,7 +316,7 @@ fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uin
   const int max_slice = mode == kModeBf16 ? kMaxSliceBf16 : kMaxSlice;
   const int NT = p.M <= 8 ? 1 : p.M <= 16 ? 2 : 4;
   const int act_rows = 8 * NT;
-  const bool tc = gemv_tc(NT, mode, p.K);
+  const bool tc = gemv_tc(NT, mode);
   const KernelFn kfn = kernel_for(NT, mode, fmt_a, fmt_w, tc);
   const int smem_limit = gemv_smem_limit(kfn);
   auto smem_for = [&](int stg, int act_stride, int nrb) {
@@ -463,7 +450,7 @@ fp8_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
 // Workspace of fp8_linear: the partial amax values, s_a and qA, except for the GEMV at up to
 // 16 tokens, which quantizes A itself.
 size_t linear_ws_bytes(int64_t M, int64_t K, int64_t N) {
-  if (M <= 0 || K <= 0 || (use_gemv(M, K, N) && gemv_self_quant(M, K))) return 0;
+  if (M <= 0 || K <= 0 || (use_gemv(M, K, N) && M <= gemv_self_quant_max_m())) return 0;
   return FP8_QUANT_WORKSPACE_BYTES + size_t(M) * size_t(round_up16(K));
 }
 
@@ -497,7 +484,7 @@ fp8_status linear_impl(const void* a, int64_t M, int64_t K, int64_t lda, int fmt
 
   const BF16Mat A{static_cast<const uint16_t*>(a), M, K, lda};
   const bool gemv = use_gemv(M, K, N);
-  if (gemv && gemv_self_quant(M, K)) {
+  if (gemv && M <= gemv_self_quant_max_m()) {
     // decode: one persistent GEMV kernel quantizes A (cluster-wide amax, or the static
     // scale) and streams qW
     gemv::Params p = gemv_params(nullptr, 0, nullptr, s_w, per_channel, bias, y, ldy, M, N, K);

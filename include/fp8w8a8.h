@@ -85,9 +85,8 @@ typedef enum fp8_format {
 int64_t fp8_min_ld(int64_t K);
 
 /* Bytes of workspace fp8_linear / fp8_linear_channelwise use for this shape.
- * 0 for decode shapes (fp8_uses_gemv) of up to 8 tokens, or up to 16 with
- * K <= 8192: the GEMV quantizes A itself. Every other shape (the GEMV on A
- * quantized beforehand, the GEMM) needs at
+ * 0 for decode shapes of up to 16 tokens (fp8_uses_gemv): the GEMV quantizes A
+ * itself. Every other shape (the GEMV at 17..32 tokens, the GEMM) needs at
  * least FP8_QUANT_WORKSPACE_BYTES (partial amax values, s_a) plus the
  * quantized activations qA [M, fp8_min_ld(K)]. GEMM shapes with too few
  * output tiles to fill the GPU (small M) split K across CTAs when the
