@@ -510,7 +510,8 @@ def run_ours(args):
         wbytes_step = copies * sum(L.N * L.K for L in layers)
         yd = [torch.empty((16, L.N), dtype=torch.bfloat16, device=dev) for L in layers]
         per_m, per_layer = {}, {}
-        for Md in I.DECODE_MS:
+        decode_ms = args.decode_ms or list(I.DECODE_MS)
+        for Md in decode_ms:
             ad = [I.decode_activations(Md, i).to(dev) for i in li]
             ydm = [y[:Md] for y in yd]
 
@@ -541,7 +542,8 @@ def run_ours(args):
         decode = {"metric": "decode weight GB/s (one fused quantize + split-K GEMV kernel per layer, "
                             "CUDA graph replay of the 4 layers x weight copies)", "unit": "GB/s",
                   "value": round(statistics.median(gbs), 1), "per_M": per_m, "per_layer": per_layer,
-                  "workload": "Mistral-7B linears qkv/o_proj/gate_up/down, M in 1,2,4,8,15, per-tensor scales",
+                  "workload": "Mistral-7B linears qkv/o_proj/gate_up/down, M in "
+                              + ",".join(str(m) for m in decode_ms) + ", per-tensor scales",
                   "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
                                "frac_median": round(statistics.median(gbs) / hbm, 4),
                                "peak_source": f"{peak_src} copy bandwidth"},
@@ -714,6 +716,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--m", type=int, default=16384, help="tokens per prefill layer")
     ap.add_argument("--decode-copies", type=int, default=3)
+    ap.add_argument("--decode-ms", type=lambda s: [int(x) for x in s.split(",")], default=None,
+                    help="token counts of the decode leg, comma-separated (default 1,2,4,8,15)")
     ap.add_argument("--cpu-rows", type=int, default=16)
     ap.add_argument("--cpu-cols", type=int, default=512)
     ap.add_argument("--sweep-max-m", type=int, default=16384, help="largest M of the TinyLlama sweep")
