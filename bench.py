@@ -701,7 +701,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (exact product)",
         "data": "synthetic",
-        "config": {"workload": "prefill: Llama-3-8B linears qkv/o_proj/gate_up/down at M=16384, channelwise "
+        "config": {"workload": f"prefill: Llama-3-8B linears qkv/o_proj/gate_up/down at M={M}, channelwise "
                                "weight scales, dynamic per-tensor activation scale (bounded CPU sample)",
                    "M": M, "layers": [[L.name, L.K, L.N] for L in layers]},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": res["cores"], "kind": "oracle",

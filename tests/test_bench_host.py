@@ -38,6 +38,21 @@ def test_reference_arm_on_a_non_zero_rank_exits_quietly():
     assert r.returncode == 0 and r.stdout.strip() == ""
 
 
+def test_reference_arm_line_on_the_host():
+    """The reference arm (the oracle on the host cores, no GPU) prints the contract's line: the
+    metric, a positive value, a cpu_baseline of kind oracle and an e2e entry in the same unit."""
+    r = _run({}, "--impl", "reference", "--steps", "1", "--warmup", "0", "--m", "64", "--cpu-rows", "4",
+             "--cpu-cols", "32")
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["n_gpus"] == 1
+    assert line["value"] > 0 and line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["cpu_baseline"]["cores"] >= 1 and line["cpu_baseline"]["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert line["config"]["M"] == 64 and "M=64" in line["config"]["workload"]
+
+
 def test_roofline_time_takes_the_slower_bound():
     peak_tf, hbm = 3788.0, 6748.7
     # decode: weight stream dominates
