@@ -67,6 +67,7 @@ _SIGNATURES = {
                                       _vp, _sz, _vp]),
     "fp8_gemm_config": (_int, [_vp, _i64, _i64, _vp, _i64, _i64, _i64, _sz, _vp, _vp, _vp, _vp, _vp]),
     "fp8_gemm_plan_model": (_int, [_i64, _i64, _i64, _int, _int, _sz, _vp, _vp, _vp, _vp, _vp]),
+    "fp8_gemv_plan_model": (_int, [_i64, _i64, _i64, _int, _int, _int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "fp8_last_device_status": (_int, [_vp]),
     "fp8_selftest_timeout": (_int, [_i64, _vp]),
     "fp8_status_string": (ctypes.c_char_p, [_int]),
@@ -392,6 +393,21 @@ def fp8_gemm_plan_model(M: int, N: int, K: int, num_sms: int = 152, pair_slots: 
         raise FP8Error(st, "fp8_gemm_plan_model")
     return {"two_sm": bool(two.value), "grid": grid.value, "group_n": gn.value, "splits": sp.value,
             "tail_split": ts.value}
+
+
+def fp8_gemv_plan_model(M: int, N: int, K: int, mode: int, clusters_of_size, smem_limit: int = 227 * 1024,
+                        static_scale: bool = False) -> dict:
+    """The decode GEMV's launch configuration computed on the host (no device): mode 0 activations
+    pre-quantized, 1 quantized in the kernel, 2 bf16 (weight-only); clusters_of_size[s - 1] =
+    co-resident clusters of s CTAs, s = 1..8."""
+    occ = (ctypes.c_int * 8)(*[int(x) for x in clusters_of_size])
+    outs = [ctypes.c_int(0) for _ in range(7)]
+    st = lib().fp8_gemv_plan_model(int(M), int(N), int(K), int(mode), int(bool(static_scale)), int(smem_limit),
+                                   ctypes.cast(occ, ctypes.c_void_p), *[ctypes.byref(o) for o in outs])
+    if st != FP8_OK:
+        raise FP8Error(st, "fp8_gemv_plan_model")
+    keys = ("cluster", "clusters", "stages", "kslice", "scratch_a", "cluster_amax", "tcgen05")
+    return {k: o.value for k, o in zip(keys, outs)}
 
 
 def min_workspace_bytes(M: int, K: int, N: int) -> int:

@@ -307,23 +307,35 @@ bool gemv_tc(int NT, int mode) {
   return NT >= from && mode == gemv::kModePrequant;
 }
 
-fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uint8_t* qw, int64_t ldqw,
-                       cudaStream_t st) {
+// One GEMV launch configuration: cluster size S (K split), clusters C, ring depth, K slice per
+// rank, activation layout and start-up (host logic only).
+struct GemvConfig {
+  bool ok = false;
+  int S = 1, C = 1, stages = gemv::kMinStages, kslice = gemv::kTileK, act_stride = 0, act_rows = 8;
+  int head_tiles = 0, cluster_amax = 0, scratch_a = 0;
+  size_t smem = 0;
+};
+
+// Picks the cluster size S and the number of clusters C so that the CTA with the most work
+// streams as few 16 KB weight tiles as possible, every cluster holds at most kMaxRowBlocks row
+// blocks and the shared memory fits smem_limit; cmax_of(S) gives the co-resident clusters of S
+// CTAs at smem_limit. Then the activation staging (bulk copy of A into idle ring stages when
+// A's rows are 16-byte aligned) and where the dynamic maximum comes from.
+template <typename ClustersOf>
+GemvConfig gemv_configure(int M, int N, int K, int mode, bool tc, bool vec_a, bool static_scale, int smem_limit,
+                          ClustersOf&& cmax_of) {
   using namespace gemv;
-  const int R = (p.N + kRows - 1) / kRows;
-  const int KT = (p.K + kTileK - 1) / kTileK;
+  GemvConfig g;
+  const int R = (N + kRows - 1) / kRows;
+  const int KT = (K + kTileK - 1) / kTileK;
   const bool dyn = mode == kModeQuantize;
   const int max_slice = mode == kModeBf16 ? kMaxSliceBf16 : kMaxSlice;
-  const int NT = p.M <= 8 ? 1 : p.M <= 16 ? 2 : 4;
-  const int act_rows = 8 * NT;
-  const bool tc = gemv_tc(NT, mode);
-  const KernelFn kfn = kernel_for(NT, mode, fmt_a, fmt_w, tc);
-  const int smem_limit = gemv_smem_limit(kfn);
+  const int NT = M <= 8 ? 1 : M <= 16 ? 2 : 4;
+  g.act_rows = 8 * NT;
   auto smem_for = [&](int stg, int act_stride, int nrb) {
-    return size_t(layout(stg, act_stride, act_rows, nrb).total) + 1024;
+    return size_t(layout(stg, act_stride, g.act_rows, nrb).total) + 1024;
   };
-  int best_cost = -1, bS = 1, bC = 1, bstages = kMinStages, bslice = kTileK;
-  size_t bsmem = 0;
+  int best_cost = -1;
   for (int S = 1; S <= kMaxCluster; ++S) {
     if (S > KT) break;
     const int slice_tiles = (KT + S - 1) / S;
@@ -334,7 +346,7 @@ fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uin
     if (smem_for(kMinStages, act_stride, 1) > size_t(smem_limit)) continue;
     // co-resident clusters at the largest shared memory any configuration may take (a lower
     // bound for every configuration, so the grid never runs in waves)
-    const int cmax = gemv_max_clusters(kfn, S, size_t(smem_limit));
+    const int cmax = cmax_of(S);
     if (cmax <= 0) continue;
     int C = std::min(cmax, R);
     const int nrb = (R + C - 1) / C;
@@ -343,7 +355,7 @@ fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uin
     if (smem_for(kMinStages, act_stride, nrb) > size_t(smem_limit)) continue;
     // streamed tiles of the busiest CTA, plus (dynamic mode) its activation prologue: each
     // batch of kRegUnits A loads per consumer thread costs about as much as two weight tiles
-    const int units = p.M * (kslice / 8);
+    const int units = M * (kslice / 8);
     const int batches = dyn ? (units + kRegUnits * kConsumerThreads - 1) / (kRegUnits * kConsumerThreads) : 0;
     const int cost = nrb * slice_tiles + 2 * (batches > 1 ? batches : 0);
     if (best_cost < 0 || cost < best_cost) {
@@ -351,57 +363,78 @@ fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uin
       int stg = kMinStages;
       while (stg < kMaxStages && smem_for(stg + 1, act_stride, nrb) <= size_t(smem_limit)) ++stg;
       best_cost = cost;
-      bS = S;
-      bC = C;
-      bstages = stg;
-      bslice = kslice;
-      bsmem = smem_for(stg, act_stride, nrb);
+      g.S = S;
+      g.C = C;
+      g.stages = stg;
+      g.kslice = kslice;
+      g.smem = smem_for(stg, act_stride, nrb);
     }
   }
-  if (best_cost < 0) {
-    report_cuda(cudaErrorInvalidConfiguration, "no GEMV configuration fits");
-    return FP8_ERR_CUDA;
-  }
-  p.kslice = bslice;
-  p.act_stride = gemv_act_stride(mode, bslice, tc);
-  p.act_rows = act_rows;
-  p.head_tiles = gemv_head_tiles();
+  if (best_cost < 0) return g;
+  g.ok = true;
+  g.act_stride = gemv_act_stride(mode, g.kslice, tc);
+  g.head_tiles = gemv_head_tiles();
   // dynamic scale: every CTA reads all of A when that is at most two load batches per thread
   // (no cluster exchange on the critical path); larger A exchanges the ranks' slice maxima
-  const int64_t units_all = int64_t(p.M) * ((p.K + 7) / 8);
-  p.cluster_amax = (bS > 1 && units_all > 2 * kRegUnits * kConsumerThreads) ? 1 : 0;
-  if (bS == 1) p.cluster_amax = 1;  // one rank: its slice is all of A
+  const int64_t units_all = int64_t(M) * ((K + 7) / 8);
+  g.cluster_amax = (g.S > 1 && units_all > 2 * kRegUnits * kConsumerThreads) ? 1 : 0;
+  if (g.S == 1) g.cluster_amax = 1;  // one rank: its slice is all of A
   // quantize mode with row-aligned A: bulk-copy A (all of it for the dynamic maximum when it
   // fits, else this rank's slice) into the ring stages that stay idle until the stream is
   // released, so the prologue reads it from shared memory with no per-thread round trips
   // (the head shrinks, down to one tile, when that makes the copy fit)
-  p.scratch_a = 0;
-  if (mode == kModeQuantize && p.vec_a && p.K % 8 == 0) {
+  g.scratch_a = 0;
+  if (mode == kModeQuantize && vec_a && K % 8 == 0) {
     auto head_for = [&](int64_t bytes) {  // largest head <= the default that leaves `bytes` free
       const int64_t slots = (bytes + kTileBytes - 1) / kTileBytes;
-      return int(std::min<int64_t>(p.head_tiles, bstages - slots));
+      return int(std::min<int64_t>(g.head_tiles, g.stages - slots));
     };
-    const int64_t full_bytes = int64_t(p.M) * p.K * 2;
-    const int64_t slice_bytes = int64_t(p.M) * bslice * 2;
-    if (p.s_static != nullptr) {
-      if (head_for(slice_bytes) >= 1) { p.scratch_a = 2; p.head_tiles = head_for(slice_bytes); }
+    const int64_t full_bytes = int64_t(M) * K * 2;
+    const int64_t slice_bytes = int64_t(M) * g.kslice * 2;
+    if (static_scale) {
+      if (head_for(slice_bytes) >= 1) { g.scratch_a = 2; g.head_tiles = head_for(slice_bytes); }
     } else if (!gemv_slice_only() && head_for(full_bytes) >= 1) {
-      p.scratch_a = 1;
-      p.head_tiles = head_for(full_bytes);
-      p.cluster_amax = 0;
+      g.scratch_a = 1;
+      g.head_tiles = head_for(full_bytes);
+      g.cluster_amax = 0;
     } else if (head_for(slice_bytes) >= 1) {
-      p.scratch_a = 2;
-      p.head_tiles = head_for(slice_bytes);
-      p.cluster_amax = 1;
+      g.scratch_a = 2;
+      g.head_tiles = head_for(slice_bytes);
+      g.cluster_amax = 1;
     }
   }
-  p.stages = bstages;
-  p.row_blocks = R;
-  p.num_clusters = bC;
+  return g;
+}
+
+fp8_status launch_gemv(gemv::Params p, int mode, int fmt_a, int fmt_w, const uint8_t* qw, int64_t ldqw,
+                       cudaStream_t st) {
+  using namespace gemv;
+  const int NT = p.M <= 8 ? 1 : p.M <= 16 ? 2 : 4;
+  const int act_rows = 8 * NT;
+  const bool tc = gemv_tc(NT, mode);
+  const KernelFn kfn = kernel_for(NT, mode, fmt_a, fmt_w, tc);
+  const int smem_limit = gemv_smem_limit(kfn);
+  const GemvConfig g = gemv_configure(p.M, p.N, p.K, mode, tc, p.vec_a != 0, p.s_static != nullptr, smem_limit,
+                                      [&](int S) { return gemv_max_clusters(kfn, S, size_t(smem_limit)); });
+  if (!g.ok) {
+    report_cuda(cudaErrorInvalidConfiguration, "no GEMV configuration fits");
+    return FP8_ERR_CUDA;
+  }
+  p.kslice = g.kslice;
+  p.act_stride = g.act_stride;
+  p.act_rows = g.act_rows;
+  p.head_tiles = g.head_tiles;
+  p.cluster_amax = g.cluster_amax;
+  p.scratch_a = g.scratch_a;
+  p.stages = g.stages;
+  p.row_blocks = (p.N + kRows - 1) / kRows;
+  p.num_clusters = g.C;
+  const int bS = g.S, bC = g.C;
+  const size_t bsmem = g.smem;
   static const bool debug = std::getenv("FP8W8A8_DEBUG") != nullptr;
   if (debug)
     std::fprintf(stderr, "fp8w8a8: gemv M=%d N=%d K=%d mode=%d cluster=%d clusters=%d stages=%d kslice=%d smem=%zu "
-                 "scratch=%d cluster_amax=%d\n", p.M, p.N, p.K, mode, bS, bC, bstages, bslice, bsmem, p.scratch_a,
+                 "scratch=%d cluster_amax=%d\n", p.M, p.N, p.K, mode, bS, bC, g.stages, g.kslice, bsmem, p.scratch_a,
                  p.cluster_amax);
   CUtensorMap map, amap;
   if (!make_fp8_tensor_map(&map, qw, p.N, p.K, ldqw, kRows)) return FP8_ERR_CUDA;
@@ -802,6 +835,27 @@ FP8_API fp8_status fp8_gemm_config(const uint8_t* qa, int64_t M, int64_t ldqa, c
     S = fp8k::gemm_split_plan(qa, ldqa, qw, ldqw, int(M), int(N), int(K), sms, probe, ws_bytes - split_off).splits;
   }
   report_plan(pl, S, sms, two_sm, grid, group_n, splits, tail_split);
+  return FP8_OK;
+}
+
+FP8_API fp8_status fp8_gemv_plan_model(int64_t M, int64_t N, int64_t K, int mode, int static_scale, int smem_limit,
+                                       const int* clusters_of_size, int* cluster, int* clusters, int* stages,
+                                       int* kslice, int* scratch_a, int* cluster_amax, int* tcgen05) {
+  if (M <= 0 || M > gemv::kMaxTokens || N <= 0 || N > kMaxDim || K <= 0 || K > kGemvMaxK || mode < 0 || mode > 2 ||
+      smem_limit <= 0 || clusters_of_size == nullptr)
+    return FP8_ERR_INVALID_ARG;
+  const int NT = M <= 8 ? 1 : M <= 16 ? 2 : 4;
+  const bool tc = gemv_tc(NT, mode);
+  const GemvConfig g = gemv_configure(int(M), int(N), int(K), mode, tc, true, static_scale != 0, smem_limit,
+                                      [&](int S) { return clusters_of_size[S - 1]; });
+  if (!g.ok) return FP8_ERR_CUDA;
+  if (cluster) *cluster = g.S;
+  if (clusters) *clusters = g.C;
+  if (stages) *stages = g.stages;
+  if (kslice) *kslice = g.kslice;
+  if (scratch_a) *scratch_a = g.scratch_a;
+  if (cluster_amax) *cluster_amax = g.cluster_amax;
+  if (tcgen05) *tcgen05 = tc ? 1 : 0;
   return FP8_OK;
 }
 

@@ -329,6 +329,23 @@ fp8_status fp8_gemm_config(const uint8_t* qa, int64_t M, int64_t ldqa, const uin
 fp8_status fp8_gemm_plan_model(int64_t M, int64_t N, int64_t K, int num_sms, int pair_slots, size_t ws_bytes,
                                int* two_sm, int* grid, int* group_n, int* splits, int* tail_split);
 
+/* The decode GEMV's launch configuration, computed on the host without a device ("[WIP] FP8
+ * support": the decode GEMV). mode: 0 activations already quantized (fp8_scaled_mm, and
+ * fp8_linear from 17 tokens on), 1 quantized inside the kernel (fp8_linear up to 16 tokens;
+ * static_scale != 0 for fp8_linear_static), 2 bf16 activations (weight-only). smem_limit:
+ * dynamic shared memory a CTA may use; clusters_of_size[s - 1]: co-resident clusters of s CTAs
+ * at that shared memory, s = 1..8 (host memory, 8 ints). Outputs (NULL allowed): *cluster = CTAs
+ * per cluster sharing K, *clusters = clusters launched, *stages = weight-ring depth, *kslice =
+ * bytes of K per CTA, *scratch_a = how A reaches shared memory in mode 1 (0 per-thread loads,
+ * 1 all of A bulk-copied, 2 the CTA's slice), *cluster_amax = 1 when the dynamic maximum is
+ * exchanged over the cluster, *tcgen05 = 1 when the main loop runs on tcgen05. A's rows are
+ * taken as 16-byte aligned. FP8_ERR_INVALID_ARG for M outside 1..32, K outside 1..32768, other
+ * bad sizes or mode; FP8_ERR_CUDA when no configuration fits (the launch would fail the same
+ * way). Host-only, never touches the device. */
+fp8_status fp8_gemv_plan_model(int64_t M, int64_t N, int64_t K, int mode, int static_scale, int smem_limit,
+                               const int* clusters_of_size, int* cluster, int* clusters, int* stages, int* kslice,
+                               int* scratch_a, int* cluster_amax, int* tcgen05);
+
 /*
  * Synchronizes `stream`, then reports and clears device-side errors recorded
  * by the library's kernels on the current device since the last query
